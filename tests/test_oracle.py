@@ -1,0 +1,331 @@
+"""Pins of the f64 oracle against facts fixed outside it (CPU only).
+
+Each test pins one part of the oracle to something other than the oracle:
+hand-worked format blocks, exhaustive comparison with numpy/torch format
+conversions, identity and one-hot weights, the closed-form probe printed in
+wavo's ``probe_tensor``, exact integer brute force, textbook erf-GELU values,
+and closed forms of the MoE routing.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from conftest import golden_lines
+
+BF16, Q8_0, Q4_0 = synth.WTYPE_BF16, synth.WTYPE_Q8_0, synth.WTYPE_Q4_0
+BIAS, GELU, RESIDUAL = synth.FLAG_BIAS, synth.FLAG_GELU, synth.FLAG_RESIDUAL
+
+
+# ----------------------------------------------------------------- formats --
+
+def test_half_hand_values(oracle_mod):
+    o = oracle_mod
+    assert o.half_to_f64(0x3C00) == 1.0
+    assert o.half_to_f64(0xC000) == -2.0
+    assert o.half_to_f64(0x2000) == 2.0 ** -7
+    assert o.half_to_f64(0x0001) == 2.0 ** -24
+    assert o.half_to_f64(0x03FF) == 1023 * 2.0 ** -24
+    assert o.half_to_f64(0x0400) == 2.0 ** -14
+    assert o.half_to_f64(0x7BFF) == 65504.0
+    assert o.half_to_f64(0x3555) == 0.333251953125
+    z = o.half_to_f64(0x8000)
+    assert z == 0.0 and np.signbit(z)
+    assert o.half_to_f64(0x7C00) == np.inf and o.half_to_f64(0xFC00) == -np.inf
+    assert np.isnan(o.half_to_f64(0x7E00))
+
+
+def test_half_exhaustive_vs_numpy(oracle_mod):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle_mod.half_to_f64(int(b)) for b in bits])
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+    assert (np.signbit(got) == np.signbit(want)).all()
+
+
+def test_bf16_exhaustive_vs_torch(oracle_mod):
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.int32)
+    t = torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16)
+    want = t.to(torch.float64).numpy()
+    got = np.array([oracle_mod.bf16_to_f64(int(b)) for b in bits])
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+
+
+def test_bf16_pair_words(oracle_mod):
+    """Hand-decoded pair words: low half = even k, high half = odd k."""
+    for line in golden_lines("bf16_pairs.txt"):
+        word_hex, lo, hi = line.split()
+        word = int(word_hex, 16)
+        img = np.frombuffer(np.array([word], dtype="<u4").tobytes(), dtype=np.uint8)
+        w = oracle_mod.dequant(BF16, 1, 2, img.reshape(1, 4))
+        assert w[0, 0] == float(lo) and w[0, 1] == float(hi), line
+        assert np.signbit(w[0, 0]) == np.signbit(float(lo))
+        assert np.signbit(w[0, 1]) == np.signbit(float(hi))
+
+
+def test_q4_0_hand_blocks(oracle_mod):
+    lines = golden_lines("q4_0_block.txt")
+    pairs = [(lines[i], lines[i + 1]) for i in range(0, len(lines), 2)]
+    assert len(pairs) == 2
+    for b_line, v_line in pairs:
+        blk = np.array([int(x, 16) for x in b_line.split(":")[1].split()], dtype=np.uint8)
+        want = np.array([float(x) for x in v_line.split(":")[1].split()])
+        assert blk.size == 18 and want.size == 32
+        got = oracle_mod.dequant(Q4_0, 1, 32, blk.reshape(1, 18))[0]
+        assert (got == want).all(), (got, want)
+
+
+def test_q8_0_hand_blocks(oracle_mod):
+    lines = golden_lines("q8_0_block.txt")
+    codes = [int(x) for x in lines[0].split(":")[1].split()]
+    assert len(codes) == 32
+    scales = [ln.split(":")[1].split() for ln in lines[1:]]
+    assert len(scales) == 4
+    for bits_hex, unit in scales:
+        bits = int(bits_hex, 16)
+        blk = np.array([bits & 0xFF, bits >> 8] + [c & 0xFF for c in codes], dtype=np.uint8)
+        got = oracle_mod.dequant(Q8_0, 1, 32, blk.reshape(1, 34))[0]
+        want = np.array([float(unit) * c for c in codes])
+        assert (got == want).all(), bits_hex
+
+
+def test_q8_0_exhaustive_codes(oracle_mod):
+    """All 256 codes under a power-of-two scale, across 8 blocks of two rows."""
+    codes = np.arange(-128, 128, dtype=np.int16).astype(np.int8).reshape(2, 128)
+    d = np.full((2, 4), 0x3400, dtype=np.uint16)  # 0.25
+    img = synth.encode_q8_0(d, codes)
+    got = oracle_mod.dequant(Q8_0, 2, 128, img)
+    assert (got == codes.astype(np.float64) * 0.25).all()
+
+
+def test_q4_0_all_nibbles_every_position(oracle_mod):
+    """Every code at every in-block position; a swapped nibble order fails."""
+    q4 = (np.arange(32)[None, :] + np.arange(16)[:, None]) % 16
+    d = np.full((16, 1), 0x4000, dtype=np.uint16)  # 2.0
+    img = synth.encode_q4_0(d, q4.astype(np.uint8))
+    got = oracle_mod.dequant(Q4_0, 16, 32, img)
+    assert (got == 2.0 * (q4 - 8)).all()
+
+
+def test_round_bf16(oracle_mod):
+    r = oracle_mod.round_bf16
+    assert r(1.0 + 2.0 ** -8) == 1.0                      # tie -> even (down)
+    assert r(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6      # tie -> even (up)
+    assert r(1.0 + 2.0 ** -8 + 2.0 ** -20) == 1.0 + 2.0 ** -7
+    assert r(-(1.0 + 2.0 ** -8)) == -1.0
+    assert r(3.4e38) == np.inf
+    assert r(2.0 ** -140) == 0.0 or r(2.0 ** -140) == 2.0 ** -133 * round(2.0 ** -7)
+    g = np.random.default_rng(7)
+    x = np.concatenate([g.standard_normal(20000).astype(np.float32),
+                        (g.standard_normal(2000) * 1e-39).astype(np.float32),
+                        (g.standard_normal(2000) * 1e30).astype(np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([r(float(v)) for v in x])
+    assert (got == want).all()
+
+
+# ------------------------------------------------------------- contraction --
+
+def _identity_image(wtype, k, one_code=None):
+    """W = I (k x k) in the given format; exact value 1.0 on the diagonal."""
+    if wtype == BF16:
+        bits = np.zeros((k, k), dtype=np.uint16)
+        np.fill_diagonal(bits, 0x3F80)
+        return synth.bf16_pairs(bits)
+    d = np.full((k, k // 32), 0x3C00, dtype=np.uint16)
+    if wtype == Q8_0:
+        q = np.zeros((k, k), dtype=np.int8)
+        np.fill_diagonal(q, 1)
+        return synth.encode_q8_0(d, q)
+    q = np.full((k, k), 8, dtype=np.uint8)
+    np.fill_diagonal(q, 9)
+    return synth.encode_q4_0(d, q)
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+def test_identity_weights(oracle_mod, wtype):
+    k, n = 96, 5
+    X = synth.normal_f32(synth.rng(11), (n, k))
+    Y, S = oracle_mod.gemm(n, k, k, wtype, 0, X, _identity_image(wtype, k))
+    assert (Y == X.astype(np.float64)).all()
+    assert (S == np.abs(X).astype(np.float64)).all()
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+def test_wavo_probe_closed_form(oracle_mod, wtype):
+    """The printed probe of wavo's tensor GEMM: c[r][j] = j % 32 + r % 32."""
+    cfg = dict(ln.split(":") for ln in golden_lines("wavo_probe.txt"))
+    n, m, k = int(cfg["n"]), int(cfg["m"]), int(cfg["k"])
+    a = np.array([[x + r % 32 for x in range(k)] for r in range(n)], dtype=np.float32)
+    onehot = np.array([[1 if x == j % 32 else 0 for x in range(k)] for j in range(m)])
+    if wtype == BF16:
+        img = synth.bf16_pairs(np.where(onehot == 1, 0x3F80, 0).astype(np.uint16))
+    elif wtype == Q8_0:
+        img = synth.encode_q8_0(np.full((m, 1), 0x3C00, np.uint16), onehot.astype(np.int8))
+    else:
+        img = synth.encode_q4_0(np.full((m, 1), 0x3C00, np.uint16), (onehot + 8).astype(np.uint8))
+    Y, _ = oracle_mod.gemm(n, m, k, wtype, BIAS, a, img, bias=np.zeros(m, np.float32))
+    want = np.array([[j % 32 + r % 32 for j in range(m)] for r in range(n)], dtype=np.float64)
+    assert (Y == want).all()
+
+
+def _exact_case(g, wtype, n, m, k):
+    """Random small-integer inputs whose every product and sum is exact in f64."""
+    X = g.integers(-3, 4, size=(n, k)).astype(np.float32)
+    nb = k // 32
+    if wtype == BF16:
+        wv = g.integers(-8, 9, size=(m, k)) * 0.5  # exact in bf16
+        img = synth.bf16_pairs(synth.bf16_bits_rne(wv.astype(np.float32)))
+        Wf = [[Fraction(v) for v in row] for row in wv]
+    else:
+        exps = g.integers(-3, 3, size=(m, nb))
+        sign = g.choice([-1, 1], size=(m, nb))
+        dval = sign * np.ldexp(1.0, exps)
+        dbits = synth.f16_bits(dval)
+        if wtype == Q8_0:
+            q = g.integers(-128, 128, size=(m, k)).astype(np.int8)
+            img = synth.encode_q8_0(dbits, q)
+            Wf = [[Fraction(dval[j, t // 32]) * int(q[j, t]) for t in range(k)] for j in range(m)]
+        else:
+            q4 = g.integers(0, 16, size=(m, k)).astype(np.uint8)
+            img = synth.encode_q4_0(dbits, q4)
+            Wf = [[Fraction(dval[j, t // 32]) * (int(q4[j, t]) - 8) for t in range(k)]
+                  for j in range(m)]
+    return X, img, Wf
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("shape", [(1, 3, 32), (3, 5, 64), (7, 2, 96), (4, 33, 32)])
+def test_exact_integer_brute_force(oracle_mod, wtype, shape):
+    """Exact rational arithmetic on the intended values (not on the byte image)."""
+    n, m, k = shape
+    g = np.random.default_rng(1000 * wtype + 10 * n + m)
+    X, img, Wf = _exact_case(g, wtype, n, m, k)
+    bias = g.integers(-4, 5, size=m).astype(np.float32)
+    R = g.integers(-4, 5, size=(n, m)).astype(np.float32)
+    for flags in (0, BIAS, RESIDUAL, BIAS | RESIDUAL):
+        Y, S = oracle_mod.gemm(n, m, k, wtype, flags, X, img, bias=bias, residual=R)
+        for i in range(n):
+            for j in range(m):
+                acc = sum(Fraction(float(X[i, t])) * Wf[j][t] for t in range(k))
+                s = sum(abs(Fraction(float(X[i, t])) * Wf[j][t]) for t in range(k))
+                if flags & BIAS:
+                    acc += Fraction(float(bias[j]))
+                if flags & RESIDUAL:
+                    acc += Fraction(float(R[i, j]))
+                assert Y[i, j] == float(acc), (flags, i, j)
+                assert S[i, j] == float(s)
+
+
+def test_gelu_closed_forms(oracle_mod):
+    pts = [tuple(float(v) for v in ln.split()) for ln in golden_lines("gelu_points.txt")]
+    for v, want in pts:
+        got = oracle_mod.gelu(v)
+        assert abs(got - want) <= 2e-16 * max(1.0, abs(want)), (v, got, want)
+    for v in np.linspace(-6, 6, 241):
+        assert abs((oracle_mod.gelu(v) - oracle_mod.gelu(-v)) - v) <= 4e-16 * max(1, abs(v))
+
+
+def test_gelu_through_gemm_and_scipy(oracle_mod):
+    from scipy.special import erf
+    k = 32
+    v = np.linspace(-5, 5, 64).astype(np.float32).reshape(2, k)
+    Y, _ = oracle_mod.gemm(2, k, k, Q8_0, GELU, v, _identity_image(Q8_0, k))
+    want = 0.5 * v.astype(np.float64) * (1 + erf(v.astype(np.float64) / np.sqrt(2.0)))
+    # 1 + erf(.) cancels in the left tail: compare on the scale of |v|.
+    assert (np.abs(Y - want) <= 1e-15 * np.maximum(1.0, np.abs(v))).all()
+
+
+def test_epilogue_order(oracle_mod):
+    """bias -> GELU -> residual, as cortiq-engine's ae_put orders them."""
+    k = 32
+    X = np.ones((1, k), np.float32)
+    Y, _ = oracle_mod.gemm(1, k, k, Q4_0, BIAS | GELU | RESIDUAL, X, _identity_image(Q4_0, k),
+                           bias=np.ones(k, np.float32), residual=np.ones((1, k), np.float32))
+    want = 1.9544997361036416 + 1.0  # gelu(1 + 1) + 1
+    assert np.allclose(Y, want, rtol=1e-15)
+
+
+@pytest.mark.parametrize("wtype", [Q8_0, Q4_0])
+def test_zero_weights_residual(oracle_mod, wtype):
+    n, m, k = 3, 7, 64
+    d = np.full((m, k // 32), 0x3C00, np.uint16)
+    img = (synth.encode_q8_0(d, np.zeros((m, k), np.int8)) if wtype == Q8_0
+           else synth.encode_q4_0(d, np.full((m, k), 8, np.uint8)))
+    g = synth.rng(3)
+    X, R, b = synth.normal_f32(g, (n, k)), synth.normal_f32(g, (n, m)), synth.normal_f32(g, (m,))
+    Y, S = oracle_mod.gemm(n, m, k, wtype, BIAS | RESIDUAL, X, img, bias=b, residual=R)
+    assert (Y == (b[None, :].astype(np.float64) + R.astype(np.float64))).all()
+    assert (S == 0).all()
+
+
+def test_row_range_and_threads(oracle_mod):
+    w = synth.workload_q8_0_gemv(n=2, m=96, k=128)
+    Y1, S1 = oracle_mod.gemm(2, 96, 128, Q8_0, 0, w["X"], w["W"], threads=1)
+    Y2, S2 = oracle_mod.gemm(2, 96, 128, Q8_0, 0, w["X"], w["W"], threads=4)
+    assert (Y1 == Y2).all() and (S1 == S2).all()
+    Y3, _ = oracle_mod.gemm(2, 96, 128, Q8_0, 0, w["X"], w["W"], rows=(10, 20))
+    assert (Y3[:, 10:20] == Y1[:, 10:20]).all() and np.isnan(Y3[:, :10]).all()
+
+
+def test_round_x_feeds_bf16_rounded_inputs(oracle_mod):
+    """round_x=True equals feeding torch-rounded X (library RNE) with round_x=False."""
+    w = synth.workload_bf16_gemm(n=4, m=40, k=64)
+    Xr = torch.from_numpy(w["X"]).to(torch.bfloat16).to(torch.float32).numpy()
+    Ya, _ = oracle_mod.gemm(4, 40, 64, BF16, 3, w["X"], w["W"], bias=w["bias"], round_x=True)
+    Yb, _ = oracle_mod.gemm(4, 40, 64, BF16, 3, Xr, w["W"], bias=w["bias"])
+    assert (Ya == Yb).all()
+
+
+def test_bad_arguments(oracle_mod):
+    img = np.zeros((2, 34), np.uint8)
+    with pytest.raises(ValueError):
+        oracle_mod.gemm(1, 2, 40, Q8_0, 0, np.zeros((1, 40), np.float32), img)
+    with pytest.raises(ValueError):
+        oracle_mod.gemm(1, 2, 32, Q8_0, BIAS, np.zeros((1, 32), np.float32), img)
+
+
+# ------------------------------------------------------------------- MoE --
+
+def test_moe_scaled_identity_routing(oracle_mod):
+    """Expert e = (e+1)*2^-6 * I, so Y[t][s] = (ids[t][s]+1)*2^-6 * X[t] exactly."""
+    E, k, n_tok, topk = 8, 64, 5, 3
+    imgs = []
+    for e in range(E):
+        d = np.full((k, k // 32), synth.f16_bits((e + 1) * 2.0 ** -6)[()], np.uint16)
+        q = np.zeros((k, k), np.int8)
+        np.fill_diagonal(q, 1)
+        imgs.append(synth.encode_q8_0(d, q))
+    bank = np.stack(imgs)
+    g = synth.rng(5)
+    X = synth.normal_f32(g, (n_tok, k))
+    ids = synth.moe_ids(g, n_tok, topk, E)
+    Y, _ = oracle_mod.moe(n_tok, topk, E, k, k, Q8_0, 0, X, bank, ids)
+    for t in range(n_tok):
+        for s in range(topk):
+            want = (ids[t, s] + 1) * 2.0 ** -6 * X[t].astype(np.float64)
+            assert (Y[t * topk + s] == want).all()
+
+
+def test_moe_bias_per_expert_and_bad_id(oracle_mod):
+    E, m, k = 3, 4, 32
+    d = np.full((E * m, 1), 0x3C00, np.uint16)
+    bank = synth.encode_q4_0(d, np.full((E * m, k), 8, np.uint8)).reshape(E, m, -1)  # W = 0
+    bias = np.arange(E * m, dtype=np.float32).reshape(E, m)
+    ids = np.array([[2, 0], [1, 2]], np.int32)
+    X = np.ones((2, k), np.float32)
+    Y, _ = oracle_mod.moe(2, 2, E, m, k, Q4_0, BIAS, X, bank, ids, bias=bias)
+    for q, e in enumerate(ids.reshape(-1)):
+        assert (Y[q] == bias[e]).all()
+    with pytest.raises(ValueError):
+        oracle_mod.moe(2, 2, E, m, k, Q4_0, 0, X, bank, np.array([[0, 3], [1, 2]], np.int32))
+
+
+def test_synth_ids_distinct_and_in_range():
+    ids = synth.moe_ids(synth.rng(5), 16, 6, 64)
+    assert ids.shape == (16, 6) and ids.min() >= 0 and ids.max() < 64
+    assert all(len(set(row)) == 6 for row in ids.tolist())
