@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""Benchmark of the weight-format GEMM/GEMV path on GB300.
+
+One *step* is one pass of the whole hot path over the five workloads, nine
+launches through the C ABI:
+    bf16 GEMM n=32 (bias+GELU) | Q8_0 GEMV n=1 | Q4_0 GEMV n=1, 4, 8 (+residual) |
+    encoder bf16 GEMMs n=1500 qkv/up/down on the tensor cores | MoE Q4_0 routed GEMV.
+The metric is the step's fraction of its roofline: sum over launches of
+max(algorithmic bytes / HBM peak, flops / bf16 tensor peak), divided by the
+measured step time.  Peaks are the measured ones in MEASURED_PEAKS.json.
+
+Timing: inputs resident in HBM; two rotating input sets (a step touches
+~340 MB, so every buffer is re-read only after ~680 MB, > 5x the 129 MB L2);
+each step is a CUDA graph of the nine launches with a timing event between
+launches; K steps are replayed back to back between a barrier + synchronize and
+timed with CUDA events; per-launch durations come from the events of the last
+min(K, 64) steps of that timed region.  `e2e` times the same steps driven from
+the host through the Python binding, with the activations copied from pinned
+host memory before and the outputs copied back after every step.
+
+`--impl reference` times the f64 CPU oracle (the only independent
+implementation of this path; the pages' wgpu kernels cannot run here) on a
+bounded sample of the same workloads.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMV HBM GB/s and GEMM TFLOP/s at 1 GB300, as % of roofline"
+UNIT = "% of roofline"
+N_EVENT_GRAPHS = 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def timing_event(torch):
+    """A timing event whose record inside stream capture becomes a real event
+    record node (torch >= 2.7 spells this `external=True`)."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured (MEASURED_PEAKS.json, burst)"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ------------------------------------------------------------------ workloads --
+
+def make_workloads():
+    import synth
+    ws = [synth.workload_bf16_gemm(), synth.workload_q8_0_gemv()]
+    ws += [synth.workload_q4_0_gemv(n=n) for n in (1, 4, 8)]
+    ws += synth.workload_encoder_gemms()
+    ws.append(synth.workload_moe())
+    return ws
+
+
+def algorithmic(w):
+    """(bytes, flops) of one launch: every weight byte touched once, X read once,
+    Y written once, bias and residual read when flagged, ids read once."""
+    import synth
+    k, m = w["k"], w["m"]
+    rb = synth.weight_bytes(w["wtype"], 1, k)
+    if w["kind"] == "moe":
+        slots = w["n_tok"] * w["topk"]
+        touched = len(set(w["ids"].reshape(-1).tolist()))
+        b = touched * m * rb + w["n_tok"] * k * 4 + slots * m * 4 + slots * 4
+        return b, 2.0 * slots * m * k
+    n = w["n"]
+    b = m * rb + n * k * 4 + n * m * 4
+    if w["flags"] & synth.FLAG_BIAS:
+        b += m * 4
+    if w["flags"] & synth.FLAG_RESIDUAL:
+        b += n * m * 4
+    return b, 2.0 * n * m * k
+
+
+def roofline_us(w, peaks):
+    b, f = algorithmic(w)
+    t_hbm = b / (peaks["hbm_gbs"] * 1e9) * 1e6
+    t_tc = f / (peaks["bf16_tflops"] * 1e12) * 1e6
+    return max(t_hbm, t_tc), ("tensor" if t_tc > t_hbm else "hbm")
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="wq_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------- distributed --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def max_over_ranks(x, world, device=None):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ CPU baseline --
+
+def oracle_step_seconds(ws, frac, threads=0):
+    """Oracle time of one step restricted to the first ceil(frac * m) output rows
+    (W rows) of every launch; returns (seconds, rows per workload)."""
+    import oracle
+    rows = []
+    t0 = time.perf_counter()
+    for w in ws:
+        r = max(1, int(np.ceil(frac * w["m"])))
+        rows.append(r)
+        if w["kind"] == "moe":
+            slots = w["n_tok"] * w["topk"]
+            q = max(1, int(np.ceil(frac * slots)))
+            oracle.moe(w["n_tok"], w["topk"], w["n_experts"], w["m"], w["k"], w["wtype"],
+                       w["flags"], w["X"], w["W"], w["ids"], slots=(0, q), threads=threads,
+                       bound=False)
+        else:
+            oracle.gemm(w["n"], w["m"], w["k"], w["wtype"], w["flags"], w["X"], w["W"],
+                        bias=w["bias"], residual=w["residual"],
+                        round_x=(w["kind"] == "gemm_tc"), rows=(0, r), threads=threads,
+                        bound=False)
+    return time.perf_counter() - t0, rows
+
+
+def cpu_baseline(ws, peaks, budget_s=12.0):
+    """The oracle as it stands, all host cores, on a bounded sample of one step."""
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    roof = sum(roofline_us(w, peaks)[0] for w in ws)
+    frac = 1.0 / 256
+    t, _ = oracle_step_seconds(ws, frac)
+    # Grow the sample toward ~budget/3 seconds per timing, then take the median of 3.
+    frac = min(1.0, frac * max(1.0, (budget_s / 3) / max(t, 1e-3)))
+    times = [oracle_step_seconds(ws, frac)[0] for _ in range(3)]
+    t_step = float(np.median(times)) / frac
+    return {"value": roof / (t_step * 1e6) * 100.0, "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"first {frac:.4%} of the output rows of every launch of one step "
+                      f"(MoE: of the routed slots), median of 3, scaled to a full step; "
+                      f"full-step estimate {t_step:.2f} s"}
+
+
+# ------------------------------------------------------------ reference arm --
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    peaks = load_peaks()
+    ws = make_workloads()
+    roof = sum(roofline_us(w, peaks)[0] for w in ws)
+    # Size each step's sample so the whole run takes about two minutes.
+    probe = 1.0 / 512
+    t, _ = oracle_step_seconds(ws, probe)
+    per_step = min(0.5, 120.0 / max(1, args.steps + args.warmup))
+    frac = min(1.0, probe * max(1e-3, per_step / max(t, 1e-6)))
+    for _ in range(args.warmup):
+        oracle_step_seconds(ws, frac)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step_seconds(ws, frac)
+    el = time.perf_counter() - t0
+    t_step = el / args.steps / frac  # seconds of one full step
+    value = roof / (t_step * 1e6) * 100.0
+    cores = oracle.max_threads()
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference",
+           "config": {"workload": "bf16 GEMM n32 + Q8_0 GEMV + Q4_0 GEMV n1/4/8 + encoder "
+                                  "GEMMs n1500 + MoE Q4_0 E64 top6", "parallelism": "host cores"},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                            "sample": f"each step: first {frac:.4%} of the output rows of "
+                                      "every launch, scaled to a full step"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm --
+
+class Launches:
+    """Device buffers of one input set and the nine C-ABI calls of one step."""
+
+    def __init__(self, ws, wq, torch, device):
+        self.ws = ws
+        self.bufs = []
+        for w in ws:
+            b = {}
+            m, k = w["m"], w["k"]
+            rows_w = m * (w["n_experts"] if w["kind"] == "moe" else 1)
+            need = wq.wq_weight_bytes(w["wtype"], rows_w, k)
+            img = np.zeros(need, np.uint8)
+            flat = np.ascontiguousarray(w["W"]).reshape(-1)
+            img[:flat.size] = flat
+            b["W"] = torch.from_numpy(img).to(device)
+            b["X"] = torch.from_numpy(w["X"]).to(device)
+            nout = (w["n_tok"] * w["topk"] if w["kind"] == "moe" else w["n"]) * m
+            b["Y"] = torch.empty(nout, dtype=torch.float32, device=device)
+            b["bias"] = torch.from_numpy(w["bias"]).to(device) if w["bias"] is not None else None
+            b["R"] = (torch.from_numpy(w["residual"]).to(device)
+                      if w["residual"] is not None else None)
+            b["ids"] = torch.from_numpy(w["ids"]).to(device) if w["kind"] == "moe" else None
+            self.bufs.append(b)
+        self.wq = wq
+
+    def call(self, i, stream=None):
+        w, b, wq = self.ws[i], self.bufs[i], self.wq
+        if w["kind"] == "moe":
+            return wq.wq_moe_gemv(w["n_tok"], w["topk"], w["n_experts"], w["m"], w["k"],
+                                  w["wtype"], w["flags"], b["X"], b["W"], b["ids"], b["bias"],
+                                  b["R"], b["Y"], stream)
+        fn = wq.wq_gemv if w["kind"] == "gemv" else wq.wq_gemm
+        flags = w["flags"] | (wq.WQ_TC_BF16 if w["kind"] == "gemm_tc" else 0)
+        return fn(w["n"], w["m"], w["k"], w["wtype"], flags, b["X"], b["W"], b["bias"], b["R"],
+                  b["Y"], stream)
+
+    def step(self, stream=None):
+        for i in range(len(self.ws)):
+            st = self.call(i, stream)
+            if st != 0:
+                raise RuntimeError(f"{self.ws[i]['name']}: {self.wq.wq_status_string(st)}")
+
+
+def per_launch_fallback(sets, nl, torch, reps=50):
+    """Average duration of each launch, timed with events around `reps`
+    back-to-back launches of it (used only when graph timing events are missing)."""
+    out = np.zeros(nl)
+    for i in range(nl):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for r in range(reps):
+            sets[r % 2].call(i)
+        e1.record()
+        torch.cuda.synchronize()
+        out[i] = e0.elapsed_time(e1) * 1e3 / reps
+    return out
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from gemv_transformer_gb300 import build
+    build.build()
+    import gemv_transformer_gb300 as wq
+    wq.load()
+
+    peaks = load_peaks()
+    ws = make_workloads()
+    sets = [Launches(ws, wq, torch, device) for _ in range(2)]
+    stream = torch.cuda.Stream(device)
+    nl = len(ws)
+    roof = [roofline_us(w, peaks) for w in ws]
+
+    with torch.cuda.stream(stream):
+        for s in range(max(3, args.warmup)):
+            sets[s % 2].step()
+        torch.cuda.synchronize()
+        st = wq.wq_get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status after warm-up: {wq.wq_status_string(st)}")
+
+        # One graph per event set: graph g replays input set g % 2 and owns its events.
+        ng = max(1, min(args.steps, N_EVENT_GRAPHS))
+        graphs, events = [], []
+        in_graph_events = timing_event(torch) is not None
+        for g in range(ng):
+            ev = [timing_event(torch) if in_graph_events else torch.cuda.Event()
+                  for _ in range(nl + 1)]
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                ev[0].record()
+                for i in range(nl):
+                    st = sets[g % 2].call(i)
+                    if st != 0:
+                        raise RuntimeError(f"capture {ws[i]['name']}: {wq.wq_status_string(st)}")
+                    ev[i + 1].record()
+            graphs.append(gr)
+            events.append(ev)
+        for s in range(max(3, args.warmup)):
+            graphs[s % ng].replay()
+        torch.cuda.synchronize()
+
+        clocks = ClockSampler(local)
+        clocks.start()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start.record()
+        for s in range(args.steps):
+            graphs[s % ng].replay()
+        t_end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        clk = clocks.stop()
+        el_ms = t_start.elapsed_time(t_end)
+        st = wq.wq_get_device_status()
+        if st != 0:
+            raise RuntimeError(f"device status after timed steps: {wq.wq_status_string(st)}")
+
+        # Per-launch durations from the events of the last min(K, 64) steps.
+        per = np.zeros((ng, nl))
+        if in_graph_events:
+            for g in range(ng):
+                for i in range(nl):
+                    per[g, i] = events[g][i].elapsed_time(events[g][i + 1]) * 1e3
+            launch_us = per.mean(axis=0)
+        else:  # no timing events in graphs: time each launch alone, host-driven
+            launch_us = per_launch_fallback(sets, nl, torch)
+
+        # End to end: host-driven calls through the binding, pinned host copies.
+        ins, outs = [], []
+        for b in sets[0].bufs:
+            hin = {k: b[k].cpu().pin_memory() for k in ("X", "R", "ids") if b[k] is not None}
+            ins.append(hin)
+            outs.append(torch.empty(b["Y"].numel(), dtype=torch.float32).pin_memory())
+        h2d = sum(t.numel() * t.element_size() for d in ins for t in d.values())
+        d2h = sum(t.numel() * 4 for t in outs)
+        k_e2e = max(1, min(args.steps, 200))
+
+        def e2e_step(lset):
+            for i, b in enumerate(lset.bufs):
+                for key, t in ins[i].items():
+                    b[key].copy_(t, non_blocking=True)
+            lset.step()
+            for i, b in enumerate(lset.bufs):
+                outs[i].copy_(b["Y"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step(sets[0])
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        w0 = time.perf_counter()
+        e0.record()
+        for _ in range(k_e2e):
+            e2e_step(sets[0])
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - w0) * 1e3) / k_e2e
+        barrier(world)
+
+    ms_step = max_over_ranks(el_ms / args.steps, world, device)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    roof_us = sum(r[0] for r in roof)
+    value = roof_us / (ms_step * 1e3) * 100.0
+
+    detail = []
+    for i, w in enumerate(ws):
+        b, f = algorithmic(w)
+        t = launch_us[i]
+        detail.append({"name": w["name"], "us": round(t, 3), "GB_s": round(b / t / 1e3, 1),
+                       "TFLOP_s": round(f / t / 1e6, 2), "bound": roof[i][1],
+                       "roofline_pct": round(roof[i][0] / t * 100, 1)})
+    dom = int(np.argmax(launch_us))
+    b, f = algorithmic(ws[dom])
+    if roof[dom][1] == "hbm":
+        rl = {"bound": "hbm", "achieved": b / launch_us[dom] / 1e3, "peak": peaks["hbm_gbs"],
+              "unit": "GB/s"}
+    else:
+        rl = {"bound": "tensor", "achieved": f / launch_us[dom] / 1e6,
+              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    rl["frac"] = rl["achieved"] / rl["peak"]
+    rl["kernel"] = ws[dom]["name"]
+    rl["traffic"] = None
+    rl["peak_source"] = peaks["source"]
+
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic (seeded; shapes and distributions of the five workloads)",
+           "config": {"workload": "bf16 GEMM n32 + Q8_0 GEMV + Q4_0 GEMV n1/4/8 + encoder "
+                                  "GEMMs n1500 (tcgen05) + MoE Q4_0 E64 top6",
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                      "l2": "inputs larger than L2: 2 rotating input sets of ~340 MB",
+                      "launches_per_step": nl, "workloads": detail},
+           "gpu_launches": nl * args.steps,
+           "roofline": rl,
+           "e2e": {"value": roof_us / (e2e_ms * 1e3) * 100.0, "unit": UNIT,
+                   "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                   "ms_per_step": e2e_ms},
+           "clocks": clk}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(ws, peaks)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["wq", "reference"], default="wq")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

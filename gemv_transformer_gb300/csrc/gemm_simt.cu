@@ -1,0 +1,185 @@
+// gemm_simt.cu -- tiled f32-FMA GEMM for any n, all three weight formats.
+//
+// Computes cortiq-engine 0.8.49 ae_gemm's Y[n.m] (=|+=) X[n.k] . W[m.k]^T (+bias)
+// (gelu) with exact f32 products (W decoded bit-exactly, X as given), and the
+// masked store of ae_store (nothing outside [n][m] is written).
+//
+// Tile 64 (X rows) x 64 (W rows) x 32 (k), 256 threads, 4x4 outputs per thread.
+// W tiles are decoded into f32 in shared memory as they are loaded (one 32-weight
+// block per row per k step for Q8_0/Q4_0).  Each k step's 32 products are summed
+// into a fresh partial that is then added to the running total, which bounds the
+// serial f32 chain per output to k/32 + 32 terms.
+#include "wq_device.cuh"
+#include "wq_internal.h"
+
+namespace wq {
+namespace {
+
+constexpr int TI = 64, TJ = 64, TK = 32;
+
+template <int WT>
+__device__ __forceinline__ void load_w_tile(const GemmArgs &a, int j0, int kk, int tid,
+                                            float (*ws)[TJ + 4]) {
+    const int r = tid >> 2, q = tid & 3;  // row of the tile, eighth of the k step
+    const int j = j0 + r;
+    float w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = 0.f;
+    if (j < a.m) {
+        const uint8_t *row = a.W + (size_t)j * row_bytes(WT, a.k);
+        if (WT == kBF16) {
+            const int t0 = kk + 8 * q;
+            if (t0 < a.k) {  // k % 8 == 0: all eight or none
+                const uint4 v = *reinterpret_cast<const uint4 *>(row + (size_t)2 * t0);
+                w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x);
+                w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+                w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z);
+                w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
+            }
+        } else if (WT == kQ8_0) {
+            const uint8_t *bp = row + (size_t)34 * (kk / 32);
+            const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = d * (float)(int8_t)bp[2 + 8 * q + e];
+        } else {
+            const uint8_t *bp = row + (size_t)18 * (kk / 32);
+            const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * q + e;  // element of the block
+                const uint32_t byte = bp[2 + (t & 15)];
+                const int code = (t < 16) ? (int)(byte & 15u) : (int)(byte >> 4);
+                w[e] = d * (float)(code - 8);
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ws[8 * q + e][r] = w[e];
+}
+
+template <int WT>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const GemmArgs a) {
+    __shared__ float xs[TK][TI + 4];
+    __shared__ float ws[TK][TJ + 4];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int i0 = blockIdx.y * TI, j0 = blockIdx.x * TJ;
+    float acc[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
+
+    for (int kk = 0; kk < a.k; kk += TK) {
+        {  // X tile, transposed into xs[k][i]
+            const int r = tid >> 2, c0 = (tid & 3) * 8;
+            const int i = i0 + r;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = kk + c0 + e;
+                xs[c0 + e][r] = (i < a.n && t < a.k) ? __ldg(a.X + (size_t)i * a.k + t) : 0.f;
+            }
+        }
+        load_w_tile<WT>(a, j0, kk, tid, ws);
+        __syncthreads();
+        float part[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) part[u][v] = 0.f;
+#pragma unroll 8
+        for (int t = 0; t < TK; ++t) {
+            const float4 xv = *reinterpret_cast<const float4 *>(&xs[t][ty * 4]);
+            const float4 wv = *reinterpret_cast<const float4 *>(&ws[t][tx * 4]);
+            const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+            const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) part[u][v] = fmaf(xa[u], wa[v], part[u][v]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) acc[u][v] += part[u][v];
+        __syncthreads();
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = i0 + ty * 4 + u;
+        if (i >= a.n) continue;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int j = j0 + tx * 4 + v;
+            if (j >= a.m) continue;
+            const size_t o = (size_t)i * a.m + j;
+            a.Y[o] = epilogue(acc[u][v], a.flags, a.bias + j, a.R + o);
+        }
+    }
+}
+
+template <int WT>
+__global__ void dequant_kernel(int m, int k, const uint8_t *W, float *out) {
+    // One thread per 8 weights.
+    const long long units = (long long)m * (k / 8);
+    const size_t rb = row_bytes(WT, k);
+    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < units;
+         u += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(u / (k / 8));
+        const int t0 = (int)(u % (k / 8)) * 8;
+        const uint8_t *row = W + (size_t)j * rb;
+        float w[8];
+        if (WT == kBF16) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(row + (size_t)2 * t0);
+            w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x);
+            w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+            w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z);
+            w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
+        } else if (WT == kQ8_0) {
+            const uint8_t *bp = row + (size_t)34 * (t0 / 32);
+            const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+            for (int e = 0; e < 8; ++e) w[e] = d * (float)(int8_t)bp[2 + (t0 & 31) + e];
+        } else {
+            const uint8_t *bp = row + (size_t)18 * (t0 / 32);
+            const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+            for (int e = 0; e < 8; ++e) {
+                const int t = (t0 & 31) + e;
+                const uint32_t byte = bp[2 + (t & 15)];
+                const int code = (t < 16) ? (int)(byte & 15u) : (int)(byte >> 4);
+                w[e] = d * (float)(code - 8);
+            }
+        }
+        float *o = out + (size_t)j * k + t0;
+        for (int e = 0; e < 8; ++e) o[e] = w[e];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev,
+                             cudaStream_t stream) {
+    (void)dev;
+    dim3 grid((a.m + TJ - 1) / TJ, (a.n + TI - 1) / TI);
+    if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+    switch (wtype) {
+    case kBF16: gemm_simt_kernel<kBF16><<<grid, 256, 0, stream>>>(a); break;
+    case kQ8_0: gemm_simt_kernel<kQ8_0><<<grid, 256, 0, stream>>>(a); break;
+    default: gemm_simt_kernel<kQ4_0><<<grid, 256, 0, stream>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out,
+                           cudaStream_t stream) {
+    const long long units = (long long)m * (k / 8);
+    long long blocks = (units + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    switch (wtype) {
+    case kBF16: dequant_kernel<kBF16><<<(int)blocks, 256, 0, stream>>>(m, k, W, out); break;
+    case kQ8_0: dequant_kernel<kQ8_0><<<(int)blocks, 256, 0, stream>>>(m, k, W, out); break;
+    default: dequant_kernel<kQ4_0><<<(int)blocks, 256, 0, stream>>>(m, k, W, out); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace wq

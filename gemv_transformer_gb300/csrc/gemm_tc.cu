@@ -1,0 +1,377 @@
+// gemm_tc.cu -- large-n GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// Computes cortiq-engine 0.8.49 ae_gemm's Y[n.m] (=|+=) X[n.k] . W[m.k]^T (+bias)
+// (gelu) with W bf16 pairs (exact) and X rounded to bf16 (round to nearest
+// even), products and sums in the tensor core's f32 accumulator, and the ae_put
+// epilogue (+bias, erf-GELU, +old Y) fused into the TMEM read-back.  The page's
+// kernel runs f32 FMAs on 128x128 register tiles; this one is a tcgen05 kernel:
+//
+//   warp 0      TMA producer: W tiles [BN rows][64 k] (bf16, 128-byte swizzle)
+//   warp 1      TMEM owner + MMA issuer (one thread): tcgen05.mma kind::f16,
+//               M = 128 (X rows) x N = BN (W rows) x K = 16, f32 accumulator in TMEM
+//   warps 2..9  converters: load X f32 rows (coalesced, two k-blocks in flight),
+//               round to bf16 and store them in the same 128-byte-swizzled
+//               K-major layout the tensor core reads (no extra HBM pass for X);
+//               afterwards the same warps are the epilogue: tcgen05.ld of the
+//               accumulator, bias/GELU/residual, masked f32 stores.
+//
+// A/B stages are a 4-deep ring guarded by mbarriers; every wait is bounded.  A
+// wait that runs out sets the CTA's abort flag and WQ_ERR_DEVICE_TIMEOUT; every
+// role then stops, the producer drains its TMA copies, the MMA thread waits for
+// its MMAs, all threads meet, TMEM is freed and the CTA returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "wq_device.cuh"
+#include "wq_internal.h"
+
+namespace wq {
+namespace {
+
+constexpr int BM = 128;           // X rows per tile (tensor-core M)
+constexpr int BK = 64;            // k per stage: one 128-byte swizzle atom of bf16
+constexpr int kStages = 4;
+constexpr int kConvWarps = 8;
+constexpr int kThreads = (2 + kConvWarps) * 32;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+
+template <int BN>
+struct Smem {
+    static constexpr int kBBytes = BN * BK * 2;
+    static constexpr size_t kA = 0;
+    static constexpr size_t kB = kA + (size_t)kStages * kABytes;
+    static constexpr size_t kBars = kB + (size_t)kStages * kBBytes;
+    // a_full[S], b_full[S], empty[S], acc_full, drain
+    static constexpr size_t kMisc = kBars + (3 * kStages + 2) * sizeof(uint64_t);
+    static constexpr size_t kBytes = kMisc + 16 + 1024;  // + tmem slot, abort flag; + alignment
+};
+
+// ------------------------------------------------------------ PTX wrappers --
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    // K-major, 128-byte swizzle: rows of 128 B, 8-row groups 1024 B apart (SBO),
+    // descriptor version 1 (bits 46-47), layout type 2 = SWIZZLE_128B (bits 61-63).
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// kind::f16 instruction descriptor: D f32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    // cvt.rn: round to nearest even; the first source goes to the upper half.
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Bounded wait that also gives up when another role has aborted the CTA.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
+                                              volatile uint32_t *abort_flag, uint64_t limit,
+                                              unsigned *status) {
+    if (mbar_test_wait(bar, parity)) return true;
+    for (uint64_t i = 1;; ++i) {
+        if (*abort_flag) return false;
+        if (i >= limit) {
+            *abort_flag = 1u;
+            record_status(status, kStTimeout);
+            return false;
+        }
+        if (mbar_try_wait(bar, parity)) return true;
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const GemmArgs a) {
+    using L = Smem<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte-swizzled operand tiles.
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t *sA = smem + L::kA;
+    uint8_t *sB = smem + L::kB;
+    uint64_t *a_full = reinterpret_cast<uint64_t *>(smem + L::kBars);
+    uint64_t *b_full = a_full + kStages;
+    uint64_t *empty = b_full + kStages;
+    uint64_t *acc_full = empty + kStages;
+    uint64_t *drain = acc_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+    volatile uint32_t *abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i0 = blockIdx.y * BM, j0 = blockIdx.x * BN;
+    const int KB = (a.k + BK - 1) / BK;
+    const uint64_t limit = a.wait_limit;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&a_full[s], kConvWarps);
+            mbar_init(&b_full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {  // TMEM: BN f32 columns x 128 lanes
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                smem_addr(tmem_slot)),
+            "r"(BN)
+            : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int kb = 0;
+            for (; kb < KB; ++kb) {
+                const int s = kb % kStages;
+                if (kb >= kStages &&
+                    !wait_or_abort(&empty[s], ((kb / kStages) - 1) & 1, abort_flag, limit,
+                                   a.status))
+                    break;
+                mbar_arrive_expect_tx(&b_full[s], (uint32_t)L::kBBytes);
+                tma_load_2d(sB + (size_t)s * L::kBBytes, &wmap, kb * BK, j0, &b_full[s]);
+            }
+            // Drain: the last kStages loads issued may still be in flight.
+            for (int d = (kb > kStages ? kb - kStages : 0); d < kb; ++d)
+                mbar_wait(&b_full[d % kStages], (d / kStages) & 1, kDrainPolls);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(BM, BN);
+            bool ok = true;
+            for (int kb = 0; kb < KB && ok; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t ph = (kb / kStages) & 1;
+                ok = wait_or_abort(&a_full[s], ph, abort_flag, limit, a.status) &&
+                     wait_or_abort(&b_full[s], ph, abort_flag, limit, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_addr(sA + (size_t)s * kABytes);
+                const uint32_t b0 = smem_addr(sB + (size_t)s * L::kBBytes);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    tc_mma(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32),
+                           idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&empty[s]);
+            }
+            if (ok) {
+                tc_commit(acc_full);
+            } else {
+                tc_commit(drain);  // completes when every MMA issued so far is done
+                mbar_wait(drain, 0, kDrainPolls);
+            }
+        }
+    } else {
+        // ----------------------------------------------------- X converters
+        const int cw = warp - 2;          // 0..7: rows 16cw .. 16cw+15 of the tile
+        const int half = lane >> 4;       // which of the two rows of one load step
+        const int c4 = lane & 15;         // float4 index within the row's 64 k
+        bool ok = true;
+        float4 b0[8], b1[8], b2[8];  // k-blocks kb, kb+1, kb+2 (two loads in flight)
+        auto load_block = [&](int kb, float4(&dst)[8]) {
+            const int col = kb * BK + 4 * c4;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int row = i0 + cw * 16 + 2 * it + half;
+                if (row < a.n && col < a.k)
+                    dst[it] = __ldg(reinterpret_cast<const float4 *>(a.X + (size_t)row * a.k + col));
+                else
+                    dst[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        };
+        // Convert block kb from `cur` into stage kb % kStages, after starting the
+        // load of block kb + 2 into `pre`.
+        auto step = [&](int kb, const float4(&cur)[8], float4(&pre)[8]) -> bool {
+            const int s = kb % kStages;
+            if (kb + 2 < KB) load_block(kb + 2, pre);
+            if (kb >= kStages &&
+                !wait_or_abort(&empty[s], ((kb / kStages) - 1) & 1, abort_flag, limit, a.status))
+                return false;
+            uint8_t *tile = sA + (size_t)s * kABytes;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = cw * 16 + 2 * it + half;  // row within the tile
+                const uint32_t lo = pack_bf16x2(cur[it].x, cur[it].y);
+                const uint32_t hi = pack_bf16x2(cur[it].z, cur[it].w);
+                const int chunk = c4 >> 1;                         // 16-byte chunk of the row
+                const uint32_t off = r * 128 + ((chunk ^ (r & 7)) << 4) + ((c4 & 1) << 3);
+                *reinterpret_cast<uint2 *>(tile + off) = make_uint2(lo, hi);
+            }
+            fence_proxy_async_smem();  // generic-proxy stores -> tensor core reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[s]);
+            return true;
+        };
+        if (KB > 0) load_block(0, b0);
+        if (KB > 1) load_block(1, b1);
+        for (int kb = 0; kb < KB && ok; kb += 3) {
+            ok = step(kb, b0, b2);
+            if (ok && kb + 1 < KB) ok = step(kb + 1, b1, b0);
+            if (ok && kb + 2 < KB) ok = step(kb + 2, b2, b1);
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok && wait_or_abort(acc_full, 0, abort_flag, limit, a.status)) {
+            tc_fence_after();
+            const int q = warp & 3;                 // TMEM lane quarter of this warp
+            const int hcol = (warp - 2) >> 2;       // which half of the BN columns
+            const int row = i0 + q * 32 + lane;     // X row = TMEM lane
+            for (int c0 = hcol * (BN / 2); c0 < (hcol + 1) * (BN / 2); c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+                if (row < a.n) {
+                    const int jb = j0 + c0;
+                    const size_t ob = (size_t)row * a.m + jb;
+                    if (jb + 32 <= a.m && (a.m & 3) == 0) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4) {
+                            float4 o;
+                            float *po = &o.x;
+                            float4 rv = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (a.flags & kResidual)
+                                rv = *reinterpret_cast<const float4 *>(a.R + ob + c);
+                            const float *pr = &rv.x;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float t = v[c + e];
+                                if (a.flags & kBias) t += __ldg(a.bias + jb + c + e);
+                                if (a.flags & kGelu) t = gelu_erf(t);
+                                if (a.flags & kResidual) t += pr[e];
+                                po[e] = t;
+                            }
+                            *reinterpret_cast<float4 *>(a.Y + ob + c) = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (jb + c < a.m)
+                                a.Y[ob + c] = epilogue(v[c], a.flags, a.bias + jb + c, a.R + ob + c);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN)
+                     : "memory");
+    }
+}
+
+// ----------------------------------------------------------- host side --
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                            cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+template <int BN>
+cudaError_t launch_bn(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
+    static std::atomic<unsigned long long> smem_set{0};
+    auto encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)a.k, (cuuint64_t)a.m};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.k * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t *>(a.W),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    auto kern = gemm_tc_kernel<BN>;
+    cudaError_t err = ensure_smem(kern, (int)Smem<BN>::kBytes, dev, smem_set);
+    if (err != cudaSuccess) return err;
+    dim3 grid((a.m + BN - 1) / BN, (a.n + BM - 1) / BM);
+    if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+    kern<<<grid, kThreads, Smem<BN>::kBytes, stream>>>(map, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
+    const long long rows = (a.n + BM - 1) / BM;
+    const long long tiles256 = rows * ((a.m + 255) / 256);
+    if (tiles256 * 5 >= (long long)dev.sm_count * 4) return launch_bn<256>(a, dev, stream);
+    return launch_bn<128>(a, dev, stream);
+}
+
+}  // namespace wq

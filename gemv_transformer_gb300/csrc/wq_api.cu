@@ -1,0 +1,202 @@
+// wq_api.cu -- the extern "C" entry points of libwq (declared in include/wq.h).
+//
+// Host-side only: argument checks (the page's own checks are hanzo-ml 0.11.13
+// matvec_q*_gpu "k must be a multiple of 32", "x count < k", moe_matvec_gpu
+// "ids count < nrows"), routing to a kernel, and the sticky device status word
+// (wavo 0.3.0 src/gpu/mod.rs keeps the first device error and reports it on the
+// next call).  Nothing here computes; every step of the contraction runs in the
+// kernels.
+#include <mutex>
+
+#include "../../include/wq.h"
+#include "wq_device.cuh"
+#include "wq_internal.h"
+
+namespace wq {
+
+// One status word per device (each device has its own copy of module globals).
+__device__ unsigned g_status = 0u;
+
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitPolls = 1ull << 22;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ok[kMaxDevices];
+unsigned long long g_wait_limit = kDefaultWaitPolls;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+wq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA; }
+
+bool shape_ok(int wtype, int m, int k) {
+    if (m <= 0 || k <= 0) return false;
+    if (wtype == kBF16) return k % 8 == 0;
+    if (wtype == kQ8_0 || wtype == kQ4_0) return k % 32 == 0;
+    return false;
+}
+
+// Common checks of wq_gemm / wq_gemv.
+wq_status check_common(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                       const void *W, const float *bias, const float *residual, const float *Y) {
+    if (n <= 0 || !shape_ok(wtype, m, k)) return WQ_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(WQ_BIAS | WQ_GELU | WQ_RESIDUAL | WQ_TC_BF16)) return WQ_ERR_INVALID_ARG;
+    if (!X || !W || !Y) return WQ_ERR_INVALID_ARG;
+    if ((flags & WQ_BIAS) && !bias) return WQ_ERR_INVALID_ARG;
+    if ((flags & WQ_RESIDUAL) && !residual) return WQ_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W)) return WQ_ERR_INVALID_ARG;
+    return WQ_OK;
+}
+}  // namespace
+
+const DeviceInfo *device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_dev_ok[dev]) {
+        DeviceInfo d{};
+        d.ordinal = dev;
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return nullptr;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+        d.status = static_cast<unsigned *>(p);
+        g_dev[dev] = d;
+        g_dev_ok[dev] = true;
+    }
+    return &g_dev[dev];
+}
+
+unsigned long long wait_limit() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    return g_wait_limit;
+}
+
+}  // namespace wq
+
+using namespace wq;
+
+extern "C" {
+
+size_t wq_weight_bytes(int wtype, int m, int k) {
+    if (!shape_ok(wtype, m, k)) return 0;
+    const size_t b = row_bytes(wtype, k) * (size_t)m;
+    return (b + 15) & ~(size_t)15;
+}
+
+static wq_status gemv_impl(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                           const void *W, const float *bias, const float *residual, float *Y,
+                           wq_stream_t stream) {
+    const DeviceInfo *dev = device_info();
+    if (!dev) return WQ_ERR_CUDA;
+    StreamArgs a{};
+    a.X = X;
+    a.W = static_cast<const uint8_t *>(W);
+    a.bias = bias;
+    a.R = residual;
+    a.Y = Y;
+    a.n = n;
+    a.m = m;
+    a.k = k;
+    a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
+    a.status = dev->status;
+    a.wait_limit = wait_limit();
+    return cuda_status(launch_stream_gemv(a, wtype, *dev, (cudaStream_t)stream));
+}
+
+wq_status wq_gemv(int n, int m, int k, int wtype, unsigned flags, const float *X, const void *W,
+                  const float *bias, const float *residual, float *Y, wq_stream_t stream) {
+    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
+    if (s != WQ_OK) return s;
+    if (n > WQ_GEMV_MAX_N || (flags & WQ_TC_BF16)) return WQ_ERR_INVALID_ARG;
+    return gemv_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream);
+}
+
+wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X, const void *W,
+                  const float *bias, const float *residual, float *Y, wq_stream_t stream) {
+    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
+    if (s != WQ_OK) return s;
+    if ((flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
+    if (n <= WQ_GEMV_MAX_N)
+        return gemv_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream);
+    const DeviceInfo *dev = device_info();
+    if (!dev) return WQ_ERR_CUDA;
+    GemmArgs a{};
+    a.X = X;
+    a.W = static_cast<const uint8_t *>(W);
+    a.bias = bias;
+    a.R = residual;
+    a.Y = Y;
+    a.n = n;
+    a.m = m;
+    a.k = k;
+    a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
+    a.status = dev->status;
+    a.wait_limit = wait_limit();
+    if (flags & WQ_TC_BF16) return cuda_status(launch_gemm_tc(a, *dev, (cudaStream_t)stream));
+    return cuda_status(launch_gemm_simt(a, wtype, *dev, (cudaStream_t)stream));
+}
+
+wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtype,
+                      unsigned flags, const float *X, const void *Wbank, const int32_t *ids,
+                      const float *bias, const float *residual, float *Y, wq_stream_t stream) {
+    if (topk <= 0 || n_experts <= 0 || !ids) return WQ_ERR_INVALID_ARG;
+    wq_status s = check_common(n_tok, m, k, wtype, flags, X, Wbank, bias, residual, Y);
+    if (s != WQ_OK) return s;
+    if (flags & WQ_TC_BF16) return WQ_ERR_INVALID_ARG;
+    if ((long long)m * n_experts > 0x7FFFFFFFll) return WQ_ERR_INVALID_ARG;
+    if ((long long)n_tok * topk > WQ_MOE_MAX_SLOTS) return WQ_ERR_UNSUPPORTED;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return WQ_ERR_CUDA;
+    StreamArgs a{};
+    a.X = X;
+    a.W = static_cast<const uint8_t *>(Wbank);
+    a.bias = bias;
+    a.R = residual;
+    a.Y = Y;
+    a.ids = ids;
+    a.n = n_tok;
+    a.m = m;
+    a.k = k;
+    a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
+    a.topk = topk;
+    a.n_experts = n_experts;
+    a.status = dev->status;
+    a.wait_limit = wait_limit();
+    return cuda_status(launch_stream_moe(a, wtype, *dev, (cudaStream_t)stream));
+}
+
+wq_status wq_dequantize(int wtype, int m, int k, const void *W, float *out, wq_stream_t stream) {
+    if (!shape_ok(wtype, m, k) || !W || !out || !aligned16(W)) return WQ_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_dequant(wtype, m, k, static_cast<const uint8_t *>(W), out, (cudaStream_t)stream));
+}
+
+wq_status wq_get_device_status(wq_stream_t stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return WQ_ERR_CUDA;
+    unsigned v = 0;
+    const unsigned zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return WQ_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess)
+        return WQ_ERR_CUDA;
+    return (wq_status)v;
+}
+
+const char *wq_status_string(int status) {
+    switch (status) {
+    case WQ_OK: return "ok";
+    case WQ_ERR_INVALID_ARG: return "invalid argument";
+    case WQ_ERR_UNSUPPORTED: return "unsupported request";
+    case WQ_ERR_CUDA: return "CUDA runtime error";
+    case WQ_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case WQ_ERR_BAD_EXPERT: return "expert id out of range";
+    default: return "unknown status";
+    }
+}
+
+void wq_set_wait_limit(uint64_t polls) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_wait_limit = polls ? (unsigned long long)polls : kDefaultWaitPolls;
+}
+
+}  // extern "C"

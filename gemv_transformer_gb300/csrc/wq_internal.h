@@ -1,0 +1,72 @@
+// wq_internal.h -- host-side declarations shared by libwq's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <atomic>
+
+namespace wq {
+
+// Arguments of the weight-streaming kernels (plain GEMV and routed MoE).
+struct StreamArgs {
+    const float *X;        // [n][k] (GEMV) or [n_tok][k] (MoE)
+    const uint8_t *W;      // [m][row_bytes] or bank [E][m][row_bytes]
+    const float *bias;     // [m] or [E][m]
+    const float *R;        // residual, [n][m] or [slots][m]
+    float *Y;              // [n][m] or [slots][m]
+    const int32_t *ids;    // MoE: [n_tok][topk]
+    int n;                 // GEMV: rows of X; MoE: n_tok
+    int m, k;
+    unsigned flags;
+    int topk, n_experts;   // MoE only
+    unsigned *status;      // device status word
+    unsigned long long wait_limit;
+};
+
+struct GemmArgs {
+    const float *X;
+    const uint8_t *W;
+    const float *bias;
+    const float *R;
+    float *Y;
+    int n, m, k;
+    unsigned flags;
+    unsigned *status;
+    unsigned long long wait_limit;
+};
+
+struct DeviceInfo {
+    int ordinal;
+    int sm_count;
+    unsigned *status;  // address of this device's status word
+};
+
+// Raise a kernel's dynamic shared memory limit once per device.  `done` holds one
+// bit per device ordinal (< 64) and belongs to the kernel.
+template <typename Kernel>
+cudaError_t ensure_smem(Kernel kern, int bytes, const DeviceInfo &dev,
+                        std::atomic<unsigned long long> &done) {
+    const unsigned long long bit = 1ull << (dev.ordinal & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return err;
+}
+
+// Cached per-device facts (current device).  Returns nullptr on a CUDA error.
+const DeviceInfo *device_info();
+unsigned long long wait_limit();
+
+cudaError_t launch_stream_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,
+                               cudaStream_t stream);
+cudaError_t launch_stream_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,
+                              cudaStream_t stream);
+cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev,
+                             cudaStream_t stream);
+cudaError_t launch_gemm_tc(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t stream);
+cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out,
+                           cudaStream_t stream);
+
+}  // namespace wq

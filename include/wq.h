@@ -1,0 +1,170 @@
+/*
+ * wq.h -- C ABI of libwq: the weight-format contraction on one GPU
+ *
+ *     Y[n][m] (=|+=) epi( X[n][k] . W[m][k]^T )
+ *
+ * with W stored as bf16 pairs, GGML Q8_0 blocks or GGML Q4_0 blocks, dequantised
+ * on the fly, accumulated in f32, and a fused epilogue (bias, erf-GELU,
+ * residual add); plus the routed MoE matvec over one expert weight bank.
+ *
+ * Sources of each operation (page title, item):
+ *   - wq_gemm: cortiq-engine 0.8.49, src/gpu_wgpu/nemotron_audio.rs,
+ *     AudioEncoder::gemm and its kernel ae_gemm ("Y[n.m] (=|+=) X[n.k] . W[m.k]^T
+ *     (+bias) (gelu); W bf16 pairs"), epilogue ae_put, masked store ae_store;
+ *     wavo 0.3.0, src/gpu/mod.rs, Pass::gemm (Q8_0 weights).
+ *   - wq_gemv: hanzo-ml 0.11.13, src/wgpu_backend.rs, matvec_q8_0_gpu /
+ *     matvec_q4_0_gpu ("y[nout] = Wq * x[k]", raw GGML blocks read in place);
+ *     wavo 0.3.0, Pass::gemv (one activation row).
+ *   - wq_moe_gemv: hanzo-ml 0.11.13, moe_matvec_gpu ("y[s, r] = sum_k
+ *     W[ids[s], r, k] * x[s, k]" over one bank [E, rows, k], router gather and
+ *     expert matvec in one dispatch).
+ *   - wq_dequantize: the block formats themselves (same pages).
+ *   - wq_get_device_status: wavo 0.3.0, Gpu "failure" (the first device error is
+ *     reported by the next call) and its completion marks.
+ *
+ * Conventions shared by every call
+ *   - Index names: n = rows of X (tokens), m = rows of W (outputs), k = inner.
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  libwq never
+ *     allocates, frees or retains them, and allocates no device memory itself.
+ *   - Calls are asynchronous and ordered on `stream` (NULL = the legacy default
+ *     stream).  They return once the work is launched.  A returned error means
+ *     nothing was launched and no output was touched.
+ *   - X is f32 row-major [n][k] and must be 16-byte aligned.
+ *   - W is the storage-format byte image [m][row_bytes], 16-byte aligned, and its
+ *     buffer must hold at least wq_weight_bytes(wtype, m, k) bytes: the format's
+ *     size rounded up to a multiple of 16.  The padding is read, never used.
+ *   - bias is f32 [m] (read when WQ_BIAS is set, else ignored, may be NULL).
+ *   - residual is f32 [n][m] (read when WQ_RESIDUAL is set); it may equal Y, which
+ *     gives the in-place "Y +=" form.  No other argument may overlap Y.
+ *   - Y is f32 row-major [n][m].  Exactly the n*m elements of Y are written;
+ *     nothing before or after them.
+ *   - Device-side faults detected by a kernel (a bounded wait that ran out, an
+ *     expert id out of range) do not trap: they are recorded in a sticky per-device
+ *     status word that wq_get_device_status() reports and clears.
+ *   - Results are deterministic: the same call on the same inputs gives the same
+ *     bits.
+ */
+#ifndef WQ_H
+#define WQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define WQ_API __attribute__((visibility("default")))
+#else
+#define WQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without including CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *wq_stream_t;
+
+/* Weight storage formats. */
+typedef enum {
+    WQ_BF16 = 0, /* bf16 pairs: u32 word c of a row = element 2c | element 2c+1 << 16;
+                    i.e. row-major little-endian bf16 [m][k]; k % 8 == 0 */
+    WQ_Q8_0 = 1, /* 34-byte blocks of 32 weights along k: f16 d (LE), int8 q[32];
+                    w = d*q; k % 32 == 0 */
+    WQ_Q4_0 = 2  /* 18-byte blocks of 32 weights: f16 d (LE), 16 bytes; element t<16
+                    = low nibble of byte t, t>=16 = high nibble of byte t-16;
+                    w = d*(q-8); k % 32 == 0 */
+} wq_wtype;
+
+/* Epilogue flags, the bit values and order of cortiq-engine's ae_put:
+ * v = acc; if BIAS v += bias[j]; if GELU v = 0.5 v (1 + erf(v / sqrt 2));
+ * if RESIDUAL v += residual[i][j]; Y[i][j] = v. */
+enum {
+    WQ_BIAS = 1u,
+    WQ_GELU = 2u,
+    WQ_RESIDUAL = 4u,
+    /* wq_gemm only, WQ_BF16 weights only: run the contraction on the tcgen05
+     * tensor cores with X rounded to bf16 (round to nearest even) and f32
+     * accumulation.  Without it every path multiplies exact f32 products. */
+    WQ_TC_BF16 = 256u
+};
+
+typedef enum {
+    WQ_OK = 0,
+    WQ_ERR_INVALID_ARG = 1,    /* bad size, null pointer, misalignment, bad flag */
+    WQ_ERR_UNSUPPORTED = 2,    /* valid request this build has no kernel for */
+    WQ_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+    WQ_ERR_DEVICE_TIMEOUT = 4, /* a kernel's bounded wait ran out (device status) */
+    WQ_ERR_BAD_EXPERT = 5      /* an expert id outside [0, n_experts) (device status) */
+} wq_status;
+
+/* Largest n that wq_gemv accepts. */
+#define WQ_GEMV_MAX_N 16
+/* Largest n_tok * topk that wq_moe_gemv accepts. */
+#define WQ_MOE_MAX_SLOTS 256
+
+/*
+ * Y = epi(X . W^T) for any n >= 1 (cortiq-engine ae_gemm semantics).
+ * Routing: n <= WQ_GEMV_MAX_N goes to the weight-streaming GEMV kernels (as
+ * wq_gemv); otherwise WQ_TC_BF16 with WQ_BF16 weights runs the tcgen05 kernel,
+ * and everything else the f32-FMA tiled kernel.
+ * Errors: WQ_ERR_INVALID_ARG for n, m, k <= 0; k % 32 != 0 (Q8_0/Q4_0) or
+ * k % 8 != 0 (bf16); null X, W or Y; null bias/residual when its flag is set;
+ * X or W not 16-byte aligned; unknown flag bits or wtype.  WQ_ERR_UNSUPPORTED for
+ * WQ_TC_BF16 with a quantised wtype.  WQ_ERR_CUDA if the launch fails.
+ */
+WQ_API wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X, const void *W,
+                  const float *bias, const float *residual, float *Y, wq_stream_t stream);
+
+/*
+ * Same contract as wq_gemm for small n (1 <= n <= WQ_GEMV_MAX_N): the
+ * HBM-bound path that streams each weight byte once (hanzo-ml matvec_q*_gpu).
+ * WQ_TC_BF16 is rejected (WQ_ERR_INVALID_ARG).
+ */
+WQ_API wq_status wq_gemv(int n, int m, int k, int wtype, unsigned flags, const float *X, const void *W,
+                  const float *bias, const float *residual, float *Y, wq_stream_t stream);
+
+/*
+ * Routed MoE matvec (hanzo-ml moe_matvec_gpu), one launch:
+ *   Y[t][s][j] = epi( X[t] . Wbank[ids[t][s]][j]^T ),  t < n_tok, s < topk, j < m.
+ * X f32 [n_tok][k]; Wbank byte image [n_experts][m][row_bytes] (16-byte aligned,
+ * at least wq_weight_bytes(wtype, n_experts * m, k) bytes); ids int32
+ * [n_tok][topk] on the device; bias f32 [n_experts][m] (per expert, WQ_BIAS);
+ * residual f32 [n_tok*topk][m] (WQ_RESIDUAL, may equal Y); Y f32 [n_tok][topk][m].
+ * Each selected expert's weights are read once per call whatever the number of
+ * slots routed to it.  With topk = 1 and X holding one row per slot this is the
+ * page's per-slot form.  An id outside [0, n_experts) leaves that slot's Y row
+ * unwritten and sets WQ_ERR_BAD_EXPERT in the device status.
+ * Errors: as wq_gemm, plus n_tok*topk > WQ_MOE_MAX_SLOTS (WQ_ERR_UNSUPPORTED),
+ * null ids, topk or n_experts <= 0 (WQ_ERR_INVALID_ARG), WQ_TC_BF16
+ * (WQ_ERR_INVALID_ARG).
+ */
+WQ_API wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtype,
+                      unsigned flags, const float *X, const void *Wbank, const int32_t *ids,
+                      const float *bias, const float *residual, float *Y, wq_stream_t stream);
+
+/* Bytes a W buffer of m rows must hold: 2mk (bf16), 34mk/32 (Q8_0) or 18mk/32
+ * (Q4_0), rounded up to a multiple of 16.  0 for an invalid wtype/shape. */
+WQ_API size_t wq_weight_bytes(int wtype, int m, int k);
+
+/* out[m][k] (f32, device) = the dequantised weights, bit-exact (d*q and d*(q-8)
+ * are exact in f32).  Same W contract as wq_gemm.  Asynchronous on `stream`. */
+WQ_API wq_status wq_dequantize(int wtype, int m, int k, const void *W, float *out, wq_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the current device's sticky
+ * status word: WQ_OK, WQ_ERR_DEVICE_TIMEOUT or WQ_ERR_BAD_EXPERT (the first
+ * recorded since the last call); WQ_ERR_CUDA if the synchronisation fails. */
+WQ_API wq_status wq_get_device_status(wq_stream_t stream);
+
+/* Static English text for a status code. */
+WQ_API const char *wq_status_string(int status);
+
+/* Diagnostics: the number of polls after which a kernel's wait on an mbarrier
+ * gives up, records WQ_ERR_DEVICE_TIMEOUT, drains its own copies in flight,
+ * releases what it holds and returns.  0 restores the default (about seconds).
+ * Affects launches made after the call, on every device. */
+WQ_API void wq_set_wait_limit(uint64_t polls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WQ_H */

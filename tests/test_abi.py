@@ -1,0 +1,92 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument checks reject bad calls before touching a device (CPU only)."""
+import os
+import re
+
+import pytest
+
+import gemv_transformer_gb300 as wq
+from gemv_transformer_gb300 import build as wqbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    wqbuild.build()
+    return wq.load()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "wq.h")) as f:
+        text = f.read()
+    return re.findall(r"WQ_API\s+[\w\s\*]+?\b(wq_\w+)\s*\(", text)
+
+
+def test_header_declares_the_binding_names():
+    assert sorted(declared_functions()) == sorted(wq.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_weight_bytes():
+    assert wq.wq_weight_bytes(wq.WQ_BF16, 512, 256) == 2 * 512 * 256
+    assert wq.wq_weight_bytes(wq.WQ_Q8_0, 4096, 4096) == 17_825_792
+    assert wq.wq_weight_bytes(wq.WQ_Q4_0, 14336, 4096) == 33_030_144
+    assert wq.wq_weight_bytes(wq.WQ_Q8_0, 1, 32) == 48      # 34 rounded up to 16
+    assert wq.wq_weight_bytes(wq.WQ_Q4_0, 3, 64) == 112     # 108 rounded up
+    assert wq.wq_weight_bytes(wq.WQ_Q4_0, 1, 40) == 0       # k % 32
+    assert wq.wq_weight_bytes(wq.WQ_BF16, 1, 12) == 0       # k % 8
+    assert wq.wq_weight_bytes(7, 1, 32) == 0
+
+
+def test_status_strings():
+    for code in range(6):
+        assert wq.wq_status_string(code) != "unknown status"
+    assert wq.wq_status_string(99) == "unknown status"
+
+
+A = 0x10000  # a 16-byte aligned fake device address: never dereferenced below
+
+
+@pytest.mark.parametrize("call", [
+    lambda: wq.wq_gemm(0, 8, 32, wq.WQ_Q8_0, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 0, 32, wq.WQ_Q8_0, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 40, wq.WQ_Q8_0, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 36, wq.WQ_Q4_0, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 12, wq.WQ_BF16, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, 3, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 8, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 0, None, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 0, A, None, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 0, A, A, None, None, None, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, wq.WQ_BIAS, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, wq.WQ_RESIDUAL, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 0, A + 4, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 0, A, A + 2, None, None, A, 0),
+    lambda: wq.wq_gemv(17, 8, 32, wq.WQ_Q8_0, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemv(1, 8, 32, wq.WQ_BF16, wq.WQ_TC_BF16, A, A, None, None, A, 0),
+    lambda: wq.wq_moe_gemv(2, 0, 4, 8, 32, wq.WQ_Q4_0, 0, A, A, A, None, None, A, 0),
+    lambda: wq.wq_moe_gemv(2, 2, 0, 8, 32, wq.WQ_Q4_0, 0, A, A, A, None, None, A, 0),
+    lambda: wq.wq_moe_gemv(2, 2, 4, 8, 32, wq.WQ_Q4_0, 0, A, A, None, None, None, A, 0),
+    lambda: wq.wq_moe_gemv(2, 2, 4, 8, 32, wq.WQ_Q4_0, wq.WQ_TC_BF16, A, A, A, None, None, A, 0),
+    lambda: wq.wq_dequantize(wq.WQ_Q8_0, 4, 40, A, A, 0),
+    lambda: wq.wq_dequantize(wq.WQ_Q8_0, 4, 32, None, A, 0),
+])
+def test_invalid_arguments_rejected_on_host(lib, call):
+    assert call() == wq.WQ_ERR_INVALID_ARG
+
+
+def test_unsupported_requests(lib):
+    assert wq.wq_gemm(32, 8, 32, wq.WQ_Q8_0, wq.WQ_TC_BF16, A, A, None, None, A, 0) == \
+        wq.WQ_ERR_UNSUPPORTED
+    assert wq.wq_moe_gemv(64, 5, 8, 8, 32, wq.WQ_Q4_0, 0, A, A, A, None, None, A, 0) == \
+        wq.WQ_ERR_UNSUPPORTED
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        wq._open(str(tmp_path / "missing.so"))

@@ -1,0 +1,294 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the f64 oracle.
+
+Small shapes span several pieces/tiles and ragged tails; the full workloads are
+checked at their real sizes.  Dequantised weights must be bit-exact; Y must be
+within tau * L * sum|x||w| (+ epilogue rounding, see helpers.py) with tau = 1e-5
+on the f32-FMA paths.  Outputs sit between guard zones that must stay intact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemv_transformer_gb300 as wq
+import synth
+from helpers import Guarded, assert_within, dev, status_ok, weights_dev
+
+pytestmark = pytest.mark.gpu
+
+BF16, Q8_0, Q4_0 = wq.WQ_BF16, wq.WQ_Q8_0, wq.WQ_Q4_0
+BIAS, GELU, RES = wq.WQ_BIAS, wq.WQ_GELU, wq.WQ_RESIDUAL
+TAU = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gemv_transformer_gb300 import build
+    build.build()
+    wq.load()
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+    yield
+    status_ok()
+
+
+def run_gemm(fn, n, m, k, wtype, flags, X, img, bias=None, R=None, inplace=False):
+    Xd, Wd = dev(X), weights_dev(img, wtype, m, k)
+    bd = dev(bias) if bias is not None else None
+    if inplace:
+        out = Guarded(n * m, R)
+        Rd = out.view
+    else:
+        out = Guarded(n * m)
+        Rd = dev(R) if R is not None else None
+    st = fn(n, m, k, wtype, flags, Xd, Wd, bd, Rd, out.view)
+    wq.check(st, fn.__name__)
+    torch.cuda.synchronize()
+    status_ok()
+    return out.result().reshape(n, m)
+
+
+def case(seed, wtype, n, m, k, flags):
+    g = synth.rng(seed)
+    X = synth.normal_f32(g, (n, k))
+    img = synth.draw_weights(g, wtype, m, k)
+    bias = synth.normal_f32(g, (m,), 0.1) if flags & BIAS else None
+    R = synth.normal_f32(g, (n, m)) if flags & RES else None
+    return X, img, bias, R
+
+
+def check_against_oracle(oracle_mod, fn, wtype, n, m, k, flags, seed=0, inplace=False):
+    X, img, bias, R = case(seed, wtype, n, m, k, flags)
+    Y = run_gemm(fn, n, m, k, wtype, flags, X, img, bias, R, inplace=inplace)
+    Yref, S = oracle_mod.gemm(n, m, k, wtype, flags, X, img, bias=bias, residual=R)
+    return assert_within(Y, Yref, S, TAU, gelu=bool(flags & GELU), bias=bias, R=R,
+                         what=f"{fn.__name__} wtype={wtype} n={n} m={m} k={k} flags={flags}")
+
+
+# ------------------------------------------------------------------ GEMV --
+
+GEMV_SHAPES = [(1, 1, 32), (1, 37, 64), (2, 130, 96), (3, 513, 4128), (4, 300, 2080),
+               (5, 77, 8224), (8, 1000, 512), (9, 64, 256), (16, 129, 4160)]
+
+
+@pytest.mark.parametrize("wtype", [Q8_0, Q4_0])
+@pytest.mark.parametrize("shape", GEMV_SHAPES)
+def test_gemv_quantized(oracle_mod, wtype, shape):
+    n, m, k = shape
+    check_against_oracle(oracle_mod, wq.wq_gemv, wtype, n, m, k, 0, seed=n * 31 + m)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 8), (1, 37, 16), (2, 130, 1032), (3, 300, 2056),
+                                   (4, 65, 4104), (8, 200, 520), (16, 33, 1000)])
+def test_gemv_bf16(oracle_mod, shape):
+    n, m, k = shape
+    check_against_oracle(oracle_mod, wq.wq_gemv, BF16, n, m, k, 0, seed=n * 31 + m)
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("flags", [BIAS, GELU, BIAS | GELU, RES, BIAS | RES, BIAS | GELU | RES])
+def test_gemv_epilogues(oracle_mod, wtype, flags):
+    check_against_oracle(oracle_mod, wq.wq_gemv, wtype, 3, 261, 2048, flags, seed=flags)
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+def test_gemv_residual_in_place(oracle_mod, wtype):
+    check_against_oracle(oracle_mod, wq.wq_gemv, wtype, 4, 190, 1024, BIAS | GELU | RES,
+                         seed=9, inplace=True)
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+def test_gemm_small_n_routes_to_gemv(oracle_mod, wtype):
+    check_against_oracle(oracle_mod, wq.wq_gemm, wtype, 16, 100, 512, BIAS | GELU, seed=4)
+
+
+# ------------------------------------------------------------ SIMT GEMM --
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("shape", [(17, 64, 32), (32, 65, 96), (100, 200, 256), (129, 31, 544)])
+def test_gemm_simt(oracle_mod, wtype, shape):
+    n, m, k = shape
+    check_against_oracle(oracle_mod, wq.wq_gemm, wtype, n, m, k, BIAS | GELU, seed=n + m)
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+def test_gemm_simt_residual_in_place(oracle_mod, wtype):
+    check_against_oracle(oracle_mod, wq.wq_gemm, wtype, 70, 130, 160 if wtype == BF16 else 192,
+                         BIAS | RES, seed=3, inplace=True)
+
+
+def test_gemm_bf16_ragged_k(oracle_mod):
+    check_against_oracle(oracle_mod, wq.wq_gemm, BF16, 40, 72, 200, BIAS, seed=8)
+
+
+# ---------------------------------------------------------------- dequant --
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("mk", [(1, 32), (7, 96), (300, 4128)])
+def test_dequantize_bit_exact(oracle_mod, wtype, mk):
+    m, k = mk
+    img = synth.draw_weights(synth.rng(m + k), wtype, m, k)
+    out = Guarded(m * k)
+    wq.check(wq.wq_dequantize(wtype, m, k, weights_dev(img, wtype, m, k), out.view))
+    got = out.result().reshape(m, k)
+    want = oracle_mod.dequant(wtype, m, k, img)
+    assert (got.astype(np.float64) == want).all()
+
+
+def test_dequantize_hand_blocks(oracle_mod):
+    """The worked Q8_0 codes under a subnormal and a negative scale, and all Q4_0 codes."""
+    codes = np.arange(-128, 128, dtype=np.int16).astype(np.int8).reshape(2, 128)
+    for dbits, unit in ((0x0001, 2.0 ** -24), (0xBC00, -1.0), (0x2000, 2.0 ** -7)):
+        img = synth.encode_q8_0(np.full((2, 4), dbits, np.uint16), codes)
+        out = Guarded(256)
+        wq.check(wq.wq_dequantize(Q8_0, 2, 128, weights_dev(img, Q8_0, 2, 128), out.view))
+        assert (out.result().reshape(2, 128) == codes.astype(np.float64) * unit).all()
+    q4 = (np.arange(32)[None, :] + np.arange(16)[:, None]) % 16
+    img = synth.encode_q4_0(np.full((16, 1), 0x4000, np.uint16), q4.astype(np.uint8))
+    out = Guarded(16 * 32)
+    wq.check(wq.wq_dequantize(Q4_0, 16, 32, weights_dev(img, Q4_0, 16, 32), out.view))
+    assert (out.result().reshape(16, 32) == 2.0 * (q4 - 8)).all()
+
+
+# -------------------------------------------------------- exact brute force --
+
+@pytest.mark.parametrize("fn", [wq.wq_gemv, wq.wq_gemm])
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+def test_integer_exact(oracle_mod, fn, wtype):
+    """Small-integer X and power-of-two scales: every sum is exact in f32, so the
+    GPU result must equal the oracle bit for bit in any summation order."""
+    n = 5 if fn is wq.wq_gemv else 40
+    m, k = 70, 256
+    g = synth.rng(77)
+    X = g.integers(-3, 4, size=(n, k)).astype(np.float32)
+    if wtype == BF16:
+        img = synth.bf16_pairs(synth.bf16_bits_rne((g.integers(-8, 9, size=(m, k)) * 0.5)
+                                                   .astype(np.float32)))
+    else:
+        d = synth.f16_bits(np.ldexp(1.0, g.integers(-6, -2, size=(m, k // 32))))
+        img = (synth.encode_q8_0(d, g.integers(-128, 128, size=(m, k)).astype(np.int8))
+               if wtype == Q8_0 else
+               synth.encode_q4_0(d, g.integers(0, 16, size=(m, k)).astype(np.uint8)))
+    Y = run_gemm(fn, n, m, k, wtype, 0, X, img)
+    Yref, _ = oracle_mod.gemm(n, m, k, wtype, 0, X, img)
+    assert (Y.astype(np.float64) == Yref).all()
+
+
+def test_wavo_probe_closed_form():
+    """wavo's probe_tensor shape: c[r][j] = j % 32 + r % 32 exactly (both paths)."""
+    n, m, k = 130, 64, 32
+    a = np.array([[x + r % 32 for x in range(k)] for r in range(n)], np.float32)
+    onehot = np.array([[1 if x == j % 32 else 0 for x in range(k)] for j in range(m)])
+    img = synth.encode_q8_0(np.full((m, 1), 0x3C00, np.uint16), onehot.astype(np.int8))
+    want = np.array([[j % 32 + r % 32 for j in range(m)] for r in range(n)], np.float32)
+    Y = run_gemm(wq.wq_gemm, n, m, k, Q8_0, BIAS, a, img, bias=np.zeros(m, np.float32))
+    assert (Y == want).all()
+    Y = run_gemm(wq.wq_gemv, 16, m, k, Q8_0, BIAS, a[:16], img, bias=np.zeros(m, np.float32))
+    assert (Y == want[:16]).all()
+
+
+# -------------------------------------------------------------------- MoE --
+
+def run_moe(n_tok, topk, E, m, k, wtype, flags, X, bank, ids, bias=None, R=None):
+    out = Guarded(n_tok * topk * m)
+    st = wq.wq_moe_gemv(n_tok, topk, E, m, k, wtype, flags, dev(X),
+                        weights_dev(bank, wtype, E * m, k), dev(ids),
+                        dev(bias) if bias is not None else None,
+                        dev(R) if R is not None else None, out.view)
+    wq.check(st, "wq_moe_gemv")
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("cfg", [(1, 1, 1, 33, 64), (3, 2, 5, 70, 256), (16, 6, 64, 140, 2048),
+                                 (8, 3, 4, 257, 4160), (32, 8, 16, 40, 96)])
+def test_moe(oracle_mod, wtype, cfg):
+    n_tok, topk, E, m, k = cfg
+    if wtype == BF16:
+        k = k + 8 if k % 32 == 0 else k
+    g = synth.rng(sum(cfg) + wtype)
+    bank = synth.draw_weights(g, wtype, E * m, k).reshape(E, m, -1)
+    X = synth.normal_f32(g, (n_tok, k))
+    ids = synth.moe_ids(g, n_tok, topk, E)
+    flags = BIAS | GELU | RES
+    bias = synth.normal_f32(g, (E, m), 0.1)
+    R = synth.normal_f32(g, (n_tok * topk, m))
+    Y = run_moe(n_tok, topk, E, m, k, wtype, flags, X, bank, ids, bias, R).result()
+    status_ok()
+    Yref, S = oracle_mod.moe(n_tok, topk, E, m, k, wtype, flags, X, bank, ids, bias=bias,
+                             residual=R)
+    bias_rows = bias[ids.reshape(-1)]
+    assert_within(Y.reshape(Yref.shape), Yref, S, TAU, gelu=True, bias=None,
+                  R=np.abs(R) + np.abs(bias_rows), what=f"moe {cfg}")
+
+
+def test_moe_repeated_expert_and_bad_id(oracle_mod):
+    """A token may route twice to one expert; a bad id sets the device status and
+    leaves only its own slot's row unwritten."""
+    n_tok, topk, E, m, k = 4, 3, 6, 50, 64
+    g = synth.rng(12)
+    bank = synth.draw_q4_0_weights(g, E * m, k).reshape(E, m, -1)
+    X = synth.normal_f32(g, (n_tok, k))
+    ids = np.array([[1, 1, 2], [5, 0, 1], [3, 9, 3], [2, 2, 2]], np.int32)  # 9 is out of range
+    out = run_moe(n_tok, topk, E, m, k, Q4_0, 0, X, bank, ids)
+    assert wq.wq_get_device_status() == wq.WQ_ERR_BAD_EXPERT
+    status_ok()  # cleared by the read
+    Y = out.result().reshape(n_tok * topk, m)
+    bad = 2 * topk + 1
+    assert (Y[bad].view(np.int32) == -1).all()
+    good = [q for q in range(n_tok * topk) if q != bad]
+    ids_ok = ids.copy()
+    ids_ok[2, 1] = 0
+    Yref, S = oracle_mod.moe(n_tok, topk, E, m, k, Q4_0, 0, X, bank, ids_ok)
+    assert_within(Y[good], Yref[good], S[good], TAU, what="moe repeated ids")
+
+
+def test_moe_scaled_identity_routing():
+    """Expert e = (e+1)*2^-6 * I: Y[t][s] is (ids[t][s]+1)*2^-6 * X[t] rounded once to f32."""
+    E, k, n_tok, topk = 8, 64, 5, 3
+    imgs = []
+    for e in range(E):
+        d = np.full((k, k // 32), synth.f16_bits((e + 1) * 2.0 ** -6)[()], np.uint16)
+        q = np.zeros((k, k), np.int8)
+        np.fill_diagonal(q, 1)
+        imgs.append(synth.encode_q8_0(d, q))
+    bank = np.stack(imgs)
+    g = synth.rng(5)
+    X = synth.normal_f32(g, (n_tok, k))
+    ids = synth.moe_ids(g, n_tok, topk, E)
+    Y = run_moe(n_tok, topk, E, k, k, Q8_0, 0, X, bank, ids).result().reshape(n_tok, topk, k)
+    want = (ids[:, :, None] + 1) * 2.0 ** -6 * X[:, None, :].astype(np.float64)
+    assert (Y == want.astype(np.float32)).all()
+
+
+# ------------------------------------------------------------ determinism --
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+def test_bit_identical_reruns(wtype):
+    n, m, k = 8, 1500, 2048
+    X, img, bias, _ = case(21, wtype, n, m, k, BIAS)
+    Y1 = run_gemm(wq.wq_gemv, n, m, k, wtype, BIAS, X, img, bias)
+    Y2 = run_gemm(wq.wq_gemv, n, m, k, wtype, BIAS, X, img, bias)
+    assert (Y1.view(np.int32) == Y2.view(np.int32)).all()
+
+
+# ------------------------------------------------------- bounded waits --
+
+def test_wait_limit_expires_without_hang(oracle_mod):
+    """A one-poll wait limit makes the weight-stream waits give up: the kernel
+    records WQ_ERR_DEVICE_TIMEOUT, drains its copies and returns; the context
+    stays usable and the next call (default limit) is correct."""
+    n, m, k = 1, 4096, 4096
+    X, img, _, _ = case(5, Q8_0, n, m, k, 0)
+    Xd, Wd = dev(X), weights_dev(img, Q8_0, m, k)
+    Y = torch.zeros(n * m, device="cuda")
+    wq.wq_set_wait_limit(1)
+    try:
+        wq.check(wq.wq_gemv(n, m, k, Q8_0, 0, Xd, Wd, None, None, Y))
+        assert wq.wq_get_device_status() == wq.WQ_ERR_DEVICE_TIMEOUT
+    finally:
+        wq.wq_set_wait_limit(0)
+    assert wq.wq_get_device_status() == wq.WQ_OK
+    wq.check(wq.wq_gemv(n, m, k, Q8_0, 0, Xd, Wd, None, None, Y))
+    status_ok()
+    Yref, S = oracle_mod.gemm(n, m, k, Q8_0, 0, X, img)
+    assert_within(Y.cpu().numpy().reshape(n, m), Yref, S, TAU)

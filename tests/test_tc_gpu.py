@@ -1,0 +1,131 @@
+"""GPU parity of the tcgen05 GEMM (WQ_TC_BF16): X is rounded to bf16 in the kernel.
+
+Two checks per case:
+  * against the oracle on the UNROUNDED X, tau = 8e-3 (the contract of the path);
+  * against the oracle fed bf16(X) (round to nearest even, the oracle's own
+    rounding), tau_k = (k/16 + 32) * 2^-23: the tensor core's f32 accumulation
+    over k/16 MMA steps plus the rounding inside each step.  This pins the
+    kernel's arithmetic apart from the input rounding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemv_transformer_gb300 as wq
+import synth
+from helpers import Guarded, assert_within, dev, status_ok, weights_dev
+
+pytestmark = pytest.mark.gpu
+
+BF16 = wq.WQ_BF16
+BIAS, GELU, RES, TC = wq.WQ_BIAS, wq.WQ_GELU, wq.WQ_RESIDUAL, wq.WQ_TC_BF16
+TAU_TC = 8e-3
+
+
+def tau_exact(k):
+    return (k / 16 + 32) * 2.0 ** -23
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gemv_transformer_gb300 import build
+    build.build()
+    wq.load()
+    yield
+    status_ok()
+
+
+def run_tc(n, m, k, flags, X, img, bias=None, R=None, inplace=False):
+    if inplace:
+        out = Guarded(n * m, R)
+        Rd = out.view
+    else:
+        out = Guarded(n * m)
+        Rd = dev(R) if R is not None else None
+    st = wq.wq_gemm(n, m, k, BF16, flags | TC, dev(X), weights_dev(img, BF16, m, k),
+                    dev(bias) if bias is not None else None, Rd, out.view)
+    wq.check(st, "wq_gemm(TC)")
+    torch.cuda.synchronize()
+    status_ok()
+    return out.result().reshape(n, m)
+
+
+def check_tc(oracle_mod, n, m, k, flags, seed, rows=None, inplace=False, std=0.03):
+    g = synth.rng(seed)
+    X = synth.normal_f32(g, (n, k))
+    img = synth.draw_bf16_weights(g, m, k, std)
+    bias = synth.normal_f32(g, (m,), 0.1) if flags & BIAS else None
+    R = synth.normal_f32(g, (n, m)) if flags & RES else None
+    Y = run_tc(n, m, k, flags, X, img, bias, R, inplace=inplace)
+    j0, j1 = rows if rows else (0, m)
+    gelu = bool(flags & GELU)
+    for round_x, tau in ((False, TAU_TC), (True, tau_exact(k))):
+        Yref, S = oracle_mod.gemm(n, m, k, BF16, flags, X, img, bias=bias, residual=R,
+                                  round_x=round_x, rows=(j0, j1))
+        assert_within(Y[:, j0:j1], Yref[:, j0:j1], S[:, j0:j1], tau, gelu=gelu,
+                      bias=None if bias is None else bias[j0:j1],
+                      R=None if R is None else R[:, j0:j1],
+                      what=f"tc n={n} m={m} k={k} flags={flags} round_x={round_x}")
+    return Y
+
+
+@pytest.mark.parametrize("shape", [(17, 16, 8), (128, 128, 64), (130, 256, 128), (300, 520, 1032),
+                                   (257, 300, 200), (1000, 1000, 512), (64, 2048, 256)])
+def test_tc_shapes(oracle_mod, shape):
+    n, m, k = shape
+    check_tc(oracle_mod, n, m, k, BIAS, seed=n + m + k)
+
+
+@pytest.mark.parametrize("flags", [0, BIAS, GELU, BIAS | GELU, RES, BIAS | RES, BIAS | GELU | RES])
+def test_tc_epilogues(oracle_mod, flags):
+    check_tc(oracle_mod, 200, 384, 320, flags, seed=flags)
+
+
+def test_tc_residual_in_place_ragged_m(oracle_mod):
+    check_tc(oracle_mod, 150, 203, 264, BIAS | RES, seed=3, inplace=True)
+
+
+def test_tc_integer_exact():
+    """bf16-exact small integers: every partial sum is an integer below 2^24, so the
+    tensor core must produce the exact result."""
+    n, m, k = 256, 256, 512
+    g = synth.rng(99)
+    X = g.integers(-4, 5, size=(n, k)).astype(np.float32)
+    Wv = g.integers(-4, 5, size=(m, k)).astype(np.float32)
+    img = synth.bf16_pairs(synth.bf16_bits_rne(Wv))
+    Y = run_tc(n, m, k, 0, X, img)
+    want = X.astype(np.float64) @ Wv.astype(np.float64).T
+    assert (Y == want).all()
+
+
+def test_tc_deterministic():
+    n, m, k = 300, 512, 1024
+    g = synth.rng(4)
+    X = synth.normal_f32(g, (n, k))
+    img = synth.draw_bf16_weights(g, m, k, 0.03)
+    b = synth.normal_f32(g, (m,), 0.1)
+    Y1 = run_tc(n, m, k, BIAS | GELU, X, img, b)
+    Y2 = run_tc(n, m, k, BIAS | GELU, X, img, b)
+    assert (Y1.view(np.int32) == Y2.view(np.int32)).all()
+
+
+def test_tc_wait_limit_expires_without_hang(oracle_mod):
+    """A one-poll wait limit aborts every CTA of the tensor-core kernel: it records
+    WQ_ERR_DEVICE_TIMEOUT, drains its TMA copies and MMAs, frees TMEM and returns;
+    the next call with the default limit is correct."""
+    n, m, k = 512, 1024, 1024
+    g = synth.rng(6)
+    X = synth.normal_f32(g, (n, k))
+    img = synth.draw_bf16_weights(g, m, k, 0.03)
+    Xd, Wd = dev(X), weights_dev(img, BF16, m, k)
+    Y = torch.zeros(n * m, device="cuda")
+    wq.wq_set_wait_limit(1)
+    try:
+        wq.check(wq.wq_gemm(n, m, k, BF16, TC, Xd, Wd, None, None, Y))
+        assert wq.wq_get_device_status() == wq.WQ_ERR_DEVICE_TIMEOUT
+    finally:
+        wq.wq_set_wait_limit(0)
+    wq.check(wq.wq_gemm(n, m, k, BF16, TC, Xd, Wd, None, None, Y))
+    status_ok()
+    Yref, S = oracle_mod.gemm(n, m, k, BF16, 0, X, img, round_x=True, rows=(0, 64))
+    assert_within(Y.cpu().numpy().reshape(n, m)[:, :64], Yref[:, :64], S[:, :64], tau_exact(k))

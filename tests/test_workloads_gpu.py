@@ -1,0 +1,93 @@
+"""The five workloads at their full sizes, through the C ABI, in the launch
+configuration the benchmark times, against the f64 oracle.
+
+The oracle computes every output of the GEMV and MoE workloads; for the encoder
+GEMMs (1500 x 3072/4096/1024, k up to 4096) it computes three 32-column bands of
+every GEMM (all 1500 rows), and the rest of Y is checked for being finite.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemv_transformer_gb300 as wq
+import synth
+from helpers import Guarded, assert_within, dev, status_ok, weights_dev
+
+pytestmark = pytest.mark.gpu
+TAU = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gemv_transformer_gb300 import build
+    build.build()
+    wq.load()
+    yield
+    status_ok()
+
+
+def run(fn, w, flags_extra=0):
+    n, m, k = w["n"], w["m"], w["k"]
+    out = Guarded(n * m)
+    b = dev(w["bias"]) if w["bias"] is not None else None
+    R = dev(w["residual"]) if w["residual"] is not None else None
+    st = fn(n, m, k, w["wtype"], w["flags"] | flags_extra, dev(w["X"]),
+            weights_dev(w["W"], w["wtype"], m, k), b, R, out.view)
+    wq.check(st, w["name"])
+    torch.cuda.synchronize()
+    status_ok()
+    return out.result().reshape(n, m)
+
+
+def check_full(oracle_mod, w, fn):
+    Y = run(fn, w)
+    Yref, S = oracle_mod.gemm(w["n"], w["m"], w["k"], w["wtype"], w["flags"], w["X"], w["W"],
+                              bias=w["bias"], residual=w["residual"])
+    return assert_within(Y, Yref, S, TAU, gelu=bool(w["flags"] & wq.WQ_GELU), bias=w["bias"],
+                         R=w["residual"], what=w["name"])
+
+
+def test_bf16_gemm_bias_gelu(oracle_mod):
+    check_full(oracle_mod, synth.workload_bf16_gemm(), wq.wq_gemm)
+
+
+def test_q8_0_gemv(oracle_mod):
+    check_full(oracle_mod, synth.workload_q8_0_gemv(), wq.wq_gemv)
+
+
+@pytest.mark.parametrize("n", [1, 4, 8])
+def test_q4_0_gemv_residual(oracle_mod, n):
+    check_full(oracle_mod, synth.workload_q4_0_gemv(n=n), wq.wq_gemv)
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
+def test_encoder_gemm_tc(oracle_mod, which):
+    w = synth.workload_encoder_gemms()[which]
+    n, m, k = w["n"], w["m"], w["k"]
+    Y = run(wq.wq_gemm, w, flags_extra=wq.WQ_TC_BF16)
+    assert np.isfinite(Y).all()
+    for j0 in (0, m // 2 - 16, m - 32):
+        for round_x, tau in ((False, 8e-3), (True, (k / 16 + 32) * 2.0 ** -23)):
+            Yref, S = oracle_mod.gemm(n, m, k, w["wtype"], w["flags"], w["X"], w["W"],
+                                      bias=w["bias"], residual=w["residual"], round_x=round_x,
+                                      rows=(j0, j0 + 32))
+            sl = slice(j0, j0 + 32)
+            assert_within(Y[:, sl], Yref[:, sl], S[:, sl], tau,
+                          gelu=bool(w["flags"] & wq.WQ_GELU), bias=w["bias"][sl],
+                          R=None if w["residual"] is None else w["residual"][:, sl],
+                          what=f"{w['name']} cols {j0}.. round_x={round_x}")
+
+
+def test_moe_q4_0(oracle_mod):
+    w = synth.workload_moe()
+    E, m, k, nt, tk = w["n_experts"], w["m"], w["k"], w["n_tok"], w["topk"]
+    out = Guarded(nt * tk * m)
+    st = wq.wq_moe_gemv(nt, tk, E, m, k, w["wtype"], w["flags"], dev(w["X"]),
+                        weights_dev(w["W"], w["wtype"], E * m, k), dev(w["ids"]), None, None,
+                        out.view)
+    wq.check(st, w["name"])
+    torch.cuda.synchronize()
+    status_ok()
+    Y = out.result().reshape(nt * tk, m)
+    Yref, S = oracle_mod.moe(nt, tk, E, m, k, w["wtype"], w["flags"], w["X"], w["W"], w["ids"])
+    assert_within(Y, Yref, S, TAU, what=w["name"])
