@@ -9,11 +9,14 @@
 //   warp 0      TMA producer: W tiles [BN rows][64 k] (bf16, 128-byte swizzle)
 //   warp 1      TMEM owner + MMA issuer (one thread): tcgen05.mma kind::f16,
 //               M = 128 (X rows) x N = BN (W rows) x K = 16, f32 accumulator in TMEM
-//   warps 2..9  converters: load X f32 rows (coalesced, two k-blocks in flight),
-//               round to bf16 and store them in the same 128-byte-swizzled
-//               K-major layout the tensor core reads (no extra HBM pass for X);
-//               afterwards the same warps are the epilogue: tcgen05.ld of the
-//               accumulator, bias/GELU/residual, masked f32 stores.
+//   warps 2..17 converters: load X f32 rows (coalesced, four k-blocks in flight
+//               in registers: the register file holds the X data in flight that
+//               shared memory, full of operand stages, cannot), round to bf16 and
+//               store them in the 128-byte-swizzled K-major layout the tensor core
+//               reads (no extra HBM pass for X); afterwards the same warps are the
+//               epilogue: tcgen05.ld of the accumulator, bias and GELU in
+//               registers, then each 32x32 block goes through shared memory so
+//               that residual loads and Y stores are whole 128-byte rows.
 //
 // A/B stages are a 4-deep ring guarded by mbarriers; every wait is bounded.  A
 // wait that runs out sets the CTA's abort flag and WQ_ERR_DEVICE_TIMEOUT; every
@@ -33,7 +36,7 @@ namespace {
 constexpr int BM = 128;           // X rows per tile (tensor-core M)
 constexpr int BK = 64;            // k per stage: one 128-byte swizzle atom of bf16
 constexpr int kStages = 4;
-constexpr int kConvWarps = 8;
+constexpr int kConvWarps = 16;
 constexpr int kThreads = (2 + kConvWarps) * 32;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 
@@ -229,16 +232,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ----------------------------------------------------- X converters
-        const int cw = warp - 2;          // 0..7: rows 16cw .. 16cw+15 of the tile
+        const int cw = warp - 2;          // 0..15: rows 8cw .. 8cw+7 of the tile
         const int half = lane >> 4;       // which of the two rows of one load step
         const int c4 = lane & 15;         // float4 index within the row's 64 k
         bool ok = true;
-        float4 b0[8], b1[8], b2[8];  // k-blocks kb, kb+1, kb+2 (two loads in flight)
-        auto load_block = [&](int kb, float4(&dst)[8]) {
+        float4 b0[4], b1[4], b2[4], b3[4];  // k-blocks kb .. kb+3 (three loads in flight)
+        auto load_block = [&](int kb, float4(&dst)[4]) {
             const int col = kb * BK + 4 * c4;
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
-                const int row = i0 + cw * 16 + 2 * it + half;
+            for (int it = 0; it < 4; ++it) {
+                const int row = i0 + cw * 8 + 2 * it + half;
                 if (row < a.n && col < a.k)
                     dst[it] = __ldg(reinterpret_cast<const float4 *>(a.X + (size_t)row * a.k + col));
                 else
@@ -246,17 +249,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         // Convert block kb from `cur` into stage kb % kStages, after starting the
-        // load of block kb + 2 into `pre`.
-        auto step = [&](int kb, const float4(&cur)[8], float4(&pre)[8]) -> bool {
+        // load of block kb + 3 into `pre`.
+        auto step = [&](int kb, const float4(&cur)[4], float4(&pre)[4]) -> bool {
             const int s = kb % kStages;
-            if (kb + 2 < KB) load_block(kb + 2, pre);
+            if (kb + 3 < KB) load_block(kb + 3, pre);
             if (kb >= kStages &&
                 !wait_or_abort(&empty[s], ((kb / kStages) - 1) & 1, abort_flag, limit, a.status))
                 return false;
             uint8_t *tile = sA + (size_t)s * kABytes;
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
-                const int r = cw * 16 + 2 * it + half;  // row within the tile
+            for (int it = 0; it < 4; ++it) {
+                const int r = cw * 8 + 2 * it + half;  // row within the tile
                 const uint32_t lo = pack_bf16x2(cur[it].x, cur[it].y);
                 const uint32_t hi = pack_bf16x2(cur[it].z, cur[it].w);
                 const int chunk = c4 >> 1;                         // 16-byte chunk of the row
@@ -270,49 +273,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if (KB > 0) load_block(0, b0);
         if (KB > 1) load_block(1, b1);
-        for (int kb = 0; kb < KB && ok; kb += 3) {
-            ok = step(kb, b0, b2);
+        if (KB > 2) load_block(2, b2);
+        for (int kb = 0; kb < KB && ok; kb += 4) {
+            ok = step(kb, b0, b3);
             if (ok && kb + 1 < KB) ok = step(kb + 1, b1, b0);
             if (ok && kb + 2 < KB) ok = step(kb + 2, b2, b1);
+            if (ok && kb + 3 < KB) ok = step(kb + 3, b3, b2);
         }
         // ------------------------------------------------------------ epilogue
         if (ok && wait_or_abort(acc_full, 0, abort_flag, limit, a.status)) {
             tc_fence_after();
-            const int q = warp & 3;                 // TMEM lane quarter of this warp
-            const int hcol = (warp - 2) >> 2;       // which half of the BN columns
-            const int row = i0 + q * 32 + lane;     // X row = TMEM lane
-            for (int c0 = hcol * (BN / 2); c0 < (hcol + 1) * (BN / 2); c0 += 32) {
+            const int q = warp & 3;                  // TMEM lane quarter of this warp
+            const int cg = cw >> 2;                  // which quarter of the BN columns
+            constexpr int kStage = 36;               // staging row stride (floats)
+            // The operand stages are idle now: every MMA has completed.
+            float *stg = reinterpret_cast<float *>(smem) + cw * 32 * kStage;
+            const bool vec = (a.m & 3) == 0;
+            for (int c0 = cg * (BN / 4); c0 < (cg + 1) * (BN / 4); c0 += 32) {
                 float v[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
-                if (row < a.n) {
-                    const int jb = j0 + c0;
-                    const size_t ob = (size_t)row * a.m + jb;
-                    if (jb + 32 <= a.m && (a.m & 3) == 0) {
+                const int jb = j0 + c0;
+                if (a.flags & (kBias | kGelu)) {
 #pragma unroll
-                        for (int c = 0; c < 32; c += 4) {
-                            float4 o;
-                            float *po = &o.x;
-                            float4 rv = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (a.flags & kResidual)
-                                rv = *reinterpret_cast<const float4 *>(a.R + ob + c);
-                            const float *pr = &rv.x;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                float t = v[c + e];
-                                if (a.flags & kBias) t += __ldg(a.bias + jb + c + e);
-                                if (a.flags & kGelu) t = gelu_erf(t);
-                                if (a.flags & kResidual) t += pr[e];
-                                po[e] = t;
-                            }
-                            *reinterpret_cast<float4 *>(a.Y + ob + c) = o;
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            if (jb + c < a.m)
-                                a.Y[ob + c] = epilogue(v[c], a.flags, a.bias + jb + c, a.R + ob + c);
+                    for (int c = 0; c < 32; ++c) {
+                        float t = v[c];
+                        if (a.flags & kBias) t += (jb + c < a.m) ? __ldg(a.bias + jb + c) : 0.f;
+                        if (a.flags & kGelu) t = gelu_erf(t);
+                        v[c] = t;
                     }
                 }
+                // Row `lane` of the 32x32 block into shared memory...
+#pragma unroll
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<float4 *>(&stg[lane * kStage + c]) =
+                        make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+                __syncwarp();
+                // ...then four rows of 128 bytes per warp instruction to global.
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int rr = it * 4 + (lane >> 3), cc = (lane & 7) * 4;
+                    const int row = i0 + q * 32 + rr, col = jb + cc;
+                    if (row >= a.n || col >= a.m) continue;
+                    float4 o = *reinterpret_cast<const float4 *>(&stg[rr * kStage + cc]);
+                    const size_t off = (size_t)row * a.m + col;
+                    if (vec && col + 4 <= a.m) {
+                        if (a.flags & kResidual) {
+                            const float4 r4 = *reinterpret_cast<const float4 *>(a.R + off);
+                            o.x += r4.x; o.y += r4.y; o.z += r4.z; o.w += r4.w;
+                        }
+                        *reinterpret_cast<float4 *>(a.Y + off) = o;
+                    } else {
+                        const float ov[4] = {o.x, o.y, o.z, o.w};
+                        for (int e = 0; e < 4 && col + e < a.m; ++e)
+                            a.Y[off + e] = ov[e] + ((a.flags & kResidual) ? a.R[off + e] : 0.f);
+                    }
+                }
+                __syncwarp();
             }
         }
     }
@@ -368,9 +384,12 @@ cudaError_t launch_bn(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t str
 }  // namespace
 
 cudaError_t launch_gemm_tc(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
+    // Pick the tile width with the smaller (waves x tile time); ties go to 256,
+    // whose X conversion is shared by twice the columns.
     const long long rows = (a.n + BM - 1) / BM;
-    const long long tiles256 = rows * ((a.m + 255) / 256);
-    if (tiles256 * 5 >= (long long)dev.sm_count * 4) return launch_bn<256>(a, dev, stream);
+    const long long w256 = (rows * ((a.m + 255) / 256) + dev.sm_count - 1) / dev.sm_count;
+    const long long w128 = (rows * ((a.m + 127) / 128) + dev.sm_count - 1) / dev.sm_count;
+    if (w256 * 2 <= w128) return launch_bn<256>(a, dev, stream);
     return launch_bn<128>(a, dev, stream);
 }
 

@@ -101,6 +101,8 @@ static wq_status gemv_impl(int n, int m, int k, int wtype, unsigned flags, const
     a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
     a.status = dev->status;
     a.wait_limit = wait_limit();
+    if (mma_gemv_supported(wtype, k))
+        return cuda_status(launch_mma_gemv(a, wtype, *dev, (cudaStream_t)stream));
     return cuda_status(launch_stream_gemv(a, wtype, *dev, (cudaStream_t)stream));
 }
 
@@ -163,6 +165,8 @@ wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtyp
     a.n_experts = n_experts;
     a.status = dev->status;
     a.wait_limit = wait_limit();
+    if (mma_gemv_supported(wtype, k))
+        return cuda_status(launch_mma_moe(a, wtype, *dev, (cudaStream_t)stream));
     return cuda_status(launch_stream_moe(a, wtype, *dev, (cudaStream_t)stream));
 }
 

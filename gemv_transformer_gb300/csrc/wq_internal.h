@@ -63,6 +63,11 @@ cudaError_t launch_stream_gemv(const StreamArgs &a, int wtype, const DeviceInfo 
                                cudaStream_t stream);
 cudaError_t launch_stream_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,
                               cudaStream_t stream);
+bool mma_gemv_supported(int wtype, int k);
+cudaError_t launch_mma_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,
+                            cudaStream_t stream);
+cudaError_t launch_mma_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,
+                           cudaStream_t stream);
 cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev,
                              cudaStream_t stream);
 cudaError_t launch_gemm_tc(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t stream);
