@@ -291,6 +291,11 @@ class Launches:
             b["R"] = (torch.from_numpy(w["residual"]).to(device)
                       if w["residual"] is not None else None)
             b["ids"] = torch.from_numpy(w["ids"]).to(device) if w["kind"] == "moe" else None
+            b["ws"] = None
+            if w["kind"] == "gemm_tc":
+                need = wq.wq_gemm_workspace_bytes(w["n"], m, k, w["wtype"],
+                                                  w["flags"] | wq.WQ_TC_BF16)
+                b["ws"] = torch.empty(need, dtype=torch.uint8, device=device)
             self.bufs.append(b)
         self.wq = wq
 
@@ -300,10 +305,13 @@ class Launches:
             return wq.wq_moe_gemv(w["n_tok"], w["topk"], w["n_experts"], w["m"], w["k"],
                                   w["wtype"], w["flags"], b["X"], b["W"], b["ids"], b["bias"],
                                   b["R"], b["Y"], stream)
+        if w["kind"] == "gemm_tc":
+            flags = w["flags"] | wq.WQ_TC_BF16
+            return wq.wq_gemm_ws(w["n"], w["m"], w["k"], w["wtype"], flags, b["X"], b["W"],
+                                 b["bias"], b["R"], b["Y"], b["ws"], b["ws"].numel(), stream)
         fn = wq.wq_gemv if w["kind"] == "gemv" else wq.wq_gemm
-        flags = w["flags"] | (wq.WQ_TC_BF16 if w["kind"] == "gemm_tc" else 0)
-        return fn(w["n"], w["m"], w["k"], w["wtype"], flags, b["X"], b["W"], b["bias"], b["R"],
-                  b["Y"], stream)
+        return fn(w["n"], w["m"], w["k"], w["wtype"], w["flags"], b["X"], b["W"], b["bias"],
+                  b["R"], b["Y"], stream)
 
     def step(self, stream=None):
         for i in range(len(self.ws)):

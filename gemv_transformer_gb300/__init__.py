@@ -25,8 +25,9 @@ WQ_ERR_DEVICE_TIMEOUT, WQ_ERR_BAD_EXPERT = 4, 5
 WQ_GEMV_MAX_N = 16
 WQ_MOE_MAX_SLOTS = 256
 
-EXPORTS = ("wq_gemm", "wq_gemv", "wq_moe_gemv", "wq_weight_bytes", "wq_dequantize",
-           "wq_get_device_status", "wq_status_string", "wq_set_wait_limit")
+EXPORTS = ("wq_gemm", "wq_gemm_ws", "wq_gemm_workspace_bytes", "wq_gemv", "wq_moe_gemv",
+           "wq_weight_bytes", "wq_dequantize", "wq_get_device_status", "wq_status_string",
+           "wq_set_wait_limit")
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +52,10 @@ def _open(path: str):
     lib.wq_gemm.restype = ci
     lib.wq_gemv.argtypes = gemm_args
     lib.wq_gemv.restype = ci
+    lib.wq_gemm_ws.argtypes = gemm_args[:-1] + [vp, sz, vp]
+    lib.wq_gemm_ws.restype = ci
+    lib.wq_gemm_workspace_bytes.argtypes = [ci, ci, ci, ci, cu]
+    lib.wq_gemm_workspace_bytes.restype = sz
     lib.wq_moe_gemv.argtypes = [ci, ci, ci, ci, ci, ci, cu, vp, vp, vp, vp, vp, vp, vp]
     lib.wq_moe_gemv.restype = ci
     lib.wq_weight_bytes.argtypes = [ci, ci, ci]
@@ -95,6 +100,16 @@ def _s(stream):
 def wq_gemm(n, m, k, wtype, flags, X, W, bias=None, residual=None, Y=None, stream=None) -> int:
     return load().wq_gemm(n, m, k, wtype, flags, _p(X), _p(W), _p(bias), _p(residual), _p(Y),
                           _s(stream))
+
+
+def wq_gemm_ws(n, m, k, wtype, flags, X, W, bias=None, residual=None, Y=None, workspace=None,
+               workspace_bytes=0, stream=None) -> int:
+    return load().wq_gemm_ws(n, m, k, wtype, flags, _p(X), _p(W), _p(bias), _p(residual), _p(Y),
+                             _p(workspace), int(workspace_bytes), _s(stream))
+
+
+def wq_gemm_workspace_bytes(n, m, k, wtype, flags) -> int:
+    return int(load().wq_gemm_workspace_bytes(n, m, k, wtype, flags))
 
 
 def wq_gemv(n, m, k, wtype, flags, X, W, bias=None, residual=None, Y=None, stream=None) -> int:

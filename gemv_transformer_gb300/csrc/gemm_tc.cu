@@ -36,8 +36,15 @@ namespace {
 constexpr int BM = 128;           // X rows per tile (tensor-core M)
 constexpr int BK = 64;            // k per stage: one 128-byte swizzle atom of bf16
 constexpr int kStages = 4;
-constexpr int kConvWarps = 16;
-constexpr int kThreads = (2 + kConvWarps) * 32;
+constexpr int kConvWarps = 16;  // X converters (fused path); they are also the epilogue
+constexpr int kEpiWarps = 8;    // epilogue warps of the path with X already in bf16
+
+// Warps after the producer and MMA warps: converters+epilogue, or epilogue only.
+template <bool ATMA>
+struct Roles {
+    static constexpr int kWork = ATMA ? kEpiWarps : kConvWarps;
+    static constexpr int kThreads = (2 + kWork) * 32;
+};
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 
 template <int BN>
@@ -139,10 +146,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
     }
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const GemmArgs a) {
+// ATMA: X arrives already rounded to bf16 (a workspace written by x_to_bf16) and is
+// loaded by TMA like W; otherwise the converter warps round it from f32.
+template <int BN, bool ATMA>
+__global__ void __launch_bounds__(Roles<ATMA>::kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
+                   const GemmArgs a) {
     using L = Smem<BN>;
+    constexpr int NW = Roles<ATMA>::kWork;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled operand tiles.
     const uint32_t raw = smem_addr(smem_raw);
@@ -196,7 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     !wait_or_abort(&empty[s], ((kb / kStages) - 1) & 1, abort_flag, limit,
                                    a.status))
                     break;
-                mbar_arrive_expect_tx(&b_full[s], (uint32_t)L::kBBytes);
+                if (ATMA) {
+                    mbar_arrive_expect_tx(&b_full[s], (uint32_t)(kABytes + L::kBBytes));
+                    tma_load_2d(sA + (size_t)s * kABytes, &xmap, kb * BK, i0, &b_full[s]);
+                } else {
+                    mbar_arrive_expect_tx(&b_full[s], (uint32_t)L::kBBytes);
+                }
                 tma_load_2d(sB + (size_t)s * L::kBBytes, &wmap, kb * BK, j0, &b_full[s]);
             }
             // Drain: the last kStages loads issued may still be in flight.
@@ -211,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < KB && ok; ++kb) {
                 const int s = kb % kStages;
                 const uint32_t ph = (kb / kStages) & 1;
-                ok = wait_or_abort(&a_full[s], ph, abort_flag, limit, a.status) &&
+                ok = (ATMA || wait_or_abort(&a_full[s], ph, abort_flag, limit, a.status)) &&
                      wait_or_abort(&b_full[s], ph, abort_flag, limit, a.status);
                 if (!ok) break;
                 tc_fence_after();
@@ -236,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = lane >> 4;       // which of the two rows of one load step
         const int c4 = lane & 15;         // float4 index within the row's 64 k
         bool ok = true;
+        const int KBc = ATMA ? 0 : KB;    // k-blocks this warp converts
         float4 b0[4], b1[4], b2[4], b3[4];  // k-blocks kb .. kb+3 (three loads in flight)
         auto load_block = [&](int kb, float4(&dst)[4]) {
             const int col = kb * BK + 4 * c4;
@@ -271,25 +288,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&a_full[s]);
             return true;
         };
-        if (KB > 0) load_block(0, b0);
-        if (KB > 1) load_block(1, b1);
-        if (KB > 2) load_block(2, b2);
-        for (int kb = 0; kb < KB && ok; kb += 4) {
+        if (KBc > 0) load_block(0, b0);
+        if (KBc > 1) load_block(1, b1);
+        if (KBc > 2) load_block(2, b2);
+        for (int kb = 0; kb < KBc && ok; kb += 4) {
             ok = step(kb, b0, b3);
-            if (ok && kb + 1 < KB) ok = step(kb + 1, b1, b0);
-            if (ok && kb + 2 < KB) ok = step(kb + 2, b2, b1);
-            if (ok && kb + 3 < KB) ok = step(kb + 3, b3, b2);
+            if (ok && kb + 1 < KBc) ok = step(kb + 1, b1, b0);
+            if (ok && kb + 2 < KBc) ok = step(kb + 2, b2, b1);
+            if (ok && kb + 3 < KBc) ok = step(kb + 3, b3, b2);
         }
         // ------------------------------------------------------------ epilogue
         if (ok && wait_or_abort(acc_full, 0, abort_flag, limit, a.status)) {
             tc_fence_after();
             const int q = warp & 3;                  // TMEM lane quarter of this warp
-            const int cg = cw >> 2;                  // which quarter of the BN columns
+            constexpr int CW = BN / (NW / 4);        // columns per warp
+            const int cg = cw >> 2;                  // which group of CW columns
             constexpr int kStage = 36;               // staging row stride (floats)
             // The operand stages are idle now: every MMA has completed.
             float *stg = reinterpret_cast<float *>(smem) + cw * 32 * kStage;
             const bool vec = (a.m & 3) == 0;
-            for (int c0 = cg * (BN / 4); c0 < (cg + 1) * (BN / 4); c0 += 32) {
+            for (int c0 = cg * CW; c0 < (cg + 1) * CW; c0 += 32) {
                 float v[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
                 const int jb = j0 + c0;
@@ -357,40 +375,79 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int BN>
-cudaError_t launch_bn(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
-    static std::atomic<unsigned long long> smem_set{0};
+bool encode_bf16_map(CUtensorMap &map, const void *base, int cols, int rows, int box_rows) {
     auto encode = encode_fn();
-    if (!encode) return cudaErrorNotSupported;
-    CUtensorMap map;
-    const cuuint64_t dims[2] = {(cuuint64_t)a.k, (cuuint64_t)a.m};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.k * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BN};
+    if (!encode) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t *>(a.W),
-                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    auto kern = gemm_tc_kernel<BN>;
+    return encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool ATMA>
+cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
+                      cudaStream_t stream) {
+    static std::atomic<unsigned long long> smem_set{0};
+    CUtensorMap wmap, xmap;
+    if (!encode_bf16_map(wmap, a.W, a.k, a.m, BN)) return cudaErrorInvalidValue;
+    if (ATMA) {
+        if (!encode_bf16_map(xmap, xb, a.k, a.n, BM)) return cudaErrorInvalidValue;
+    } else {
+        xmap = wmap;  // unused
+    }
+    auto kern = gemm_tc_kernel<BN, ATMA>;
     cudaError_t err = ensure_smem(kern, (int)Smem<BN>::kBytes, dev, smem_set);
     if (err != cudaSuccess) return err;
     dim3 grid((a.m + BN - 1) / BN, (a.n + BM - 1) / BM);
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-    kern<<<grid, kThreads, Smem<BN>::kBytes, stream>>>(map, a);
+    kern<<<grid, Roles<ATMA>::kThreads, Smem<BN>::kBytes, stream>>>(wmap, xmap, a);
     return cudaGetLastError();
+}
+
+// X f32 -> bf16, round to nearest even (the rounding the fused path applies).
+__global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict__ xb, size_t n4) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const float4 v = __ldg(x + i);
+        xb[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+}
+
+template <bool ATMA>
+cudaError_t launch_tc(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
+                      cudaStream_t stream) {
+    // Pick the tile width with the smaller (waves x tile time); ties go to 256,
+    // whose X tile is shared by twice the columns.
+    const long long rows = (a.n + BM - 1) / BM;
+    const long long w256 = (rows * ((a.m + 255) / 256) + dev.sm_count - 1) / dev.sm_count;
+    const long long w128 = (rows * ((a.m + 127) / 128) + dev.sm_count - 1) / dev.sm_count;
+    if (w256 * 2 <= w128) return launch_bn<256, ATMA>(a, xb, dev, stream);
+    return launch_bn<128, ATMA>(a, xb, dev, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_tc(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
-    // Pick the tile width with the smaller (waves x tile time); ties go to 256,
-    // whose X conversion is shared by twice the columns.
-    const long long rows = (a.n + BM - 1) / BM;
-    const long long w256 = (rows * ((a.m + 255) / 256) + dev.sm_count - 1) / dev.sm_count;
-    const long long w128 = (rows * ((a.m + 127) / 128) + dev.sm_count - 1) / dev.sm_count;
-    if (w256 * 2 <= w128) return launch_bn<256>(a, dev, stream);
-    return launch_bn<128>(a, dev, stream);
+    return launch_tc<false>(a, nullptr, dev, stream);
+}
+
+size_t gemm_tc_workspace_bytes(int n, int k) { return ((size_t)n * k * 2 + 255) & ~(size_t)255; }
+
+cudaError_t launch_gemm_tc_ws(const GemmArgs &a, void *workspace, const DeviceInfo &dev,
+                              cudaStream_t stream) {
+    const size_t n4 = (size_t)a.n * a.k / 4;
+    long long blocks = (long long)((n4 + 255) / 256);
+    const long long cap = (long long)dev.sm_count * 8;
+    if (blocks > cap) blocks = cap;
+    x_to_bf16_kernel<<<(int)blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(a.X),
+                                                     reinterpret_cast<uint2 *>(workspace), n4);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_tc<true>(a, workspace, dev, stream);
 }
 
 }  // namespace wq

@@ -139,6 +139,40 @@ wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X
     return cuda_status(launch_gemm_simt(a, wtype, *dev, (cudaStream_t)stream));
 }
 
+size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned flags) {
+    if (n <= 0 || !shape_ok(wtype, m, k)) return 0;
+    if (!(flags & WQ_TC_BF16) || wtype != kBF16 || n <= WQ_GEMV_MAX_N) return 0;
+    return gemm_tc_workspace_bytes(n, k);
+}
+
+wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                     const void *W, const float *bias, const float *residual, float *Y,
+                     void *workspace, size_t workspace_bytes, wq_stream_t stream) {
+    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
+    if (s != WQ_OK) return s;
+    if ((flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
+    const size_t need = wq_gemm_workspace_bytes(n, m, k, wtype, flags);
+    if (need == 0)
+        return wq_gemm(n, m, k, wtype, flags, X, W, bias, residual, Y, stream);
+    if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < need)
+        return WQ_ERR_INVALID_ARG;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return WQ_ERR_CUDA;
+    GemmArgs a{};
+    a.X = X;
+    a.W = static_cast<const uint8_t *>(W);
+    a.bias = bias;
+    a.R = residual;
+    a.Y = Y;
+    a.n = n;
+    a.m = m;
+    a.k = k;
+    a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
+    a.status = dev->status;
+    a.wait_limit = wait_limit();
+    return cuda_status(launch_gemm_tc_ws(a, workspace, *dev, (cudaStream_t)stream));
+}
+
 wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtype,
                       unsigned flags, const float *X, const void *Wbank, const int32_t *ids,
                       const float *bias, const float *residual, float *Y, wq_stream_t stream) {

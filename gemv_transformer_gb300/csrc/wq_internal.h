@@ -71,6 +71,9 @@ cudaError_t launch_mma_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev
 cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev,
                              cudaStream_t stream);
 cudaError_t launch_gemm_tc(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t stream);
+size_t gemm_tc_workspace_bytes(int n, int k);
+cudaError_t launch_gemm_tc_ws(const GemmArgs &a, void *workspace, const DeviceInfo &dev,
+                              cudaStream_t stream);
 cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out,
                            cudaStream_t stream);
 

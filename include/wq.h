@@ -116,6 +116,28 @@ WQ_API wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const f
                   const float *bias, const float *residual, float *Y, wq_stream_t stream);
 
 /*
+ * wq_gemm with a caller-provided device workspace, which lets the tensor-core path
+ * round X to bf16 once in a separate pass (into the workspace) and then feed both
+ * operands to the tcgen05 kernel by TMA; that is faster than rounding X inside the
+ * GEMM, where the f32 X in flight does not fit on chip.  The results are
+ * identical to wq_gemm's (same rounding, same accumulation order per output).
+ * workspace: device memory of at least wq_gemm_workspace_bytes(n, m, k, wtype,
+ * flags) bytes, 256-byte aligned, not overlapping any other argument; it is
+ * overwritten and may be reused once the stream has passed this call.  When that
+ * size is 0 the workspace is not touched and may be NULL.
+ * Errors: as wq_gemm, plus WQ_ERR_INVALID_ARG for a missing, misaligned or too
+ * small workspace when one is needed.
+ */
+WQ_API wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                            const void *W, const float *bias, const float *residual, float *Y,
+                            void *workspace, size_t workspace_bytes, wq_stream_t stream);
+
+/* Workspace bytes wq_gemm_ws needs for this call: 2*n*k rounded up to 256 when the
+ * call takes the tensor-core path (WQ_TC_BF16, WQ_BF16 weights, n > WQ_GEMV_MAX_N),
+ * else 0.  0 also for an invalid shape. */
+WQ_API size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned flags);
+
+/*
  * Same contract as wq_gemm for small n (1 <= n <= WQ_GEMV_MAX_N): the
  * HBM-bound path that streams each weight byte once (hanzo-ml matvec_q*_gpu).
  * WQ_TC_BF16 is rejected (WQ_ERR_INVALID_ARG).

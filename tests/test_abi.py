@@ -80,6 +80,20 @@ def test_invalid_arguments_rejected_on_host(lib, call):
     assert call() == wq.WQ_ERR_INVALID_ARG
 
 
+def test_workspace_sizes_and_errors(lib):
+    TC = wq.WQ_TC_BF16
+    assert wq.wq_gemm_workspace_bytes(1500, 3072, 1024, wq.WQ_BF16, TC) == 1500 * 1024 * 2
+    assert wq.wq_gemm_workspace_bytes(1500, 3072, 1000, wq.WQ_BF16, TC) == 3_000_064  # -> 256
+    assert wq.wq_gemm_workspace_bytes(16, 3072, 1024, wq.WQ_BF16, TC) == 0   # GEMV route
+    assert wq.wq_gemm_workspace_bytes(1500, 3072, 1024, wq.WQ_BF16, 0) == 0  # f32-FMA route
+    assert wq.wq_gemm_workspace_bytes(1500, 3072, 1024, wq.WQ_Q8_0, TC) == 0
+    need = wq.wq_gemm_workspace_bytes(32, 64, 64, wq.WQ_BF16, TC)
+    call = lambda ws, nb: wq.wq_gemm_ws(32, 64, 64, wq.WQ_BF16, TC, A, A, None, None, A, ws, nb, 0)
+    assert call(None, need) == wq.WQ_ERR_INVALID_ARG          # missing
+    assert call(A + 16, need) == wq.WQ_ERR_INVALID_ARG        # not 256-byte aligned
+    assert call(A, need - 1) == wq.WQ_ERR_INVALID_ARG         # too small
+
+
 def test_unsupported_requests(lib):
     assert wq.wq_gemm(32, 8, 32, wq.WQ_Q8_0, wq.WQ_TC_BF16, A, A, None, None, A, 0) == \
         wq.WQ_ERR_UNSUPPORTED

@@ -35,28 +35,37 @@ def built():
     status_ok()
 
 
-def run_tc(n, m, k, flags, X, img, bias=None, R=None, inplace=False):
+def run_tc(n, m, k, flags, X, img, bias=None, R=None, inplace=False, ws=False):
+    """wq_gemm (X rounded inside the GEMM) or, with ws=True, wq_gemm_ws (X rounded
+    into a workspace by a separate pass, then both operands by TMA)."""
     if inplace:
         out = Guarded(n * m, R)
         Rd = out.view
     else:
         out = Guarded(n * m)
         Rd = dev(R) if R is not None else None
-    st = wq.wq_gemm(n, m, k, BF16, flags | TC, dev(X), weights_dev(img, BF16, m, k),
-                    dev(bias) if bias is not None else None, Rd, out.view)
+    args = (n, m, k, BF16, flags | TC, dev(X), weights_dev(img, BF16, m, k),
+            dev(bias) if bias is not None else None, Rd, out.view)
+    if ws:
+        need = wq.wq_gemm_workspace_bytes(n, m, k, BF16, flags | TC)
+        assert need >= 2 * n * k
+        work = torch.empty(need, dtype=torch.uint8, device="cuda")
+        st = wq.wq_gemm_ws(*args, work, need)
+    else:
+        st = wq.wq_gemm(*args)
     wq.check(st, "wq_gemm(TC)")
     torch.cuda.synchronize()
     status_ok()
     return out.result().reshape(n, m)
 
 
-def check_tc(oracle_mod, n, m, k, flags, seed, rows=None, inplace=False, std=0.03):
+def check_tc(oracle_mod, n, m, k, flags, seed, rows=None, inplace=False, std=0.03, ws=False):
     g = synth.rng(seed)
     X = synth.normal_f32(g, (n, k))
     img = synth.draw_bf16_weights(g, m, k, std)
     bias = synth.normal_f32(g, (m,), 0.1) if flags & BIAS else None
     R = synth.normal_f32(g, (n, m)) if flags & RES else None
-    Y = run_tc(n, m, k, flags, X, img, bias, R, inplace=inplace)
+    Y = run_tc(n, m, k, flags, X, img, bias, R, inplace=inplace, ws=ws)
     j0, j1 = rows if rows else (0, m)
     gelu = bool(flags & GELU)
     for round_x, tau in ((False, TAU_TC), (True, tau_exact(k))):
@@ -69,20 +78,37 @@ def check_tc(oracle_mod, n, m, k, flags, seed, rows=None, inplace=False, std=0.0
     return Y
 
 
+@pytest.mark.parametrize("ws", [False, True], ids=["fused", "workspace"])
 @pytest.mark.parametrize("shape", [(17, 16, 8), (128, 128, 64), (130, 256, 128), (300, 520, 1032),
                                    (257, 300, 200), (1000, 1000, 512), (64, 2048, 256)])
-def test_tc_shapes(oracle_mod, shape):
+def test_tc_shapes(oracle_mod, shape, ws):
     n, m, k = shape
-    check_tc(oracle_mod, n, m, k, BIAS, seed=n + m + k)
+    check_tc(oracle_mod, n, m, k, BIAS, seed=n + m + k, ws=ws)
 
 
+@pytest.mark.parametrize("ws", [False, True], ids=["fused", "workspace"])
 @pytest.mark.parametrize("flags", [0, BIAS, GELU, BIAS | GELU, RES, BIAS | RES, BIAS | GELU | RES])
-def test_tc_epilogues(oracle_mod, flags):
-    check_tc(oracle_mod, 200, 384, 320, flags, seed=flags)
+def test_tc_epilogues(oracle_mod, flags, ws):
+    check_tc(oracle_mod, 200, 384, 320, flags, seed=flags, ws=ws)
 
 
-def test_tc_residual_in_place_ragged_m(oracle_mod):
-    check_tc(oracle_mod, 150, 203, 264, BIAS | RES, seed=3, inplace=True)
+@pytest.mark.parametrize("ws", [False, True], ids=["fused", "workspace"])
+def test_tc_residual_in_place_ragged_m(oracle_mod, ws):
+    check_tc(oracle_mod, 150, 203, 264, BIAS | RES, seed=3, inplace=True, ws=ws)
+
+
+@pytest.mark.parametrize("shape", [(300, 520, 1032), (1500, 1024, 4096)])
+def test_tc_workspace_path_bit_identical(shape):
+    """Both tensor-core paths round X the same way and accumulate in the same
+    order, so their outputs agree bit for bit."""
+    n, m, k = shape
+    g = synth.rng(17)
+    X = synth.normal_f32(g, (n, k))
+    img = synth.draw_bf16_weights(g, m, k, 0.03)
+    b = synth.normal_f32(g, (m,), 0.1)
+    Y1 = run_tc(n, m, k, BIAS | GELU, X, img, b)
+    Y2 = run_tc(n, m, k, BIAS | GELU, X, img, b, ws=True)
+    assert (Y1.view(np.int32) == Y2.view(np.int32)).all()
 
 
 def test_tc_integer_exact():
@@ -109,23 +135,37 @@ def test_tc_deterministic():
     assert (Y1.view(np.int32) == Y2.view(np.int32)).all()
 
 
-def test_tc_wait_limit_expires_without_hang(oracle_mod):
-    """A one-poll wait limit aborts every CTA of the tensor-core kernel: it records
-    WQ_ERR_DEVICE_TIMEOUT, drains its TMA copies and MMAs, frees TMEM and returns;
-    the next call with the default limit is correct."""
-    n, m, k = 512, 1024, 1024
+@pytest.mark.parametrize("ws", [False, True], ids=["fused", "workspace"])
+def test_tc_wait_limit_expires_without_hang(oracle_mod, ws):
+    """A one-poll wait limit aborts the tensor-core kernel's CTAs at their first
+    unfilled stage: they record WQ_ERR_DEVICE_TIMEOUT, drain their TMA copies and
+    MMAs, free TMEM and return; the next call with the default limit is correct."""
+    n, m, k = 512, 1024, 4096
     g = synth.rng(6)
     X = synth.normal_f32(g, (n, k))
     img = synth.draw_bf16_weights(g, m, k, 0.03)
     Xd, Wd = dev(X), weights_dev(img, BF16, m, k)
     Y = torch.zeros(n * m, device="cuda")
+    need = wq.wq_gemm_workspace_bytes(n, m, k, BF16, TC)
+    work = torch.empty(need, dtype=torch.uint8, device="cuda")
+
+    def call():
+        if ws:
+            return wq.wq_gemm_ws(n, m, k, BF16, TC, Xd, Wd, None, None, Y, work, need)
+        return wq.wq_gemm(n, m, k, BF16, TC, Xd, Wd, None, None, Y)
+
+    seen = []
     wq.wq_set_wait_limit(1)
     try:
-        wq.check(wq.wq_gemm(n, m, k, BF16, TC, Xd, Wd, None, None, Y))
-        assert wq.wq_get_device_status() == wq.WQ_ERR_DEVICE_TIMEOUT
+        for _ in range(5):
+            wq.check(call())
+            seen.append(wq.wq_get_device_status())
+            if seen[-1] == wq.WQ_ERR_DEVICE_TIMEOUT:
+                break
     finally:
         wq.wq_set_wait_limit(0)
-    wq.check(wq.wq_gemm(n, m, k, BF16, TC, Xd, Wd, None, None, Y))
+    assert wq.WQ_ERR_DEVICE_TIMEOUT in seen, seen
+    wq.check(call())
     status_ok()
     Yref, S = oracle_mod.gemm(n, m, k, BF16, 0, X, img, round_x=True, rows=(0, 64))
     assert_within(Y.cpu().numpy().reshape(n, m)[:, :64], Yref[:, :64], S[:, :64], tau_exact(k))

@@ -31,8 +31,14 @@ def run(fn, w, flags_extra=0):
     out = Guarded(n * m)
     b = dev(w["bias"]) if w["bias"] is not None else None
     R = dev(w["residual"]) if w["residual"] is not None else None
-    st = fn(n, m, k, w["wtype"], w["flags"] | flags_extra, dev(w["X"]),
+    args = (n, m, k, w["wtype"], w["flags"] | flags_extra, dev(w["X"]),
             weights_dev(w["W"], w["wtype"], m, k), b, R, out.view)
+    if fn is wq.wq_gemm_ws:
+        need = wq.wq_gemm_workspace_bytes(n, m, k, w["wtype"], w["flags"] | flags_extra)
+        work = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        st = fn(*args, work, need)
+    else:
+        st = fn(*args)
     wq.check(st, w["name"])
     torch.cuda.synchronize()
     status_ok()
@@ -60,11 +66,12 @@ def test_q4_0_gemv_residual(oracle_mod, n):
     check_full(oracle_mod, synth.workload_q4_0_gemv(n=n), wq.wq_gemv)
 
 
+@pytest.mark.parametrize("fn", [wq.wq_gemm, wq.wq_gemm_ws], ids=["fused", "workspace"])
 @pytest.mark.parametrize("which", [0, 1, 2])
-def test_encoder_gemm_tc(oracle_mod, which):
+def test_encoder_gemm_tc(oracle_mod, which, fn):
     w = synth.workload_encoder_gemms()[which]
     n, m, k = w["n"], w["m"], w["k"]
-    Y = run(wq.wq_gemm, w, flags_extra=wq.WQ_TC_BF16)
+    Y = run(fn, w, flags_extra=wq.WQ_TC_BF16)
     assert np.isfinite(Y).all()
     for j0 in (0, m // 2 - 16, m - 32):
         for round_x, tau in ((False, 8e-3), (True, (k / 16 + 32) * 2.0 ** -23)):
