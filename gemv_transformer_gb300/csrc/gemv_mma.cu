@@ -16,16 +16,23 @@
 // The block scale d is applied once per 32-weight block per row (an f32x2 FMA
 // on the MMA's partial sums), as in the block definition w = d*q.
 //
-// Data movement: 16-row x 512-weight tiles of W are streamed with TMA (2-D
-// tensor map over the byte image, two 8-block boxes per tile) into a ring of
-// shared-memory stages.  Each of the 16 warps owns one 32-weight block of every
+// Data movement: a stage holds one 512-weight chunk of every row of the CTA's
+// current row group, loaded by a producer warp as one tall TMA box (2-D tensor
+// map over the byte image; two boxes for Q8_0), since a TMA request's cost is
+// per request and tall boxes keep HBM streaming at full rate.  The producer is a
+// warp of its own because a TMA issue blocks its thread while the engine takes
+// the box.  Each of the 16 consumer warps owns one 32-weight block of every
 // stage, prefetches its X one stage ahead, builds its B fragments once and
-// applies them to all row tiles of the CTA.  There is no producer warp: the
-// last warp to finish with a stage (a shared-memory arrival count) issues the
-// TMA that refills it, so every warp computes and none blocks on a refill.  The
-// 16 warps' partial sums are reduced in shared memory in a fixed order
-// (deterministic), the three splits are summed, and the epilogue (bias,
-// erf-GELU, residual) is fused into the store.
+// applies them to all row tiles of the group.
+//
+// Column layouts of the MMA (n = tokens of a pass): for 1-2 tokens the three
+// splits of each token are packed into one n-tile (column s*P + i); for 3-8
+// tokens n-tile s holds split s of token i in column i, so a thread's three
+// n-tile results are the same token's three splits and one accumulator chain
+// sums them; 9-16 tokens use six n-tiles the same way (two token halves).
+// The partial sums of the 16 warps are reduced in shared memory in a fixed
+// order (deterministic) and the epilogue (bias, erf-GELU, residual) is fused
+// into the store.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -38,37 +45,43 @@ namespace wq {
 namespace {
 
 constexpr int kCW = 16;                  // consumer warps (one block of each chunk each)
-constexpr int kThreads = kCW * 32;       // no producer warp: the last warp to free a stage refills it
-constexpr int kBoxBlocks = 8;            // blocks per TMA box row (inner box <= 256 u16)
-constexpr int kChunk = kCW * 32;         // weights per row per stage (16 blocks)
+constexpr int kThreads = (kCW + 1) * 32; // + one producer warp
+constexpr int kBlocks = 16;              // blocks (of 32 weights) per chunk
 constexpr int kMaxSlots = 256;
 constexpr int kRedBufs = 4;              // partial-sum buffers of the ordered reduction
 
+// A stage holds, for every row of the group, the 16 blocks (512 weights) of one
+// chunk, loaded as NBOX tall TMA boxes (the box inner size is at most 256 u16, so
+// Q8_0's 544-byte chunk row takes two boxes of 8 blocks).
 template <int WT>
 struct Fmt;
 template <>
 struct Fmt<kQ4_0> {
-    static constexpr int BB = 18;                 // block bytes
-    static constexpr int BOX = kBoxBlocks * 18;   // bytes of one box row (144)
+    static constexpr int BB = 18;     // block bytes
+    static constexpr int BOXB = 16;   // blocks per box row
+    static constexpr int NBOX = 1;
+    static constexpr int ROWB = 288;  // bytes per box row
 };
 template <>
 struct Fmt<kQ8_0> {
     static constexpr int BB = 34;
-    static constexpr int BOX = kBoxBlocks * 34;   // 272
+    static constexpr int BOXB = 8;
+    static constexpr int NBOX = 2;
+    static constexpr int ROWB = 272;
 };
 
-// Accumulator columns per row: per (split, token) column, or per token when the
-// three split partials are summed in-thread (PF = 8 or 16 tokens per pass).
-template <int NT, int PF>
+// Accumulator columns per row of the reduction buffer: 8 (one n-tile), 16 when wide.
+template <bool WIDE>
 struct Cols {
-    static constexpr int C = PF ? PF : NT * 8;
+    static constexpr int C = WIDE ? 16 : 8;
 };
 
-template <int WT, int NT, int T, int PF>
+template <int WT, bool WIDE, int T>
 struct Layout {
-    static constexpr int kTileBytes = 2 * 16 * Fmt<WT>::BOX;  // 16 rows x 2 boxes
-    static constexpr int kStageBytes = T * kTileBytes;
-    static constexpr int kRedBytes = kRedBufs * T * 16 * Cols<NT, PF>::C * 4;
+    static constexpr int kTileBytes = 16 * Fmt<WT>::ROWB;       // one tile, one box
+    static constexpr int kBoxBytes = T * kTileBytes;            // the group's rows, one box
+    static constexpr int kStageBytes = Fmt<WT>::NBOX * kBoxBytes;
+    static constexpr int kRedBytes = kRedBufs * T * 16 * Cols<WIDE>::C * 4;
     static constexpr int kBudget = 200 * 1024 - kRedBytes;
     static constexpr int kStages = (kBudget / kStageBytes) > 8 ? 8 : (kBudget / kStageBytes);
     static_assert(kStages >= 2, "at least two stages");
@@ -101,6 +114,16 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A.B with a zero accumulator input.
+__device__ __forceinline__ void mma_bf16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                           uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 // acc[0..1] += d0 * p[0..1]; acc[2..3] += d1 * p[2..3] (packed f32x2 FMAs).
@@ -185,23 +208,23 @@ __device__ __forceinline__ int group_tiles(const Sched &sc, long long u) {
     return (int)(e - u);
 }
 
-template <int WT, bool MOE, int NT, int T, int PF>
+template <int WT, bool MOE, bool WIDE, int T>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const StreamArgs a) {
-    using L = Layout<WT, NT, T, PF>;
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap_t,
+                    const __grid_constant__ CUtensorMap wmap_1, const StreamArgs a) {
+    using L = Layout<WT, WIDE, T>;
     constexpr int S = L::kStages;
-    constexpr int C = Cols<NT, PF>::C;
-    // Tokens per pass: PF when fixed, else what NT n-tiles hold (3 splits each).
-    constexpr int P_MAX = PF ? PF : ((NT * 8) / 3 >= 4 ? 4 : 2);
+    constexpr int C = Cols<WIDE>::C;
+    constexpr int P_MAX = WIDE ? 16 : 8;   // tokens per pass
+    constexpr int NT = WIDE ? 6 : 3;       // n-tiles at most
+    constexpr int NH = WIDE ? 2 : 1;       // tokens per thread in the split-major layout
+    constexpr int NA = NH;                 // accumulator groups per tile
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *stages = smem;
     float *red = reinterpret_cast<float *>(smem + (size_t)S * L::kStageBytes);  // [4][T*16][C]
     uint64_t *full = reinterpret_cast<uint64_t *>(red + kRedBufs * T * 16 * C);
-    unsigned *released = reinterpret_cast<unsigned *>(full + S);   // [S] warp releases per stage
-    unsigned *issued = released + S;                               // loads issued so far
-    // 64-bit keys: round the offset up to 16 bytes (S may be odd).
-    unsigned long long *s_key = reinterpret_cast<unsigned long long *>(
-        (reinterpret_cast<uintptr_t>(issued + 2) + 15) & ~(uintptr_t)15);
+    uint64_t *empty = full + S;
+    unsigned long long *s_key = reinterpret_cast<unsigned long long *>(empty + S);
     int *s_sorted = reinterpret_cast<int *>(s_key + kMaxSlots);
     int *s_seg = s_sorted + kMaxSlots;
     int *s_act = s_seg + kMaxSlots + 1;
@@ -211,16 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int m = a.m, k = a.k;
-    const int nb = k / 32;                    // blocks per row
-    const int KC = (nb + kCW - 1) / kCW;      // chunks per row (last may be half)
+    const int nb = k / 32;                          // blocks per row
+    const int KC = (nb + kBlocks - 1) / kBlocks;    // chunks per row (last may be half)
     const uint64_t limit = a.wait_limit;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            released[s] = 0u;
+            mbar_init(&empty[s], kCW);
         }
-        *issued = 0u;
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -243,21 +265,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_sorted[r] = q;
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int na = 0, prev = -1, r = 0;
-            for (; r < Sl; ++r) {
-                const unsigned long long kr = s_key[s_sorted[r]];
-                if (kr & big) break;
-                const int e = (int)(kr >> 16);
-                if (e != prev) {
-                    s_seg[na] = r;
-                    s_act[na] = e;
-                    ++na;
-                    prev = e;
+        if (warp == 0) {  // segment starts of the sorted slots, by ballot and prefix count
+            int na = 0;
+            for (int base = 0; base < Sl; base += 32) {
+                const int r = base + lane;
+                bool valid = false, start = false;
+                int e = 0;
+                if (r < Sl) {
+                    const unsigned long long kr = s_key[s_sorted[r]];
+                    valid = !(kr & big);
+                    e = (int)(kr >> 16);
+                    start = valid && (r == 0 || (int)(s_key[s_sorted[r - 1]] >> 16) != e);
+                }
+                const unsigned sm = __ballot_sync(0xFFFFFFFFu, start);
+                if (start) {
+                    const int idx = na + __popc(sm & ((1u << lane) - 1u));
+                    s_seg[idx] = r;
+                    s_act[idx] = e;
+                }
+                na += __popc(sm);
+                const unsigned vm = __ballot_sync(0xFFFFFFFFu, valid);
+                if (vm != 0xFFFFFFFFu) {  // the first invalid slot ends the valid ones
+                    if (lane == 0) {
+                        s_seg[na] = base + __popc(vm);
+                        *s_nact = na;
+                    }
+                    break;
+                }
+                if (base + 32 >= Sl && lane == 0) {
+                    s_seg[na] = Sl;
+                    *s_nact = na;
                 }
             }
-            s_seg[na] = r;
-            *s_nact = na;
         }
         __syncthreads();
         sc.n_act = *s_nact;
@@ -283,50 +322,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         return MOE ? s_act[ai] * m + j : j;
     };
 
-    // Load cursor: (row group start u, pass start p0, chunk c) of a stage load, in
-    // the order the warps consume stages.
-    struct Cursor {
-        long long u;
-        int p0, c;
-    };
-    auto advance = [&](Cursor &cu) {
-        if (++cu.c < KC) return;
-        cu.c = 0;
-        int seg0;
-        const int ntok = group_tokens(cu.u, seg0);
-        cu.p0 += P_MAX;
-        if (cu.p0 < ntok) return;
-        cu.p0 = 0;
-        cu.u += group_tiles<T>(sc, cu.u);
-    };
-    const uint64_t policy = l2_evict_first();
-    auto issue = [&](const Cursor &cu, long long q) {
-        const int s = (int)(q % S);
-        const int nt = group_tiles<T>(sc, cu.u);
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(nt * L::kTileBytes));
-        uint8_t *dst = stages + (size_t)s * L::kStageBytes;
-        for (int tt = 0; tt < nt; ++tt) {
-            const int y = tile_row(cu.u + tt);
-            for (int bx = 0; bx < 2; ++bx)
-                tma_load_2d(dst + tt * L::kTileBytes + bx * 16 * Fmt<WT>::BOX, &wmap,
-                            (cu.c * 2 + bx) * (Fmt<WT>::BOX / 2), y, &full[s], policy);
+    if (warp == kCW) {
+        // ------------------------------------------------------------ producer
+        // A full group is one tall box per NBOX (T tiles of rows); a short group
+        // takes one 16-row box per tile.
+        if (lane == 0) {
+            const uint64_t policy = l2_evict_first();
+            long long q = 0;
+            bool ok = true;
+            for (long long u = sc.u0; u < sc.u1 && ok;) {
+                const int nt = group_tiles<T>(sc, u);
+                int seg0;
+                const int ntok = group_tokens(u, seg0);
+                for (int p0 = 0; p0 < ntok && ok; p0 += P_MAX) {
+                    for (int c = 0; c < KC; ++c, ++q) {
+                        const int s = (int)(q % S);
+                        if (q >= S) {
+                            const uint32_t par = (uint32_t)(((q / S) - 1) & 1);
+                            bool w = mbar_test_wait(&empty[s], par);
+                            for (uint64_t i = 1; !w && i < limit && !*abort_flag; ++i)
+                                w = mbar_try_wait(&empty[s], par);
+                            if (!w) {
+                                if (!*abort_flag) record_status(a.status, kStTimeout);
+                                *abort_flag = 1u;
+                                ok = false;
+                                break;
+                            }
+                        }
+                        mbar_arrive_expect_tx(&full[s],
+                                              (uint32_t)(Fmt<WT>::NBOX * nt * L::kTileBytes));
+                        uint8_t *dst = stages + (size_t)s * L::kStageBytes;
+                        for (int bx = 0; bx < Fmt<WT>::NBOX; ++bx) {
+                            const int x = (c * Fmt<WT>::NBOX + bx) * (Fmt<WT>::ROWB / 2);
+                            if (nt == T) {
+                                tma_load_2d(dst + bx * L::kBoxBytes, &wmap_t, x, tile_row(u),
+                                            &full[s], policy);
+                            } else {
+                                for (int tt = 0; tt < nt; ++tt)
+                                    tma_load_2d(dst + bx * L::kBoxBytes + tt * L::kTileBytes,
+                                                &wmap_1, x, tile_row(u + tt), &full[s], policy);
+                            }
+                        }
+                    }
+                }
+                u += nt;
+            }
+            for (long long d = (q > S ? q - S : 0); d < q; ++d)
+                mbar_wait(&full[d % S], (uint32_t)((d / S) & 1), kDrainPolls);
         }
-    };
-    // Every warp's lane 0 keeps the cursor of the load S stages ahead of it.
-    Cursor ahead{sc.u0, 0, 0};
-    if (lane == 0) {
-        unsigned n_init = 0;
-        for (long long i = 0; i < S && ahead.u < sc.u1; ++i, ++n_init) {
-            if (warp == 0) issue(ahead, i);
-            advance(ahead);
-        }
-        if (warp == 0) atomicAdd(issued, n_init);
+        return;
     }
 
     // ---------------------------------------------------------------- consumers
     long long q = 0;
     bool ok = true;
-    const int bx = warp >> 3, bi = warp & 7;  // this warp's block: box and slot in the box
     for (long long u = sc.u0; u < sc.u1 && ok;) {
         const int ntiles = group_tiles<T>(sc, u);
         int seg0;
@@ -336,29 +385,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row0 = (int)(u % sc.tpe) * 16;
         for (int p0 = 0; p0 < ntok_all && ok; p0 += P_MAX) {
             const int ntok = min(P_MAX, ntok_all - p0);
-            // Column layout: c = s * P + i (split s, token i); P | 8 or P = 16.
-            const int P = PF ? PF : (ntok <= 1 ? 1 : (ntok <= 2 ? 2 : 4));
-            constexpr int NH = PF == 16 ? 2 : 1;   // tokens per thread
+            // packed: 1-2 tokens, column g = split (g / P) of token (g % P), one n-tile;
+            // else split-major: n-tile s, column g = token g (+8 for the second half).
+            const bool packed = !WIDE && ntok <= 2;
+            const int P = packed ? ntok : (WIDE ? 16 : 8);
             int xrow[NH];
             bool tok_ok[NH];
+            int col_s = 0;  // packed: which split this thread's column carries
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
-                const int i = (h * 8 + g) % P;
-                tok_ok[h] = i < ntok;
+                const int i = packed ? g % P : h * 8 + g;
+                tok_ok[h] = packed ? (g < 3 * P) : (i < ntok);
                 const int r = p0 + (tok_ok[h] ? i : 0);
                 xrow[h] = MOE ? s_sorted[seg0 + r] / a.topk : r;
             }
-            // Runtime column bookkeeping (PF == 0 only): split index and validity.
-            int col_s[NT];
-            bool col_ok[NT];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int c = nt * 8 + g;
-                col_s[nt] = c / P;
-                col_ok[nt] = c < 3 * P && tok_ok[0];
-            }
+            if (packed) col_s = g / P;
 
-            constexpr int NA = PF == 0 ? NT : NH;  // accumulator groups per tile
             float acc[T][NA][4];
 #pragma unroll
             for (int tt = 0; tt < T; ++tt)
@@ -367,31 +409,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int r = 0; r < 4; ++r) acc[tt][j][r] = 0.f;
 
-            // X of this warp's block, prefetched one chunk ahead.
-            auto load_x = [&](int c, float (&xv)[NH][8]) {
-                const int blk = c * kCW + warp;
+            // X of this warp's block of a chunk.
+            auto load_x = [&](int c, float (&xv)[1][NH][8]) {
 #pragma unroll
-                for (int h = 0; h < NH; ++h) {
-                    float4 u0v = make_float4(0.f, 0.f, 0.f, 0.f), u1v = u0v;
-                    if (blk < nb && tok_ok[h]) {
-                        const float *xp = a.X + (size_t)xrow[h] * k + (size_t)blk * 32;
-                        if (WT == kQ4_0) {
-                            u0v = __ldg(reinterpret_cast<const float4 *>(xp + 4 * t));
-                            u1v = __ldg(reinterpret_cast<const float4 *>(xp + 16 + 4 * t));
-                        } else {
-                            u0v = __ldg(reinterpret_cast<const float4 *>(xp + 8 * t));
-                            u1v = __ldg(reinterpret_cast<const float4 *>(xp + 8 * t + 4));
+                for (int hb = 0; hb < 1; ++hb) {
+                    const int blk = c * kBlocks + warp;
+#pragma unroll
+                    for (int h = 0; h < NH; ++h) {
+                        float4 u0v = make_float4(0.f, 0.f, 0.f, 0.f), u1v = u0v;
+                        if (blk < nb && tok_ok[h]) {
+                            const float *xp = a.X + (size_t)xrow[h] * k + (size_t)blk * 32;
+                            if (WT == kQ4_0) {
+                                u0v = __ldg(reinterpret_cast<const float4 *>(xp + 4 * t));
+                                u1v = __ldg(reinterpret_cast<const float4 *>(xp + 16 + 4 * t));
+                            } else {
+                                u0v = __ldg(reinterpret_cast<const float4 *>(xp + 8 * t));
+                                u1v = __ldg(reinterpret_cast<const float4 *>(xp + 8 * t + 4));
+                            }
                         }
+                        xv[hb][h][0] = u0v.x; xv[hb][h][1] = u0v.y;
+                        xv[hb][h][2] = u0v.z; xv[hb][h][3] = u0v.w;
+                        xv[hb][h][4] = u1v.x; xv[hb][h][5] = u1v.y;
+                        xv[hb][h][6] = u1v.z; xv[hb][h][7] = u1v.w;
                     }
-                    xv[h][0] = u0v.x; xv[h][1] = u0v.y; xv[h][2] = u0v.z; xv[h][3] = u0v.w;
-                    xv[h][4] = u1v.x; xv[h][5] = u1v.y; xv[h][6] = u1v.z; xv[h][7] = u1v.w;
                 }
             };
-            float xcur[NH][8];
+            float xcur[1][NH][8];
             load_x(0, xcur);
 
             for (int c = 0; c < KC; ++c, ++q) {
-                float xnext[NH][8];
+                float xnext[1][NH][8];
                 if (c + 1 < KC) load_x(c + 1, xnext);
                 const int s = (int)(q % S);
                 bool w = mbar_test_wait(&full[s], (uint32_t)((q / S) & 1));
@@ -406,22 +453,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const int blk = c * kCW + warp;
-                if (blk < nb) {
+#pragma unroll
+                for (int hb = 0; hb < 1; ++hb) {
+                    const int wb = warp;             // block within the chunk (0..15)
+                    const int blk = c * kBlocks + wb;
+                    if (blk >= nb) continue;
                     // Exact 3-term split of X, pairs in the element order of the A decode.
                     uint32_t sp[NH][4][3];
 #pragma unroll
                     for (int h = 0; h < NH; ++h) {
+                        const float *xv = xcur[hb][h];
                         if (WT == kQ4_0) {  // pairs (0,2), (1,3) of each nibble group
-                            split3(xcur[h][0], xcur[h][2], sp[h][0][0], sp[h][0][1], sp[h][0][2]);
-                            split3(xcur[h][1], xcur[h][3], sp[h][1][0], sp[h][1][1], sp[h][1][2]);
-                            split3(xcur[h][4], xcur[h][6], sp[h][2][0], sp[h][2][1], sp[h][2][2]);
-                            split3(xcur[h][5], xcur[h][7], sp[h][3][0], sp[h][3][1], sp[h][3][2]);
+                            split3(xv[0], xv[2], sp[h][0][0], sp[h][0][1], sp[h][0][2]);
+                            split3(xv[1], xv[3], sp[h][1][0], sp[h][1][1], sp[h][1][2]);
+                            split3(xv[4], xv[6], sp[h][2][0], sp[h][2][1], sp[h][2][2]);
+                            split3(xv[5], xv[7], sp[h][3][0], sp[h][3][1], sp[h][3][2]);
                         } else {            // pairs (0,1), (2,3), (4,5), (6,7)
-                            split3(xcur[h][0], xcur[h][1], sp[h][0][0], sp[h][0][1], sp[h][0][2]);
-                            split3(xcur[h][2], xcur[h][3], sp[h][1][0], sp[h][1][1], sp[h][1][2]);
-                            split3(xcur[h][4], xcur[h][5], sp[h][2][0], sp[h][2][1], sp[h][2][2]);
-                            split3(xcur[h][6], xcur[h][7], sp[h][3][0], sp[h][3][1], sp[h][3][2]);
+                            split3(xv[0], xv[1], sp[h][0][0], sp[h][0][1], sp[h][0][2]);
+                            split3(xv[2], xv[3], sp[h][1][0], sp[h][1][1], sp[h][1][2]);
+                            split3(xv[4], xv[5], sp[h][2][0], sp[h][2][1], sp[h][2][2]);
+                            split3(xv[6], xv[7], sp[h][3][0], sp[h][3][1], sp[h][3][2]);
                         }
                     }
                     // B fragments [k-step][n-tile][reg]: k-step 0 uses pairs 0,1; k-step 1 pairs 2,3.
@@ -434,26 +485,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int rr = 0; rr < 2; ++rr) {
                                 const int pr = ks * 2 + rr;
                                 uint32_t v;
-                                if (PF == 8) {
-                                    v = sp[0][pr][nt];                    // n-tile = split
-                                } else if (PF == 16) {
+                                if (WIDE) {
                                     v = sp[nt & 1][pr][nt >> 1];          // n-tile = 2 * split + half
+                                } else if (packed) {
+                                    v = col_s == 0 ? sp[0][pr][0] : (col_s == 1 ? sp[0][pr][1] : sp[0][pr][2]);
                                 } else {
-                                    const int sidx = col_s[nt];
-                                    v = sidx == 0 ? sp[0][pr][0] : (sidx == 1 ? sp[0][pr][1] : sp[0][pr][2]);
-                                    if (!col_ok[nt]) v = 0u;
+                                    v = sp[0][pr][nt];                    // n-tile = split
                                 }
                                 bf[ks][nt][rr] = v;
                             }
                         }
                     }
-                    const uint8_t *st = stages + (size_t)s * L::kStageBytes + bx * 16 * Fmt<WT>::BOX +
-                                        bi * Fmt<WT>::BB;
+                    const uint8_t *st = stages + (size_t)s * L::kStageBytes +
+                                        (wb / Fmt<WT>::BOXB) * L::kBoxBytes +
+                                        (wb % Fmt<WT>::BOXB) * Fmt<WT>::BB;
 #pragma unroll
                     for (int tt = 0; tt < T; ++tt) {
                         if (tt < ntiles) {
-                            const uint8_t *r0p = st + tt * L::kTileBytes + g * Fmt<WT>::BOX;
-                            const uint8_t *r1p = r0p + 8 * Fmt<WT>::BOX;
+                            const uint8_t *r0p = st + tt * L::kTileBytes + g * Fmt<WT>::ROWB;
+                            const uint8_t *r1p = r0p + 8 * Fmt<WT>::ROWB;
                             const float d0 = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(r0p));
                             const float d1 = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(r1p));
                             uint32_t a1[4], a2[4];  // A of k-step 0 and 1
@@ -469,52 +519,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 a1[0] = q0[0]; a1[2] = q0[1]; a1[1] = q1[0]; a1[3] = q1[1];
                                 a2[0] = q0[2]; a2[2] = q0[3]; a2[1] = q1[2]; a2[3] = q1[3];
                             }
-                            if (PF == 0) {
-#pragma unroll
-                                for (int nt = 0; nt < NT; ++nt) {
-                                    float part[4] = {0.f, 0.f, 0.f, 0.f};
-                                    mma_bf16(part, a1, bf[0][nt][0], bf[0][nt][1]);
-                                    mma_bf16(part, a2, bf[1][nt][0], bf[1][nt][1]);
-                                    scale_acc(acc[tt][nt], part, d0, d1);
-                                }
+                            if (packed) {
+                                float part[4];
+                                mma_bf16_z(part, a1, bf[0][0][0], bf[0][0][1]);
+                                mma_bf16(part, a2, bf[1][0][0], bf[1][0][1]);
+                                scale_acc(acc[tt][0], part, d0, d1);
                             } else {
+                                // The three splits of a token sit in the same thread and
+                                // column of three n-tiles: one accumulator chain sums them.
 #pragma unroll
                                 for (int h = 0; h < NH; ++h) {
-                                    float ps[3][4];
+                                    float part[4];
 #pragma unroll
                                     for (int sp_i = 0; sp_i < 3; ++sp_i) {
-                                        const int nt = PF == 16 ? 2 * sp_i + h : sp_i;
-                                        ps[sp_i][0] = ps[sp_i][1] = ps[sp_i][2] = ps[sp_i][3] = 0.f;
-                                        mma_bf16(ps[sp_i], a1, bf[0][nt][0], bf[0][nt][1]);
-                                        mma_bf16(ps[sp_i], a2, bf[1][nt][0], bf[1][nt][1]);
+                                        const int nt = WIDE ? 2 * sp_i + h : sp_i;
+                                        if (sp_i == 0)
+                                            mma_bf16_z(part, a1, bf[0][nt][0], bf[0][nt][1]);
+                                        else
+                                            mma_bf16(part, a1, bf[0][nt][0], bf[0][nt][1]);
+                                        mma_bf16(part, a2, bf[1][nt][0], bf[1][nt][1]);
                                     }
-                                    float sum[4];
-#pragma unroll
-                                    for (int r = 0; r < 4; ++r) sum[r] = (ps[0][r] + ps[1][r]) + ps[2][r];
-                                    scale_acc(acc[tt][h], sum, d0, d1);
+                                    scale_acc(acc[tt][h], part, d0, d1);
                                 }
                             }
                         }
                     }
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    // The last of the 16 warps to finish with stage s refills it with the
-                    // load S stages ahead (if any).
-                    // (The count only grows: every kCW-th arrival on a stage is the last one.)
-                    if ((atomicAdd(&released[s], 1u) + 1u) % kCW == 0u) {
-                        if (ahead.u < sc.u1) {
-                            fence_proxy_async_smem();
-                            issue(ahead, q + S);
-                            atomicAdd(issued, 1u);
-                        }
-                    }
-                    if (ahead.u < sc.u1) advance(ahead);
-                }
+                if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
                 for (int h = 0; h < NH; ++h)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) xcur[h][j] = xnext[h][j];
+                    for (int j = 0; j < 8; ++j) xcur[0][h][j] = xnext[0][h][j];
             }
             // Every consumer warp gets here, aborted or not; the flag read after the
             // barrier is the same in all of them, so they leave (or go on) together.
@@ -554,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int b = 0; b < kRedBufs; ++b) {
                         const float *rp = red + b * RT + r * C;
-                        v += PF ? rp[i] : (rp[i] + rp[P + i]) + rp[2 * P + i];
+                        v += packed ? (rp[i] + rp[P + i]) + rp[2 * P + i] : rp[i];
                     }
                     const int yrow = MOE ? s_sorted[seg0 + p0 + i] : p0 + i;
                     const size_t o = (size_t)yrow * m + row;
@@ -565,14 +601,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             consumers_sync();
         }
         u += ntiles;
-    }
-    // Leave only when no TMA write into this CTA's shared memory is in flight: in a
-    // normal run every load was consumed; after an abort the last S issued may not be.
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const long long n_issued = *issued;
-        for (long long d = (n_issued > S ? n_issued - S : 0); d < n_issued; ++d)
-            mbar_wait(&full[d % S], (uint32_t)((d / S) & 1), kDrainPolls);
     }
 }
 
@@ -590,35 +618,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int WT, int NT, int T, int PF>
+template <int WT, bool WIDE, int T>
 constexpr size_t smem_bytes() {
-    using L = Layout<WT, NT, T, PF>;
-    return (size_t)L::kStages * L::kStageBytes + L::kRedBytes + L::kStages * sizeof(uint64_t) +
-           (L::kStages + 2) * sizeof(unsigned) + 16 +
+    using L = Layout<WT, WIDE, T>;
+    return (size_t)L::kStages * L::kStageBytes + L::kRedBytes + 2 * L::kStages * sizeof(uint64_t) +
            kMaxSlots * sizeof(unsigned long long) + (3 * kMaxSlots + 4) * sizeof(int) + 16;
 }
 
-template <int WT, bool MOE, int NT, int T, int PF>
-cudaError_t launch_inst(const StreamArgs &a, const CUtensorMap &map, int grid,
-                        const DeviceInfo &dev, cudaStream_t stream) {
-    static std::atomic<unsigned long long> smem_set{0};
-    auto kern = gemv_mma_kernel<WT, MOE, NT, T, PF>;
-    constexpr size_t bytes = smem_bytes<WT, NT, T, PF>();
-    static_assert(bytes <= 227 * 1024, "shared memory budget");
-    cudaError_t err = ensure_smem(kern, (int)bytes, dev, smem_set);
-    if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, bytes, stream>>>(map, a);
-    return cudaGetLastError();
-}
-
-bool make_map(CUtensorMap &map, const StreamArgs &a, int wtype, long long rows) {
+bool make_map(CUtensorMap &map, const StreamArgs &a, int wtype, long long rows, int box_rows) {
     auto encode = encode_fn();
     if (!encode) return false;
     const size_t rb = row_bytes(wtype, a.k);
-    const int box = wtype == kQ4_0 ? Fmt<kQ4_0>::BOX : Fmt<kQ8_0>::BOX;
+    const int box = wtype == kQ4_0 ? Fmt<kQ4_0>::ROWB : Fmt<kQ8_0>::ROWB;
     const cuuint64_t dims[2] = {(cuuint64_t)(rb / 2), (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)rb};
-    const cuuint32_t boxd[2] = {(cuuint32_t)(box / 2), 16};
+    const cuuint32_t boxd[2] = {(cuuint32_t)(box / 2), (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t *>(a.W), dims,
                   strides, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -626,25 +640,31 @@ bool make_map(CUtensorMap &map, const StreamArgs &a, int wtype, long long rows) 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int WT, int NT, int PF>
-cudaError_t launch_t(const StreamArgs &a, const CUtensorMap &map, int grid, long long per,
-                     const DeviceInfo &dev, cudaStream_t stream) {
-    if (per <= 2) return launch_inst<WT, false, NT, 2, PF>(a, map, grid, dev, stream);
-    if (per <= 4) return launch_inst<WT, false, NT, 4, PF>(a, map, grid, dev, stream);
-    if (per <= 6) return launch_inst<WT, false, NT, 6, PF>(a, map, grid, dev, stream);
-    return launch_inst<WT, false, NT, 8, PF>(a, map, grid, dev, stream);
+template <int WT, bool MOE, bool WIDE, int T>
+cudaError_t launch_inst(const StreamArgs &a, long long rows, int grid, const DeviceInfo &dev,
+                        cudaStream_t stream) {
+    static std::atomic<unsigned long long> smem_set{0};
+    CUtensorMap map_t, map_1;
+    if (!make_map(map_t, a, WT, rows, T * 16) || !make_map(map_1, a, WT, rows, 16))
+        return cudaErrorInvalidValue;
+    auto kern = gemv_mma_kernel<WT, MOE, WIDE, T>;
+    constexpr size_t bytes = smem_bytes<WT, WIDE, T>();
+    static_assert(bytes <= 227 * 1024, "shared memory budget");
+    cudaError_t err = ensure_smem(kern, (int)bytes, dev, smem_set);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, kThreads, bytes, stream>>>(map_t, map_1, a);
+    return cudaGetLastError();
 }
 
 template <int WT>
-cudaError_t launch_gemv_wt(const StreamArgs &a, const CUtensorMap &map, const DeviceInfo &dev,
-                           cudaStream_t stream) {
+cudaError_t launch_gemv_wt(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
     const long long tiles = (a.m + 15) / 16;
     const int grid = (int)(tiles < dev.sm_count ? tiles : dev.sm_count);
     const long long per = (tiles + grid - 1) / grid;  // tiles per CTA (max)
-    if (a.n > 8) return launch_inst<WT, false, 6, 4, 16>(a, map, grid, dev, stream);
-    if (a.n > 4) return launch_t<WT, 3, 8>(a, map, grid, per, dev, stream);
-    if (a.n > 2) return launch_t<WT, 2, 0>(a, map, grid, per, dev, stream);
-    return launch_t<WT, 1, 0>(a, map, grid, per, dev, stream);
+    if (a.n > 8) return launch_inst<WT, false, true, 3>(a, a.m, grid, dev, stream);
+    if (per <= 2) return launch_inst<WT, false, false, 2>(a, a.m, grid, dev, stream);
+    if (per <= 4) return launch_inst<WT, false, false, 4>(a, a.m, grid, dev, stream);
+    return launch_inst<WT, false, false, 6>(a, a.m, grid, dev, stream);
 }
 
 }  // namespace
@@ -655,19 +675,16 @@ bool mma_gemv_supported(int wtype, int k) {
 
 cudaError_t launch_mma_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,
                             cudaStream_t stream) {
-    CUtensorMap map;
-    if (!make_map(map, a, wtype, a.m)) return cudaErrorInvalidValue;
-    return wtype == kQ4_0 ? launch_gemv_wt<kQ4_0>(a, map, dev, stream)
-                          : launch_gemv_wt<kQ8_0>(a, map, dev, stream);
+    return wtype == kQ4_0 ? launch_gemv_wt<kQ4_0>(a, dev, stream)
+                          : launch_gemv_wt<kQ8_0>(a, dev, stream);
 }
 
 cudaError_t launch_mma_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,
                            cudaStream_t stream) {
-    CUtensorMap map;
-    if (!make_map(map, a, wtype, (long long)a.n_experts * a.m)) return cudaErrorInvalidValue;
+    const long long rows = (long long)a.n_experts * a.m;
     const int grid = dev.sm_count;
-    return wtype == kQ4_0 ? launch_inst<kQ4_0, true, 2, 8, 0>(a, map, grid, dev, stream)
-                          : launch_inst<kQ8_0, true, 2, 4, 0>(a, map, grid, dev, stream);
+    return wtype == kQ4_0 ? launch_inst<kQ4_0, true, false, 6>(a, rows, grid, dev, stream)
+                          : launch_inst<kQ8_0, true, false, 4>(a, rows, grid, dev, stream);
 }
 
 }  // namespace wq

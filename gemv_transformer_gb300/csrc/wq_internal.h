@@ -72,6 +72,9 @@ cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev
                              cudaStream_t stream);
 cudaError_t launch_gemm_tc(const GemmArgs &a, const DeviceInfo &dev, cudaStream_t stream);
 size_t gemm_tc_workspace_bytes(int n, int k);
+bool gemm_tcp_supported(const GemmArgs &a);
+cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
+                            cudaStream_t stream);
 cudaError_t launch_gemm_tc_ws(const GemmArgs &a, void *workspace, const DeviceInfo &dev,
                               cudaStream_t stream);
 cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out,
