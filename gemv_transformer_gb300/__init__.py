@@ -21,12 +21,13 @@ LIB_PATH = os.path.join(HERE, "_build", "libwq.so")
 WQ_BF16, WQ_Q8_0, WQ_Q4_0 = 0, 1, 2
 WQ_BIAS, WQ_GELU, WQ_RESIDUAL, WQ_TC_BF16 = 1, 2, 4, 256
 WQ_OK, WQ_ERR_INVALID_ARG, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA = 0, 1, 2, 3
-WQ_ERR_DEVICE_TIMEOUT, WQ_ERR_BAD_EXPERT = 4, 5
+WQ_ERR_DEVICE_TIMEOUT, WQ_ERR_BAD_EXPERT, WQ_ERR_TOO_LARGE = 4, 5, 6
+WQ_GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20
 WQ_GEMV_MAX_N = 16
 WQ_MOE_MAX_SLOTS = 256
 
-EXPORTS = ("wq_gemm", "wq_gemm_ws", "wq_gemm_workspace_bytes", "wq_gemv", "wq_moe_gemv",
-           "wq_weight_bytes", "wq_dequantize", "wq_get_device_status", "wq_status_string",
+EXPORTS = ("wq_gemm", "wq_gemm_ws", "wq_gemm_workspace_bytes", "wq_gemm_noalloc", "wq_gemv",
+           "wq_moe_gemv", "wq_weight_bytes", "wq_dequantize", "wq_get_device_status", "wq_status_string",
            "wq_set_wait_limit")
 
 _lock = threading.Lock()
@@ -52,6 +53,8 @@ def _open(path: str):
     lib.wq_gemm.restype = ci
     lib.wq_gemv.argtypes = gemm_args
     lib.wq_gemv.restype = ci
+    lib.wq_gemm_noalloc.argtypes = gemm_args
+    lib.wq_gemm_noalloc.restype = ci
     lib.wq_gemm_ws.argtypes = gemm_args[:-1] + [vp, sz, vp]
     lib.wq_gemm_ws.restype = ci
     lib.wq_gemm_workspace_bytes.argtypes = [ci, ci, ci, ci, cu]
@@ -106,6 +109,12 @@ def wq_gemm_ws(n, m, k, wtype, flags, X, W, bias=None, residual=None, Y=None, wo
                workspace_bytes=0, stream=None) -> int:
     return load().wq_gemm_ws(n, m, k, wtype, flags, _p(X), _p(W), _p(bias), _p(residual), _p(Y),
                              _p(workspace), int(workspace_bytes), _s(stream))
+
+
+def wq_gemm_noalloc(n, m, k, wtype, flags, X, W, bias=None, residual=None, Y=None,
+                    stream=None) -> int:
+    return load().wq_gemm_noalloc(n, m, k, wtype, flags, _p(X), _p(W), _p(bias), _p(residual),
+                                  _p(Y), _s(stream))
 
 
 def wq_gemm_workspace_bytes(n, m, k, wtype, flags) -> int:

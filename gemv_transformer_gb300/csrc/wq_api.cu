@@ -49,6 +49,14 @@ wq_status check_common(int n, int m, int k, int wtype, unsigned flags, const flo
 }
 }  // namespace
 
+wq_status check_gemm_args(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                          const void *W, const float *bias, const float *residual,
+                          const float *Y) {
+    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
+    if (s == WQ_OK && (flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
+    return s;
+}
+
 const DeviceInfo *device_info() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -228,6 +236,7 @@ const char *wq_status_string(int status) {
     case WQ_ERR_CUDA: return "CUDA runtime error";
     case WQ_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case WQ_ERR_BAD_EXPERT: return "expert id out of range";
+    case WQ_ERR_TOO_LARGE: return "request exceeds the fixed scratch size";
     default: return "unknown status";
     }
 }

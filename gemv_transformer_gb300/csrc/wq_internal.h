@@ -7,6 +7,8 @@
 
 #include <atomic>
 
+#include "../../include/wq.h"
+
 namespace wq {
 
 // Arguments of the weight-streaming kernels (plain GEMV and routed MoE).
@@ -54,6 +56,11 @@ cudaError_t ensure_smem(Kernel kern, int bytes, const DeviceInfo &dev,
     if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
     return err;
 }
+
+// Host-side argument checks shared by the wq_gemm family (no device work).
+wq_status check_gemm_args(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                          const void *W, const float *bias, const float *residual,
+                          const float *Y);
 
 // Cached per-device facts (current device).  Returns nullptr on a CUDA error.
 const DeviceInfo *device_info();

@@ -25,7 +25,8 @@
  * Conventions shared by every call
  *   - Index names: n = rows of X (tokens), m = rows of W (outputs), k = inner.
  *   - All tensor pointers are DEVICE pointers owned by the caller.  libwq never
- *     allocates, frees or retains them, and allocates no device memory itself.
+ *     allocates, frees or retains them, and allocates no device memory itself
+ *     (the one fixed array of wq_gemm_noalloc is part of its device image).
  *   - Calls are asynchronous and ordered on `stream` (NULL = the legacy default
  *     stream).  They return once the work is launched.  A returned error means
  *     nothing was launched and no output was touched.
@@ -94,7 +95,8 @@ typedef enum {
     WQ_ERR_UNSUPPORTED = 2,    /* valid request this build has no kernel for */
     WQ_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
     WQ_ERR_DEVICE_TIMEOUT = 4, /* a kernel's bounded wait ran out (device status) */
-    WQ_ERR_BAD_EXPERT = 5      /* an expert id outside [0, n_experts) (device status) */
+    WQ_ERR_BAD_EXPERT = 5,     /* an expert id outside [0, n_experts) (device status) */
+    WQ_ERR_TOO_LARGE = 6       /* wq_gemm_noalloc: the call needs more than its fixed scratch */
 } wq_status;
 
 /* Largest n that wq_gemv accepts. */
@@ -136,6 +138,35 @@ WQ_API wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, cons
  * call takes the tensor-core path (WQ_TC_BF16, WQ_BF16 weights, n > WQ_GEMV_MAX_N),
  * else 0.  0 also for an invalid shape. */
 WQ_API size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned flags);
+
+/* Size of the fixed device scratch array behind wq_gemm_noalloc (one per device). */
+#define WQ_GEMM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * wq_gemm_ws without a caller workspace, for callers that may not allocate device
+ * memory and have no buffer to lend: code on a path where an allocation could
+ * block or fail (a serving loop with a frozen memory budget), a host application
+ * that owns the device allocator, a runtime with no allocator.  None of the pages
+ * this library follows has a counterpart; it is a library convenience.
+ * The bf16 copy of X lives in a statically reserved device array of
+ * WQ_GEMM_NOALLOC_SCRATCH_BYTES (16 MiB) per device, so the tensor-core route
+ * takes 2*n*k <= 16 MiB (n*k <= 8,388,608; e.g. 1500 x 4096).  The call allocates
+ * nothing, by any route.  Nothing in the array needs to start at zero: each call
+ * writes every byte it later reads.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's address; make that first call before any stream capture begins.
+ * Concurrency: all calls on one device share the one array.  Calls ordered on one
+ * stream are safe; calls that may overlap in time (different streams without an
+ * ordering between them, or different host threads) race on it and give wrong
+ * results: serialise them, or use wq_gemm_ws with a buffer per stream.
+ * Routes without scratch (wq_gemm_workspace_bytes(...) == 0) run as wq_gemm.
+ * Results are identical to wq_gemm_ws's.
+ * Errors: as wq_gemm_ws, plus WQ_ERR_TOO_LARGE when wq_gemm_workspace_bytes(n, m,
+ * k, wtype, flags) > WQ_GEMM_NOALLOC_SCRATCH_BYTES (nothing is launched).
+ */
+WQ_API wq_status wq_gemm_noalloc(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                                 const void *W, const float *bias, const float *residual, float *Y,
+                                 wq_stream_t stream);
 
 /*
  * Same contract as wq_gemm for small n (1 <= n <= WQ_GEMV_MAX_N): the

@@ -44,7 +44,7 @@ def test_weight_bytes():
 
 
 def test_status_strings():
-    for code in range(6):
+    for code in range(7):
         assert wq.wq_status_string(code) != "unknown status"
     assert wq.wq_status_string(99) == "unknown status"
 
@@ -92,6 +92,18 @@ def test_workspace_sizes_and_errors(lib):
     assert call(None, need) == wq.WQ_ERR_INVALID_ARG          # missing
     assert call(A + 16, need) == wq.WQ_ERR_INVALID_ARG        # not 256-byte aligned
     assert call(A, need - 1) == wq.WQ_ERR_INVALID_ARG         # too small
+
+
+def test_noalloc_rejects_requests_beyond_its_scratch(lib):
+    """2*n*k above the fixed 16 MiB array is refused on the host, before any device
+    work; one element less than the limit is not refused for its size."""
+    TC = wq.WQ_TC_BF16
+    assert wq.wq_gemm_noalloc(2049, 64, 4096, wq.WQ_BF16, TC, A, A, None, None, A, 0) == \
+        wq.WQ_ERR_TOO_LARGE
+    assert wq.wq_gemm_noalloc(2048, 64, 4096, wq.WQ_BF16, TC, None, A, None, None, A, 0) == \
+        wq.WQ_ERR_INVALID_ARG
+    assert wq.wq_gemm_noalloc(0, 64, 4096, wq.WQ_BF16, TC, A, A, None, None, A, 0) == \
+        wq.WQ_ERR_INVALID_ARG
 
 
 def test_unsupported_requests(lib):
