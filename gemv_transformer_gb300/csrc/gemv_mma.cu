@@ -7,14 +7,20 @@
 // Why tensor cores for an HBM-bound op: with f32 FMAs every weight costs a
 // decode, an X load and one FMA per token, which issues more instructions than
 // the SM can retire while HBM streams 4-8 weights per SM-cycle.  Here the
-// weights' integer codes (exact in bf16) are decoded in registers straight into
+// weights' integer codes (exact in f16) are decoded in registers straight into
 // the A fragments of mma.sync.m16n8k16 (no shared-memory round trip for the
-// decoded operand), and X is split exactly into three bf16 terms
-// x = x1 + x2 + x3 (8 + 8 + 8 significant bits: every product is exact and the
-// f32 accumulation is the only rounding).  The columns of the MMA are
-// (split, token) pairs, so one decoded weight tile serves every token and split.
-// The block scale d is applied once per 32-weight block per row (an f32x2 FMA
-// on the MMA's partial sums), as in the block definition w = d*q.
+// decoded operand): a mask-and-or places each 4- or 8-bit code in the mantissa of
+// an f16 magic number and one packed f16 subtract (or fma) removes the bias, two
+// weights per instruction.  X is brought into f16 range by a power of two per
+// (token, 32-block) -- chosen from the block's largest |x| -- and split exactly
+// into three f16 terms x = x1 + x2 + x3 (33 significant bits cover f32's 24), so
+// every product is exact and the f32 accumulation is the only rounding (values
+// below 2^-15 of their block's largest |x| lose bits past f16's subnormal range:
+// an absolute error of at most 2^-39 of that largest |x|).  The columns of the
+// MMA are (split, token) pairs, so one decoded weight tile serves every token and
+// split.  The block scale d times the power of two's inverse is applied once per
+// 32-weight block per row, on the MMA's partial sums, as in the block definition
+// w = d*q.
 //
 // Data movement: a stage holds one 512-weight chunk of every row of the CTA's
 // current row group, loaded by a producer warp as one tall TMA box (2-D tensor
@@ -37,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "wq_device.cuh"
 #include "wq_internal.h"
@@ -89,87 +96,115 @@ struct Layout {
 
 // ------------------------------------------------------------------ helpers --
 
-__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+__device__ __forceinline__ uint32_t pack_f16x2_rn(float lo, float hi) {
     uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
-// The three exact bf16 terms of a pair of f32 values, packed (lo, hi) per term.
-__device__ __forceinline__ void split3(float a, float b, uint32_t &p1, uint32_t &p2,
-                                       uint32_t &p3) {
-    p1 = pack_bf16x2_rn(a, b);
-    a -= __uint_as_float(p1 << 16);
-    b -= __uint_as_float(p1 & 0xFFFF0000u);
-    p2 = pack_bf16x2_rn(a, b);
-    a -= __uint_as_float(p2 << 16);
-    b -= __uint_as_float(p2 & 0xFFFF0000u);
-    p3 = pack_bf16x2_rn(a, b);
+__device__ __forceinline__ void unpack_f16x2(uint32_t p, float &lo, float &hi) {
+    unsigned short l, h;
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(l), "=h"(h) : "r"(p));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(l));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(h));
 }
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
+// The three f16 terms of a pair of f32 values with |v| < 2^15, packed (lo, hi) per
+// term: v = t1 + t2 + t3 exactly when v is a multiple of 2^-24 (33 bits of f16
+// significand cover f32's 24; each subtraction is exact).
+__device__ __forceinline__ void split3(float a, float b, uint32_t &p1, uint32_t &p2,
+                                       uint32_t &p3) {
+    float a1, b1;
+    p1 = pack_f16x2_rn(a, b);
+    unpack_f16x2(p1, a1, b1);
+    a -= a1;
+    b -= b1;
+    p2 = pack_f16x2_rn(a, b);
+    unpack_f16x2(p2, a1, b1);
+    a -= a1;
+    b -= b1;
+    p3 = pack_f16x2_rn(a, b);
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // D = A.B with a zero accumulator input.
-__device__ __forceinline__ void mma_bf16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                           uint32_t b1) {
+__device__ __forceinline__ void mma_f16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%10,%10,%10,%10};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
 }
 
-// acc[0..1] += d0 * p[0..1]; acc[2..3] += d1 * p[2..3] (packed f32x2 FMAs).
-__device__ __forceinline__ void scale_acc(float (&acc)[4], const float (&p)[4], float d0,
-                                          float d1) {
-    unsigned long long a01, a23, p01, p23, dd0, dd1;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(a01) : "f"(acc[0]), "f"(acc[1]));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(a23) : "f"(acc[2]), "f"(acc[3]));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(p01) : "f"(p[0]), "f"(p[1]));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(p23) : "f"(p[2]), "f"(p[3]));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(dd0) : "f"(d0));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(dd1) : "f"(d1));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a01) : "l"(dd0), "l"(p01));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a23) : "l"(dd1), "l"(p23));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[0]), "=f"(acc[1]) : "l"(a01));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[2]), "=f"(acc[3]) : "l"(a23));
-}
-
-__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
     return r;
 }
 
-// Q4_0: the four bytes v = qs[4t..4t+3] of one row give, for the two MMA k-steps of
-// the block, A registers (low nibbles: elements 4t..4t+3; high: 16+4t..16+4t+3).
-// Each bf16x2 holds elements (j, j+2) of its nibble group: 0x4300 | q is 128 + q
-// exactly, and subtracting 136 leaves q - 8.
-__device__ __forceinline__ void decode_q4(uint32_t v, uint32_t &lo02, uint32_t &lo13,
-                                          uint32_t &hi02, uint32_t &hi13) {
-    const uint32_t m = 0x000F000Fu, magic = 0x43004300u, off = 0x43084308u;  // 136, 136
-    lo02 = sub_bf16x2((v & m) | magic, off);
-    lo13 = sub_bf16x2(((v >> 8) & m) | magic, off);
-    hi02 = sub_bf16x2(((v >> 4) & m) | magic, off);
-    hi13 = sub_bf16x2(((v >> 12) & m) | magic, off);
+// acc[0..1] += (d0 * inv0, d0 * inv1) * p[0..1]; acc[2..3] += (d1 * inv0, d1 * inv1) * p[2..3].
+__device__ __forceinline__ void scale_acc(float (&acc)[4], const float (&p)[4], float d0,
+                                          float d1, float inv0, float inv1) {
+    acc[0] = fmaf(d0 * inv0, p[0], acc[0]);
+    acc[1] = fmaf(d0 * inv1, p[1], acc[1]);
+    acc[2] = fmaf(d1 * inv0, p[2], acc[2]);
+    acc[3] = fmaf(d1 * inv1, p[3], acc[3]);
 }
 
-// Q8_0: eight signed bytes -> four bf16x2 (pairs (0,1), (2,3), (4,5), (6,7)), exact.
-__device__ __forceinline__ void decode_q8(uint32_t v0, uint32_t v1, uint32_t (&r)[4]) {
-    float f[8];
-    s8x4_to_f32(v0, f[0], f[1], f[2], f[3]);
-    s8x4_to_f32(v1, f[4], f[5], f[6], f[7]);
-    r[0] = pack_bf16x2_rn(f[0], f[1]);
-    r[1] = pack_bf16x2_rn(f[2], f[3]);
-    r[2] = pack_bf16x2_rn(f[4], f[5]);
-    r[3] = pack_bf16x2_rn(f[6], f[7]);
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+// Q4_0: the four code bytes v = qs[4t..4t+3] of one row -> the A registers of the
+// block's two MMA k-steps, as exact f16 (q - 8).  Low nibbles (elements 4t..4t+3):
+// 0x6400 | q is 1024 + q, minus 1032.  High nibbles (elements 16+4t..16+4t+3) sit
+// four bits up: 0x6400 | 16q is 1024 + 16q, times 1/16 minus 72 (one exact fma).
+// Each register pairs elements (j, j+2): l02 = (4t, 4t+2), l13 = (4t+1, 4t+3),
+// h02 = (16+4t, 18+4t), h13 = (17+4t, 19+4t).
+__device__ __forceinline__ void decode_q4(uint32_t v, uint32_t &l02, uint32_t &l13,
+                                          uint32_t &h02, uint32_t &h13) {
+    const uint32_t v8 = v >> 8;
+    const uint32_t one16 = 0x2C002C00u, m72 = 0xD480D480u, c1032 = 0x64086408u;
+    l02 = hsub2((v & 0x000F000Fu) | 0x64006400u, c1032);
+    l13 = hsub2((v8 & 0x000F000Fu) | 0x64006400u, c1032);
+    h02 = hfma2((v & 0x00F000F0u) | 0x64006400u, one16, m72);
+    h13 = hfma2((v8 & 0x00F000F0u) | 0x64006400u, one16, m72);
+}
+
+// Q8_0: four signed code bytes v = qs[j..j+3] -> f16 pairs (j, j+2) and (j+1, j+3),
+// exact: the byte biased to unsigned becomes the low byte of 0x64xx = 1024 + u, and
+// 1024 + u - 1152 = u - 128 is the signed code.
+__device__ __forceinline__ void decode_q8(uint32_t v, uint32_t &p02, uint32_t &p13) {
+    const uint32_t u = v ^ 0x80808080u;
+    p02 = hsub2(__byte_perm(u, 0x64646464u, 0x4240), 0x64806480u);
+    p13 = hsub2(__byte_perm(u, 0x64646464u, 0x4341), 0x64806480u);
+}
+
+// The power of two s = 2^e that brings a block's largest |x| into [2^14, 2^15)
+// (so every scaled value is below f16's 65504), and 1/s; e is clamped to
+// [-113, 126] so both stay normal f32.
+__device__ __forceinline__ void block_scale(float mx, float &s, float &inv) {
+    const int E = (int)((__float_as_uint(mx) >> 23) & 0xFFu);
+    const int sb = min(253, max(1, 268 - E));
+    s = __uint_as_float((uint32_t)sb << 23);
+    inv = __uint_as_float((uint32_t)(254 - sb) << 23);
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -374,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------- consumers
-    long long q = 0;
+    int qs = 0;            // stage of the next chunk
+    uint32_t qph = 0u;     // its fill parity
     bool ok = true;
     for (long long u = sc.u0; u < sc.u1 && ok;) {
         const int ntiles = group_tiles<T>(sc, u);
@@ -385,220 +421,271 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row0 = (int)(u % sc.tpe) * 16;
         for (int p0 = 0; p0 < ntok_all && ok; p0 += P_MAX) {
             const int ntok = min(P_MAX, ntok_all - p0);
-            // packed: 1-2 tokens, column g = split (g / P) of token (g % P), one n-tile;
-            // else split-major: n-tile s, column g = token g (+8 for the second half).
-            const bool packed = !WIDE && ntok <= 2;
-            const int P = packed ? ntok : (WIDE ? 16 : 8);
-            int xrow[NH];
-            bool tok_ok[NH];
-            int col_s = 0;  // packed: which split this thread's column carries
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                const int i = packed ? g % P : h * 8 + g;
-                tok_ok[h] = packed ? (g < 3 * P) : (i < ntok);
-                const int r = p0 + (tok_ok[h] ? i : 0);
-                xrow[h] = MOE ? s_sorted[seg0 + r] / a.topk : r;
-            }
-            if (packed) col_s = g / P;
+            // One pass over the group's chunks; the column layout is a compile-time
+            // choice so the tile loop carries no layout branches.
+            auto pass = [&](auto pk) {
+                // packed: 1-2 tokens, column g = split (g / P) of token (g % P), one n-tile;
+                // else split-major: n-tile s, column g = token g (+8 for the second half).
+                constexpr bool packed = decltype(pk)::value;
+                const int P = packed ? ntok : (WIDE ? 16 : 8);
+                int xrow[NH];
+                bool tok_ok[NH];
+                int col_s = 0;  // packed: which split this thread's column carries
+    #pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    const int i = packed ? g % P : h * 8 + g;
+                    tok_ok[h] = packed ? (g < 3 * P) : (i < ntok);
+                    const int r = p0 + (tok_ok[h] ? i : 0);
+                    xrow[h] = MOE ? s_sorted[seg0 + r] / a.topk : r;
+                }
+                if (packed) col_s = g / P;
 
-            float acc[T][NA][4];
-#pragma unroll
-            for (int tt = 0; tt < T; ++tt)
-#pragma unroll
-                for (int j = 0; j < NA; ++j)
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) acc[tt][j][r] = 0.f;
+                float acc[T][NA][4];
+    #pragma unroll
+                for (int tt = 0; tt < T; ++tt)
+    #pragma unroll
+                    for (int j = 0; j < NA; ++j)
+    #pragma unroll
+                        for (int r = 0; r < 4; ++r) acc[tt][j][r] = 0.f;
 
-            // X of this warp's block of a chunk.
-            auto load_x = [&](int c, float (&xv)[1][NH][8]) {
-#pragma unroll
-                for (int hb = 0; hb < 1; ++hb) {
+                // X of this warp's block of a chunk, in the element order of the A decode:
+                // (4t..4t+3, 16+4t..19+4t) for Q4_0, (8t..8t+7) for Q8_0.
+                auto load_x = [&](int c, float (&xv)[NH][8]) {
                     const int blk = c * kBlocks + warp;
-#pragma unroll
+    #pragma unroll
                     for (int h = 0; h < NH; ++h) {
                         float4 u0v = make_float4(0.f, 0.f, 0.f, 0.f), u1v = u0v;
                         if (blk < nb && tok_ok[h]) {
                             const float *xp = a.X + (size_t)xrow[h] * k + (size_t)blk * 32;
-                            if (WT == kQ4_0) {
-                                u0v = __ldg(reinterpret_cast<const float4 *>(xp + 4 * t));
-                                u1v = __ldg(reinterpret_cast<const float4 *>(xp + 16 + 4 * t));
-                            } else {
-                                u0v = __ldg(reinterpret_cast<const float4 *>(xp + 8 * t));
-                                u1v = __ldg(reinterpret_cast<const float4 *>(xp + 8 * t + 4));
-                            }
+                            u0v = __ldg(reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 4 * t : 8 * t)));
+                            u1v = __ldg(reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 16 + 4 * t : 8 * t + 4)));
                         }
-                        xv[hb][h][0] = u0v.x; xv[hb][h][1] = u0v.y;
-                        xv[hb][h][2] = u0v.z; xv[hb][h][3] = u0v.w;
-                        xv[hb][h][4] = u1v.x; xv[hb][h][5] = u1v.y;
-                        xv[hb][h][6] = u1v.z; xv[hb][h][7] = u1v.w;
+                        xv[h][0] = u0v.x; xv[h][1] = u0v.y; xv[h][2] = u0v.z; xv[h][3] = u0v.w;
+                        xv[h][4] = u1v.x; xv[h][5] = u1v.y; xv[h][6] = u1v.z; xv[h][7] = u1v.w;
                     }
-                }
-            };
-            float xcur[1][NH][8];
-            load_x(0, xcur);
+                };
+                float xcur[NH][8];
+                load_x(0, xcur);
+                // The warp's block sits at the same offset in every stage; its code bytes
+                // start 4-byte aligned when the block's byte offset is 2 mod 4.
+                const int wb = warp;
+                const bool qs_aligned = ((Fmt<WT>::BB * (wb % Fmt<WT>::BOXB)) & 3) == 2;
+                const int blk_off = (wb / Fmt<WT>::BOXB) * L::kBoxBytes +
+                                    (wb % Fmt<WT>::BOXB) * Fmt<WT>::BB + g * Fmt<WT>::ROWB;
 
-            for (int c = 0; c < KC; ++c, ++q) {
-                float xnext[1][NH][8];
-                if (c + 1 < KC) load_x(c + 1, xnext);
-                const int s = (int)(q % S);
-                bool w = mbar_test_wait(&full[s], (uint32_t)((q / S) & 1));
-                for (uint64_t i = 1; !w && i < limit && !*abort_flag; ++i)
-                    w = mbar_try_wait(&full[s], (uint32_t)((q / S) & 1));
-                w = __all_sync(0xFFFFFFFFu, w);
-                if (!w) {
-                    if (lane == 0) {
-                        if (!*abort_flag) record_status(a.status, kStTimeout);
-                        *abort_flag = 1u;
+                for (int c = 0; c < KC; ++c) {
+                    float xnext[NH][8];
+                    if (c + 1 < KC) load_x(c + 1, xnext);
+                    const int s = qs;
+                    const uint32_t par = qph;
+                    if (++qs == S) {
+                        qs = 0;
+                        qph ^= 1u;
                     }
-                    ok = false;
-                    break;
-                }
-#pragma unroll
-                for (int hb = 0; hb < 1; ++hb) {
-                    const int wb = warp;             // block within the chunk (0..15)
-                    const int blk = c * kBlocks + wb;
-                    if (blk >= nb) continue;
-                    // Exact 3-term split of X, pairs in the element order of the A decode.
-                    uint32_t sp[NH][4][3];
-#pragma unroll
-                    for (int h = 0; h < NH; ++h) {
-                        const float *xv = xcur[hb][h];
-                        if (WT == kQ4_0) {  // pairs (0,2), (1,3) of each nibble group
-                            split3(xv[0], xv[2], sp[h][0][0], sp[h][0][1], sp[h][0][2]);
-                            split3(xv[1], xv[3], sp[h][1][0], sp[h][1][1], sp[h][1][2]);
-                            split3(xv[4], xv[6], sp[h][2][0], sp[h][2][1], sp[h][2][2]);
-                            split3(xv[5], xv[7], sp[h][3][0], sp[h][3][1], sp[h][3][2]);
-                        } else {            // pairs (0,1), (2,3), (4,5), (6,7)
-                            split3(xv[0], xv[1], sp[h][0][0], sp[h][0][1], sp[h][0][2]);
-                            split3(xv[2], xv[3], sp[h][1][0], sp[h][1][1], sp[h][1][2]);
-                            split3(xv[4], xv[5], sp[h][2][0], sp[h][2][1], sp[h][2][2]);
-                            split3(xv[6], xv[7], sp[h][3][0], sp[h][3][1], sp[h][3][2]);
+                    bool w = mbar_test_wait(&full[s], par);
+                    for (uint64_t i = 1; !w && i < limit && !*abort_flag; ++i)
+                        w = mbar_try_wait(&full[s], par);
+                    w = __all_sync(0xFFFFFFFFu, w);
+                    if (!w) {
+                        if (lane == 0) {
+                            if (!*abort_flag) record_status(a.status, kStTimeout);
+                            *abort_flag = 1u;
                         }
+                        ok = false;
+                        break;
                     }
-                    // B fragments [k-step][n-tile][reg]: k-step 0 uses pairs 0,1; k-step 1 pairs 2,3.
-                    uint32_t bf[2][NT][2];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-                            for (int rr = 0; rr < 2; ++rr) {
-                                const int pr = ks * 2 + rr;
-                                uint32_t v;
-                                if (WIDE) {
-                                    v = sp[nt & 1][pr][nt >> 1];          // n-tile = 2 * split + half
-                                } else if (packed) {
-                                    v = col_s == 0 ? sp[0][pr][0] : (col_s == 1 ? sp[0][pr][1] : sp[0][pr][2]);
-                                } else {
-                                    v = sp[0][pr][nt];                    // n-tile = split
-                                }
-                                bf[ks][nt][rr] = v;
-                            }
+                    if (c * kBlocks + wb < nb) {
+                        // B: each token's block scaled by a power of two (block_scale), then
+                        // split exactly into three f16 terms; pairs in the A decode's order.
+                        uint32_t sp[NH][4][3];
+                        float inv_own[NH];
+    #pragma unroll
+                        for (int h = 0; h < NH; ++h) {
+                            float mx = 0.f;
+    #pragma unroll
+                            for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(xcur[h][j]));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+                            float sc;
+                            block_scale(mx, sc, inv_own[h]);
+                            float xs[8];
+    #pragma unroll
+                            for (int j = 0; j < 8; ++j) xs[j] = xcur[h][j] * sc;
+                            split3(xs[0], xs[2], sp[h][0][0], sp[h][0][1], sp[h][0][2]);
+                            split3(xs[1], xs[3], sp[h][1][0], sp[h][1][1], sp[h][1][2]);
+                            split3(xs[4], xs[6], sp[h][2][0], sp[h][2][1], sp[h][2][2]);
+                            split3(xs[5], xs[7], sp[h][3][0], sp[h][3][1], sp[h][3][2]);
                         }
-                    }
-                    const uint8_t *st = stages + (size_t)s * L::kStageBytes +
-                                        (wb / Fmt<WT>::BOXB) * L::kBoxBytes +
-                                        (wb % Fmt<WT>::BOXB) * Fmt<WT>::BB;
-#pragma unroll
-                    for (int tt = 0; tt < T; ++tt) {
-                        if (tt < ntiles) {
-                            const uint8_t *r0p = st + tt * L::kTileBytes + g * Fmt<WT>::ROWB;
-                            const uint8_t *r1p = r0p + 8 * Fmt<WT>::ROWB;
-                            const float d0 = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(r0p));
-                            const float d1 = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(r1p));
-                            uint32_t a1[4], a2[4];  // A of k-step 0 and 1
-                            if (WT == kQ4_0) {
-                                const uint32_t v0 = ld_u32_a2(r0p + 2 + 4 * t);
-                                const uint32_t v1 = ld_u32_a2(r1p + 2 + 4 * t);
-                                decode_q4(v0, a1[0], a1[2], a2[0], a2[2]);
-                                decode_q4(v1, a1[1], a1[3], a2[1], a2[3]);
-                            } else {
-                                uint32_t q0[4], q1[4];
-                                decode_q8(ld_u32_a2(r0p + 2 + 8 * t), ld_u32_a2(r0p + 6 + 8 * t), q0);
-                                decode_q8(ld_u32_a2(r1p + 2 + 8 * t), ld_u32_a2(r1p + 6 + 8 * t), q1);
-                                a1[0] = q0[0]; a1[2] = q0[1]; a1[1] = q1[0]; a1[3] = q1[1];
-                                a2[0] = q0[2]; a2[2] = q0[3]; a2[1] = q1[2]; a2[3] = q1[3];
-                            }
-                            if (packed) {
-                                float part[4];
-                                mma_bf16_z(part, a1, bf[0][0][0], bf[0][0][1]);
-                                mma_bf16(part, a2, bf[1][0][0], bf[1][0][1]);
-                                scale_acc(acc[tt][0], part, d0, d1);
-                            } else {
-                                // The three splits of a token sit in the same thread and
-                                // column of three n-tiles: one accumulator chain sums them.
-#pragma unroll
-                                for (int h = 0; h < NH; ++h) {
-                                    float part[4];
-#pragma unroll
-                                    for (int sp_i = 0; sp_i < 3; ++sp_i) {
-                                        const int nt = WIDE ? 2 * sp_i + h : sp_i;
-                                        if (sp_i == 0)
-                                            mma_bf16_z(part, a1, bf[0][nt][0], bf[0][nt][1]);
-                                        else
-                                            mma_bf16(part, a1, bf[0][nt][0], bf[0][nt][1]);
-                                        mma_bf16(part, a2, bf[1][nt][0], bf[1][nt][1]);
+                        // 1/scale of the accumulator columns 2t and 2t+1: that of the threads
+                        // whose B column they are (g = 2t, 2t+1).
+                        float inv0[NH], inv1[NH];
+    #pragma unroll
+                        for (int h = 0; h < NH; ++h) {
+                            inv0[h] = __shfl_sync(0xFFFFFFFFu, inv_own[h], 8 * t);
+                            inv1[h] = __shfl_sync(0xFFFFFFFFu, inv_own[h], 8 * t + 4);
+                        }
+                        // B fragments [k-step][n-tile][reg]: k-step 0 uses pairs 0,1; k-step 1 pairs 2,3.
+                        uint32_t bf[2][NT][2];
+    #pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+    #pragma unroll
+                            for (int ks = 0; ks < 2; ++ks) {
+    #pragma unroll
+                                for (int rr = 0; rr < 2; ++rr) {
+                                    const int pr = ks * 2 + rr;
+                                    uint32_t v;
+                                    if (WIDE) {
+                                        v = sp[nt & 1][pr][nt >> 1];  // n-tile = 2 * split + half
+                                    } else if (packed) {
+                                        v = col_s == 0 ? sp[0][pr][0]
+                                                       : (col_s == 1 ? sp[0][pr][1] : sp[0][pr][2]);
+                                    } else {
+                                        v = sp[0][pr][nt];            // n-tile = split
                                     }
-                                    scale_acc(acc[tt][h], part, d0, d1);
+                                    bf[ks][nt][rr] = v;
+                                }
+                            }
+                        }
+                        const uint8_t *st = stages + (size_t)s * L::kStageBytes + blk_off;
+                        // Every tile of the stage is computed; rows of tiles past the group's
+                        // end hold stale bytes and are never reduced or stored.
+                        auto tiles = [&](auto aligned) {
+                            constexpr bool AL = decltype(aligned)::value;
+    #pragma unroll
+                            for (int tt = 0; tt < T; ++tt) {
+                                const uint8_t *r0p = st + tt * L::kTileBytes;
+                                const uint8_t *r1p = r0p + 8 * Fmt<WT>::ROWB;
+                                const float d0 = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(r0p));
+                                const float d1 = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(r1p));
+                                uint32_t a1[4], a2[4];  // A of k-step 0 and 1
+                                if (WT == kQ4_0) {
+                                    uint32_t v0, v1;
+                                    if (AL) {
+                                        v0 = *reinterpret_cast<const uint32_t *>(r0p + 2 + 4 * t);
+                                        v1 = *reinterpret_cast<const uint32_t *>(r1p + 2 + 4 * t);
+                                    } else {
+                                        const uint32_t *w0 = reinterpret_cast<const uint32_t *>(r0p + 4 * t);
+                                        const uint32_t *w1 = reinterpret_cast<const uint32_t *>(r1p + 4 * t);
+                                        v0 = __funnelshift_r(w0[0], w0[1], 16);
+                                        v1 = __funnelshift_r(w1[0], w1[1], 16);
+                                    }
+                                    decode_q4(v0, a1[0], a1[2], a2[0], a2[2]);
+                                    decode_q4(v1, a1[1], a1[3], a2[1], a2[3]);
+                                } else {
+                                    uint32_t v00, v01, v10, v11;  // bytes 8t.., 8t+4.. of rows g, g+8
+                                    if (AL) {
+                                        const uint32_t *w0 = reinterpret_cast<const uint32_t *>(r0p + 2 + 8 * t);
+                                        const uint32_t *w1 = reinterpret_cast<const uint32_t *>(r1p + 2 + 8 * t);
+                                        v00 = w0[0]; v01 = w0[1];
+                                        v10 = w1[0]; v11 = w1[1];
+                                    } else {
+                                        const uint32_t *w0 = reinterpret_cast<const uint32_t *>(r0p + 8 * t);
+                                        const uint32_t *w1 = reinterpret_cast<const uint32_t *>(r1p + 8 * t);
+                                        const uint32_t x0 = w0[0], x1 = w0[1], x2 = w0[2];
+                                        const uint32_t y0 = w1[0], y1 = w1[1], y2 = w1[2];
+                                        v00 = __funnelshift_r(x0, x1, 16);
+                                        v01 = __funnelshift_r(x1, x2, 16);
+                                        v10 = __funnelshift_r(y0, y1, 16);
+                                        v11 = __funnelshift_r(y1, y2, 16);
+                                    }
+                                    decode_q8(v00, a1[0], a1[2]);
+                                    decode_q8(v01, a2[0], a2[2]);
+                                    decode_q8(v10, a1[1], a1[3]);
+                                    decode_q8(v11, a2[1], a2[3]);
+                                }
+                                if (packed) {
+                                    float part[4];
+                                    mma_f16_z(part, a1, bf[0][0][0], bf[0][0][1]);
+                                    mma_f16(part, a2, bf[1][0][0], bf[1][0][1]);
+                                    scale_acc(acc[tt][0], part, d0, d1, inv0[0], inv1[0]);
+                                } else {
+                                    // The three splits of a token sit in the same thread and
+                                    // column of three n-tiles: one accumulator chain sums them.
+    #pragma unroll
+                                    for (int h = 0; h < NH; ++h) {
+                                        float part[4];
+    #pragma unroll
+                                        for (int sp_i = 0; sp_i < 3; ++sp_i) {
+                                            const int nt = WIDE ? 2 * sp_i + h : sp_i;
+                                            if (sp_i == 0)
+                                                mma_f16_z(part, a1, bf[0][nt][0], bf[0][nt][1]);
+                                            else
+                                                mma_f16(part, a1, bf[0][nt][0], bf[0][nt][1]);
+                                            mma_f16(part, a2, bf[1][nt][0], bf[1][nt][1]);
+                                        }
+                                        scale_acc(acc[tt][h], part, d0, d1, inv0[h], inv1[h]);
+                                    }
+                                }
+                            }
+                        };
+                        if (qs_aligned)
+                            tiles(std::integral_constant<bool, true>{});
+                        else
+                            tiles(std::integral_constant<bool, false>{});
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+    #pragma unroll
+                    for (int h = 0; h < NH; ++h)
+    #pragma unroll
+                        for (int j = 0; j < 8; ++j) xcur[h][j] = xnext[h][j];
+                }
+                // Every consumer warp gets here, aborted or not; the flag read after the
+                // barrier is the same in all of them, so they leave (or go on) together.
+                consumers_sync();
+                ok = *abort_flag == 0u;
+                if (!ok) return;
+
+                // Ordered reduction: warp w adds into buffer w % 4, in 4 rounds.
+                const int RT = T * 16 * C;
+                for (int rnd = 0; rnd < kCW / kRedBufs; ++rnd) {
+                    if (warp / kRedBufs == rnd) {
+                        float *buf = red + (warp % kRedBufs) * RT;
+    #pragma unroll
+                        for (int tt = 0; tt < T; ++tt) {
+                            if (tt < ntiles) {
+    #pragma unroll
+                                for (int j = 0; j < NA; ++j) {
+    #pragma unroll
+                                    for (int r = 0; r < 4; ++r) {
+                                        const int row = tt * 16 + g + (r >= 2 ? 8 : 0);
+                                        const int col = j * 8 + 2 * t + (r & 1);
+                                        float *dst = &buf[row * C + col];
+                                        *dst = (rnd == 0) ? acc[tt][j][r] : *dst + acc[tt][j][r];
+                                    }
                                 }
                             }
                         }
                     }
+                    consumers_sync();
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-                for (int h = 0; h < NH; ++h)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) xcur[0][h][j] = xnext[0][h][j];
-            }
-            // Every consumer warp gets here, aborted or not; the flag read after the
-            // barrier is the same in all of them, so they leave (or go on) together.
-            consumers_sync();
-            ok = *abort_flag == 0u;
-            if (!ok) break;
-
-            // Ordered reduction: warp w adds into buffer w % 4, in 4 rounds.
-            const int RT = T * 16 * C;
-            for (int rnd = 0; rnd < kCW / kRedBufs; ++rnd) {
-                if (warp / kRedBufs == rnd) {
-                    float *buf = red + (warp % kRedBufs) * RT;
-#pragma unroll
-                    for (int tt = 0; tt < T; ++tt) {
-                        if (tt < ntiles) {
-#pragma unroll
-                            for (int j = 0; j < NA; ++j) {
-#pragma unroll
-                                for (int r = 0; r < 4; ++r) {
-                                    const int row = tt * 16 + g + (r >= 2 ? 8 : 0);
-                                    const int col = j * 8 + 2 * t + (r & 1);
-                                    float *dst = &buf[row * C + col];
-                                    *dst = (rnd == 0) ? acc[tt][j][r] : *dst + acc[tt][j][r];
-                                }
-                            }
+                const int R = ntiles * 16;
+                for (int idx = threadIdx.x; idx < R * ntok; idx += kCW * 32) {
+                    const int i = idx / R, r = idx % R;
+                    const int row = row0 + r;
+                    if (row < m) {
+                        float v = 0.f;
+    #pragma unroll
+                        for (int b = 0; b < kRedBufs; ++b) {
+                            const float *rp = red + b * RT + r * C;
+                            v += packed ? (rp[i] + rp[P + i]) + rp[2 * P + i] : rp[i];
                         }
+                        const int yrow = MOE ? s_sorted[seg0 + p0 + i] : p0 + i;
+                        const size_t o = (size_t)yrow * m + row;
+                        const float *bj = a.bias + (MOE ? (size_t)e * m + row : (size_t)row);
+                        a.Y[o] = epilogue(v, a.flags, bj, a.R + o);
                     }
                 }
                 consumers_sync();
+            };
+            if constexpr (!WIDE) {
+                if (ntok <= 2)
+                    pass(std::true_type{});
+                else
+                    pass(std::false_type{});
+            } else {
+                pass(std::false_type{});
             }
-            const int R = ntiles * 16;
-            for (int idx = threadIdx.x; idx < R * ntok; idx += kCW * 32) {
-                const int i = idx / R, r = idx % R;
-                const int row = row0 + r;
-                if (row < m) {
-                    float v = 0.f;
-#pragma unroll
-                    for (int b = 0; b < kRedBufs; ++b) {
-                        const float *rp = red + b * RT + r * C;
-                        v += packed ? (rp[i] + rp[P + i]) + rp[2 * P + i] : rp[i];
-                    }
-                    const int yrow = MOE ? s_sorted[seg0 + p0 + i] : p0 + i;
-                    const size_t o = (size_t)yrow * m + row;
-                    const float *bj = a.bias + (MOE ? (size_t)e * m + row : (size_t)row);
-                    a.Y[o] = epilogue(v, a.flags, bj, a.R + o);
-                }
-            }
-            consumers_sync();
         }
         u += ntiles;
     }

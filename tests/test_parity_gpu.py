@@ -76,7 +76,7 @@ def test_gemv_quantized(oracle_mod, wtype, shape):
     check_against_oracle(oracle_mod, wq.wq_gemv, wtype, n, m, k, 0, seed=n * 31 + m)
 
 
-# k % 256 == 0 takes the tensor-core GEMV (exact 3-term bf16 split of X).
+# k % 256 == 0 takes the tensor-core GEMV (X scaled per 32-block, exact 3-term f16 split).
 MMA_SHAPES = [(1, 1, 256), (1, 17, 512), (2, 300, 256), (3, 64, 768), (4, 1000, 1024),
               (5, 33, 256), (6, 100, 512), (8, 129, 2048), (9, 50, 512), (12, 16, 256),
               (16, 257, 1024), (7, 4100, 256)]
@@ -87,6 +87,24 @@ MMA_SHAPES = [(1, 1, 256), (1, 17, 512), (2, 300, 256), (3, 64, 768), (4, 1000, 
 def test_gemv_tensor_core_path(oracle_mod, wtype, shape):
     n, m, k = shape
     check_against_oracle(oracle_mod, wq.wq_gemv, wtype, n, m, k, BIAS | RES, seed=7 * n + m)
+
+
+@pytest.mark.parametrize("wtype", [Q8_0, Q4_0])
+@pytest.mark.parametrize("n", [1, 2, 5, 12])
+def test_gemv_tensor_core_wide_range_x(oracle_mod, wtype, n):
+    """X spanning 2^-60 .. 2^60 (far outside f16), a zero block, a block of values
+    near 2^100 and an f32 subnormal: the per-block power-of-two scaling must keep every
+    product exact to the tolerance."""
+    m, k = 300, 1024
+    g = synth.rng(90 + n)
+    X = synth.normal_f32(g, (n, k)) * np.exp2(g.integers(-60, 61, size=(n, k))).astype(np.float32)
+    X[:, 64:96] = 0.0                                   # a zero block
+    X[:, 128:160] = synth.normal_f32(g, (n, 32)) * np.float32(2.0 ** 100)  # huge block
+    X[:, 200] = np.float32(1e-40)                       # an f32 subnormal
+    img = synth.draw_weights(g, wtype, m, k)
+    Y = run_gemm(wq.wq_gemv, n, m, k, wtype, 0, X, img)
+    Yref, S = oracle_mod.gemm(n, m, k, wtype, 0, X, img)
+    assert_within(Y, Yref, S, TAU, what=f"wide-range X wtype={wtype} n={n}")
 
 
 @pytest.mark.parametrize("shape", [(1, 1, 8), (1, 37, 16), (2, 130, 1032), (3, 300, 2056),
