@@ -9,6 +9,14 @@
 // block per row per k step for Q8_0/Q4_0).  Each k step's 32 products are summed
 // into a fresh partial that is then added to the running total, which bounds the
 // serial f32 chain per output to k/32 + 32 terms.
+//
+// Grids smaller than one wave (small n and m, e.g. n = 32, m = 512) instead run
+// gemm_splitk_kernel: 32 x 32 output tiles, the k steps of a tile split across the
+// KS CTAs of a thread-block cluster (KS <= 8), each CTA summing its steps the same
+// way; the CTA of cluster rank 0 then adds the KS partials in rank order through
+// distributed shared memory (deterministic) and applies the epilogue.
+#include <cooperative_groups.h>
+
 #include "wq_device.cuh"
 #include "wq_internal.h"
 
@@ -117,6 +125,129 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const GemmArgs a) {
     }
 }
 
+// ------------------------------------------------------------ split-k --
+
+constexpr int SK = 32;  // tile rows (X) = tile rows (W) = k step
+
+// Four consecutive weights 4q..4q+3 of the 32-step at kk of row j, decoded to f32.
+template <int WT>
+__device__ __forceinline__ void load_w4(const GemmArgs &a, int j, int kk, int q, float (&w)[4]) {
+    w[0] = w[1] = w[2] = w[3] = 0.f;
+    if (j >= a.m || kk + 4 * q >= a.k) return;
+    const uint8_t *row = a.W + (size_t)j * row_bytes(WT, a.k);
+    if (WT == kBF16) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(row + (size_t)2 * (kk + 4 * q));
+        w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x);
+        w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+    } else if (WT == kQ8_0) {
+        const uint8_t *bp = row + (size_t)34 * (kk / 32);
+        const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = d * (float)(int8_t)bp[2 + 4 * q + e];
+    } else {
+        const uint8_t *bp = row + (size_t)18 * (kk / 32);
+        const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int t = 4 * q + e;  // element of the block
+            const uint32_t byte = bp[2 + (t & 15)];
+            const int code = (t < 16) ? (int)(byte & 15u) : (int)(byte >> 4);
+            w[e] = d * (float)(code - 8);
+        }
+    }
+}
+
+template <int WT>
+__global__ void __launch_bounds__(256) gemm_splitk_kernel(const GemmArgs a, int steps_per_rank) {
+    namespace cg = cooperative_groups;
+    __shared__ float xs[SK][SK + 4];   // [k][i]
+    __shared__ float ws[SK][SK + 4];   // [k][j]
+    __shared__ float red[SK * SK];     // this CTA's partial tile, [i][j]
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int i0 = blockIdx.y * SK, j0 = blockIdx.x * SK;
+    const int rank = (int)cluster.block_rank();
+    const int KS = (int)cluster.num_blocks();
+    const int nsteps = (a.k + SK - 1) / SK;
+    const int s0 = rank * steps_per_rank, s1 = min(nsteps, s0 + steps_per_rank);
+
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    for (int st = s0; st < s1; ++st) {
+        const int kk = st * SK;
+        {   // X tile: row r, elements 4q..4q+3 (k % 4 == 0: a float4 is all in or all out)
+            const int r = tid >> 3, q = tid & 7, i = i0 + r, t = kk + 4 * q;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < a.n && t < a.k) v = __ldg(reinterpret_cast<const float4 *>(a.X + (size_t)i * a.k + t));
+            xs[4 * q + 0][r] = v.x; xs[4 * q + 1][r] = v.y;
+            xs[4 * q + 2][r] = v.z; xs[4 * q + 3][r] = v.w;
+        }
+        {
+            const int r = tid >> 3, q = tid & 7;
+            float w[4];
+            load_w4<WT>(a, j0 + r, kk, q, w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ws[4 * q + e][r] = w[e];
+        }
+        __syncthreads();
+        float part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll 8
+        for (int t = 0; t < SK; ++t) {
+            const float2 xv = *reinterpret_cast<const float2 *>(&xs[t][2 * ty]);
+            const float2 wv = *reinterpret_cast<const float2 *>(&ws[t][2 * tx]);
+            part[0][0] = fmaf(xv.x, wv.x, part[0][0]);
+            part[0][1] = fmaf(xv.x, wv.y, part[0][1]);
+            part[1][0] = fmaf(xv.y, wv.x, part[1][0]);
+            part[1][1] = fmaf(xv.y, wv.y, part[1][1]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int v = 0; v < 2; ++v) acc[u][v] += part[u][v];
+        __syncthreads();
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int v = 0; v < 2; ++v) red[(2 * ty + u) * SK + 2 * tx + v] = acc[u][v];
+    cluster.sync();
+    if (rank == 0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = i0 + 2 * ty + u;
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                const int j = j0 + 2 * tx + v;
+                const int idx = (2 * ty + u) * SK + 2 * tx + v;
+                float sum = red[idx];
+                for (int r = 1; r < KS; ++r) sum += cluster.map_shared_rank(red, r)[idx];
+                if (i < a.n && j < a.m) {
+                    const size_t o = (size_t)i * a.m + j;
+                    a.Y[o] = epilogue(sum, a.flags, a.bias + j, a.R + o);
+                }
+            }
+        }
+    }
+    cluster.sync();  // the other ranks keep their shared memory until rank 0 has read it
+}
+
+template <int WT>
+cudaError_t launch_splitk_wt(const GemmArgs &a, int tiles_m, int tiles_n, int ks, int spr,
+                             cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)tiles_m, (unsigned)tiles_n, (unsigned)ks);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)ks;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_splitk_kernel<WT>, a, spr);
+}
+
 template <int WT>
 __global__ void dequant_kernel(int m, int k, const uint8_t *W, float *out) {
     // One thread per 8 weights.
@@ -157,8 +288,25 @@ __global__ void dequant_kernel(int m, int k, const uint8_t *W, float *out) {
 
 cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev,
                              cudaStream_t stream) {
-    (void)dev;
     dim3 grid((a.m + TJ - 1) / TJ, (a.n + TI - 1) / TI);
+    if ((long long)grid.x * grid.y < dev.sm_count) {
+        // Under one wave: split k across a cluster so that about one wave of CTAs runs.
+        const long long tm = (a.m + SK - 1) / SK, tn = (a.n + SK - 1) / SK;
+        const int nsteps = (a.k + SK - 1) / SK;
+        long long ks = dev.sm_count / (tm * tn);
+        if (ks > 8) ks = 8;
+        if (ks > nsteps) ks = nsteps;
+        if (ks < 1) ks = 1;
+        const int spr = (nsteps + (int)ks - 1) / (int)ks;
+        ks = (nsteps + spr - 1) / spr;  // no rank without steps
+        if (tn <= 65535) {
+            switch (wtype) {
+            case kBF16: return launch_splitk_wt<kBF16>(a, (int)tm, (int)tn, (int)ks, spr, stream);
+            case kQ8_0: return launch_splitk_wt<kQ8_0>(a, (int)tm, (int)tn, (int)ks, spr, stream);
+            default: return launch_splitk_wt<kQ4_0>(a, (int)tm, (int)tn, (int)ks, spr, stream);
+            }
+        }
+    }
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     switch (wtype) {
     case kBF16: gemm_simt_kernel<kBF16><<<grid, 256, 0, stream>>>(a); break;

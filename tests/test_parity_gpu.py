@@ -134,7 +134,10 @@ def test_gemm_small_n_routes_to_gemv(oracle_mod, wtype):
 # ------------------------------------------------------------ SIMT GEMM --
 
 @pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
-@pytest.mark.parametrize("shape", [(17, 64, 32), (32, 65, 96), (100, 200, 256), (129, 31, 544)])
+# Grids under one wave take the cluster split-k kernel; (700, 900, 96) fills a
+# wave of 64 x 64 tiles and takes the plain tiled kernel.
+@pytest.mark.parametrize("shape", [(17, 64, 32), (32, 65, 96), (100, 200, 256), (129, 31, 544),
+                                   (17, 40, 8192), (33, 512, 256), (700, 900, 96)])
 def test_gemm_simt(oracle_mod, wtype, shape):
     n, m, k = shape
     check_against_oracle(oracle_mod, wq.wq_gemm, wtype, n, m, k, BIAS | GELU, seed=n + m)
