@@ -12,15 +12,15 @@
 // decoded operand): a mask-and-or places each 4- or 8-bit code in the mantissa of
 // an f16 magic number and one packed f16 subtract (or fma) removes the bias, two
 // weights per instruction.  X is brought into f16 range by a power of two per
-// (token, 32-block) -- chosen from the block's largest |x| -- and split exactly
-// into three f16 terms x = x1 + x2 + x3 (33 significant bits cover f32's 24), so
-// every product is exact and the f32 accumulation is the only rounding (values
-// below 2^-15 of their block's largest |x| lose bits past f16's subnormal range:
-// an absolute error of at most 2^-39 of that largest |x|).  The columns of the
-// MMA are (split, token) pairs, so one decoded weight tile serves every token and
-// split.  The block scale d times the power of two's inverse is applied once per
-// 32-weight block per row, on the MMA's partial sums, as in the block definition
-// w = d*q.
+// (token, 32-block) -- chosen from the block's largest |x| -- and split into two
+// f16 terms x ~ x1 + x2 with |x - x1 - x2| <= 2^-22 |x| (elements below 2^-17 of
+// their block's largest |x| keep an absolute error of at most 2^-39 of it, f16's
+// subnormal floor).  Every product of a code and a term is exact in the f32
+// accumulation, so the result is within 2^-22 sum|x||w| plus f32 rounding of the
+// sums -- far inside the 1e-5 sum|x||w| contract.  The columns of the MMA are
+// (term, token) pairs, so one decoded weight tile serves every token and term.
+// The block scale d times the power of two's inverse is applied once per 32-weight
+// block per row, on the MMA's partial sums, as in the block definition w = d*q.
 //
 // Data movement: a stage holds one 512-weight chunk of every row of the CTA's
 // current row group, loaded by a producer warp as one tall TMA box (2-D tensor
@@ -31,11 +31,11 @@
 // stage, prefetches its X one stage ahead, builds its B fragments once and
 // applies them to all row tiles of the group.
 //
-// Column layouts of the MMA (n = tokens of a pass): for 1-2 tokens the three
-// splits of each token are packed into one n-tile (column s*P + i); for 3-8
-// tokens n-tile s holds split s of token i in column i, so a thread's three
-// n-tile results are the same token's three splits and one accumulator chain
-// sums them; 9-16 tokens use six n-tiles the same way (two token halves).
+// Column layouts of the MMA (n = tokens of a pass): for 1-4 tokens the two terms
+// of each token are packed into one n-tile (column s*P + i); for 5-8 tokens
+// n-tile s holds term s of token i in column i, so a thread's two n-tile results
+// are the same token's two terms and one accumulator chain sums them; 9-16
+// tokens use four n-tiles the same way (two token halves).
 // The partial sums of the 16 warps are reduced in shared memory in a fixed
 // order (deterministic) and the epilogue (bias, erf-GELU, residual) is fused
 // into the store.
@@ -77,19 +77,35 @@ struct Fmt<kQ8_0> {
     static constexpr int ROWB = 272;
 };
 
-// Accumulator columns per row of the reduction buffer: 8 (one n-tile), 16 when wide.
-template <bool WIDE>
-struct Cols {
-    static constexpr int C = WIDE ? 16 : 8;
+// Column layouts of a pass (see the file comment):
+//   kPacked  1-4 tokens, the two terms of each token in one n-tile;
+//   kSplit8  up to 8 tokens, n-tile s = term s, column = token;
+//   kSplit16 up to 16 tokens, four n-tiles (two token halves);
+//   kMixed   up to 8 tokens, packed when a pass has at most 4 (MoE: token counts
+//            per expert vary from pass to pass).
+enum PassMode : int { kPacked = 0, kSplit8 = 1, kSplit16 = 2, kMixed = 3 };
+
+template <int MODE>
+struct Mode {
+    static constexpr bool WIDE = MODE == kSplit16;
+    static constexpr int P_MAX = MODE == kPacked ? 4 : (WIDE ? 16 : 8);  // tokens per pass
+    static constexpr int C = WIDE ? 16 : 8;     // accumulator columns per reduction row
+    static constexpr int NT = WIDE ? 4 : 2;     // n-tiles at most
+    static constexpr int NH = WIDE ? 2 : 1;     // token halves per thread (split layouts)
 };
 
-template <int WT, bool WIDE, int T>
+constexpr int kXChunkBytes = kBlocks * 32 * 4;  // one token's X for one chunk (f32)
+
+template <int WT, int MODE, int T>
 struct Layout {
     static constexpr int kTileBytes = 16 * Fmt<WT>::ROWB;       // one tile, one box
     static constexpr int kBoxBytes = T * kTileBytes;            // the group's rows, one box
-    static constexpr int kStageBytes = Fmt<WT>::NBOX * kBoxBytes;
-    static constexpr int kRedBytes = kRedBufs * T * 16 * Cols<WIDE>::C * 4;
-    static constexpr int kBudget = 200 * 1024 - kRedBytes;
+    static constexpr int kWBytes = Fmt<WT>::NBOX * kBoxBytes;   // weights of a stage
+    static constexpr int kStageBytes = kWBytes + Mode<MODE>::P_MAX * kXChunkBytes;
+    static constexpr int kRedBytes = kRedBufs * T * 16 * Mode<MODE>::C * 4;
+    // epilogue inputs staged at the start of a pass: residual [P_MAX][T*16], bias [T*16]
+    static constexpr int kEpiBytes = (T * 16 * Mode<MODE>::P_MAX + T * 16) * 4;
+    static constexpr int kBudget = 200 * 1024 - kRedBytes - kEpiBytes;
     static constexpr int kStages = (kBudget / kStageBytes) > 8 ? 8 : (kBudget / kStageBytes);
     static_assert(kStages >= 2, "at least two stages");
 };
@@ -109,21 +125,14 @@ __device__ __forceinline__ void unpack_f16x2(uint32_t p, float &lo, float &hi) {
     asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(h));
 }
 
-// The three f16 terms of a pair of f32 values with |v| < 2^15, packed (lo, hi) per
-// term: v = t1 + t2 + t3 exactly when v is a multiple of 2^-24 (33 bits of f16
-// significand cover f32's 24; each subtraction is exact).
-__device__ __forceinline__ void split3(float a, float b, uint32_t &p1, uint32_t &p2,
-                                       uint32_t &p3) {
+// The two f16 terms of a pair of f32 values with |v| < 2^15, packed (lo, hi) per
+// term: t1 = f16(v), t2 = f16(v - t1) (the subtraction is exact), so
+// |v - t1 - t2| <= 2^-22 |v| while t2 is a normal f16, and <= 2^-25 below that.
+__device__ __forceinline__ void split2(float a, float b, uint32_t &p1, uint32_t &p2) {
     float a1, b1;
     p1 = pack_f16x2_rn(a, b);
     unpack_f16x2(p1, a1, b1);
-    a -= a1;
-    b -= b1;
-    p2 = pack_f16x2_rn(a, b);
-    unpack_f16x2(p2, a1, b1);
-    a -= a1;
-    b -= b1;
-    p3 = pack_f16x2_rn(a, b);
+    p2 = pack_f16x2_rn(a - a1, b - b1);
 }
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -216,6 +225,31 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// 4-byte global -> shared copy that does not hold a register (completes at
+// cp_async_wait_all).
+__device__ __forceinline__ void cp_async4(float *dst, const float *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Global -> shared bulk copy completing on `bar`, default L2 policy (X is read
+// by every CTA).
+__device__ __forceinline__ void bulk_g2s_nohint(void *dst, const void *src, uint32_t bytes,
+                                                uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
 }
@@ -243,21 +277,24 @@ __device__ __forceinline__ int group_tiles(const Sched &sc, long long u) {
     return (int)(e - u);
 }
 
-template <int WT, bool MOE, bool WIDE, int T>
+template <int WT, bool MOE, int MODE, int T>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap_t,
-                    const __grid_constant__ CUtensorMap wmap_1, const StreamArgs a) {
-    using L = Layout<WT, WIDE, T>;
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap_t, const StreamArgs a) {
+    using L = Layout<WT, MODE, T>;
+    using MD = Mode<MODE>;
     constexpr int S = L::kStages;
-    constexpr int C = Cols<WIDE>::C;
-    constexpr int P_MAX = WIDE ? 16 : 8;   // tokens per pass
-    constexpr int NT = WIDE ? 6 : 3;       // n-tiles at most
-    constexpr int NH = WIDE ? 2 : 1;       // tokens per thread in the split-major layout
+    constexpr bool WIDE = MD::WIDE;
+    constexpr int C = MD::C;
+    constexpr int P_MAX = MD::P_MAX;
+    constexpr int NT = MD::NT;
+    constexpr int NH = MD::NH;
     constexpr int NA = NH;                 // accumulator groups per tile
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *stages = smem;
     float *red = reinterpret_cast<float *>(smem + (size_t)S * L::kStageBytes);  // [4][T*16][C]
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + kRedBufs * T * 16 * C);
+    float *s_res = red + kRedBufs * T * 16 * C;      // [P_MAX][T*16]
+    float *s_bias = s_res + T * 16 * P_MAX;           // [T*16]
+    uint64_t *full = reinterpret_cast<uint64_t *>(s_bias + T * 16);
     uint64_t *empty = full + S;
     unsigned long long *s_key = reinterpret_cast<unsigned long long *>(empty + S);
     int *s_sorted = reinterpret_cast<int *>(s_key + kMaxSlots);
@@ -359,8 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
-        // A full group is one tall box per NBOX (T tiles of rows); a short group
-        // takes one 16-row box per tile.
+        // Every group is one tall box per NBOX (T tiles of rows).  A short group's
+        // extra rows belong to the next group or lie past the matrix (zero-filled
+        // by the TMA unit); they are computed and never stored.
         if (lane == 0) {
             const uint64_t policy = l2_evict_first();
             long long q = 0;
@@ -384,19 +422,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 break;
                             }
                         }
-                        mbar_arrive_expect_tx(&full[s],
-                                              (uint32_t)(Fmt<WT>::NBOX * nt * L::kTileBytes));
+                        // X of the pass's tokens for this chunk (256 or 512 floats each).
+                        const int npass = min(P_MAX, ntok - p0);
+                        const uint32_t xbytes = (uint32_t)min(kBlocks * 32, k - c * kBlocks * 32) * 4u;
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)L::kWBytes + npass * xbytes);
                         uint8_t *dst = stages + (size_t)s * L::kStageBytes;
                         for (int bx = 0; bx < Fmt<WT>::NBOX; ++bx) {
                             const int x = (c * Fmt<WT>::NBOX + bx) * (Fmt<WT>::ROWB / 2);
-                            if (nt == T) {
-                                tma_load_2d(dst + bx * L::kBoxBytes, &wmap_t, x, tile_row(u),
-                                            &full[s], policy);
-                            } else {
-                                for (int tt = 0; tt < nt; ++tt)
-                                    tma_load_2d(dst + bx * L::kBoxBytes + tt * L::kTileBytes,
-                                                &wmap_1, x, tile_row(u + tt), &full[s], policy);
-                            }
+                            tma_load_2d(dst + bx * L::kBoxBytes, &wmap_t, x, tile_row(u),
+                                        &full[s], policy);
+                        }
+                        for (int i = 0; i < npass; ++i) {
+                            const int tok = MOE ? s_sorted[seg0 + p0 + i] / a.topk : p0 + i;
+                            bulk_g2s_nohint(dst + L::kWBytes + i * kXChunkBytes,
+                                            a.X + (size_t)tok * k + (size_t)c * kBlocks * 32,
+                                            xbytes, &full[s]);
                         }
                     }
                 }
@@ -424,22 +464,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             // One pass over the group's chunks; the column layout is a compile-time
             // choice so the tile loop carries no layout branches.
             auto pass = [&](auto pk) {
-                // packed: 1-2 tokens, column g = split (g / P) of token (g % P), one n-tile;
+                // packed: 1-4 tokens, column g = term (g / P) of token (g % P), one n-tile;
                 // else split-major: n-tile s, column g = token g (+8 for the second half).
                 constexpr bool packed = decltype(pk)::value;
                 const int P = packed ? ntok : (WIDE ? 16 : 8);
-                int xrow[NH];
+                int xslot[NH];  // the token slot of this thread's B column in the stage
                 bool tok_ok[NH];
                 int col_s = 0;  // packed: which split this thread's column carries
     #pragma unroll
                 for (int h = 0; h < NH; ++h) {
                     const int i = packed ? g % P : h * 8 + g;
-                    tok_ok[h] = packed ? (g < 3 * P) : (i < ntok);
-                    const int r = p0 + (tok_ok[h] ? i : 0);
-                    xrow[h] = MOE ? s_sorted[seg0 + r] / a.topk : r;
+                    tok_ok[h] = packed ? (g < 2 * P) : (i < ntok);
+                    xslot[h] = tok_ok[h] ? i : 0;
                 }
                 if (packed) col_s = g / P;
 
+                // Stage this pass's bias and residual values in shared memory now, so the
+                // epilogue does not wait on global loads (same index map as the epilogue).
+                {
+                    const int R = ntiles * 16;
+                    for (int idx = threadIdx.x; idx < R * ntok; idx += kCW * 32) {
+                        const int i = idx / R, r = idx % R, row = row0 + r;
+                        if (row < m) {
+                            if (a.flags & kResidual) {
+                                const int yrow = MOE ? s_sorted[seg0 + p0 + i] : p0 + i;
+                                cp_async4(&s_res[idx], a.R + (size_t)yrow * m + row);
+                            }
+                            if (i == 0 && (a.flags & kBias))
+                                cp_async4(&s_bias[r], a.bias + (MOE ? (size_t)e * m + row : (size_t)row));
+                        }
+                    }
+                    cp_async_commit();
+                }
                 float acc[T][NA][4];
     #pragma unroll
                 for (int tt = 0; tt < T; ++tt)
@@ -448,24 +504,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll
                         for (int r = 0; r < 4; ++r) acc[tt][j][r] = 0.f;
 
-                // X of this warp's block of a chunk, in the element order of the A decode:
-                // (4t..4t+3, 16+4t..19+4t) for Q4_0, (8t..8t+7) for Q8_0.
-                auto load_x = [&](int c, float (&xv)[NH][8]) {
-                    const int blk = c * kBlocks + warp;
-    #pragma unroll
-                    for (int h = 0; h < NH; ++h) {
-                        float4 u0v = make_float4(0.f, 0.f, 0.f, 0.f), u1v = u0v;
-                        if (blk < nb && tok_ok[h]) {
-                            const float *xp = a.X + (size_t)xrow[h] * k + (size_t)blk * 32;
-                            u0v = __ldg(reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 4 * t : 8 * t)));
-                            u1v = __ldg(reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 16 + 4 * t : 8 * t + 4)));
-                        }
-                        xv[h][0] = u0v.x; xv[h][1] = u0v.y; xv[h][2] = u0v.z; xv[h][3] = u0v.w;
-                        xv[h][4] = u1v.x; xv[h][5] = u1v.y; xv[h][6] = u1v.z; xv[h][7] = u1v.w;
-                    }
-                };
-                float xcur[NH][8];
-                load_x(0, xcur);
                 // The warp's block sits at the same offset in every stage; its code bytes
                 // start 4-byte aligned when the block's byte offset is 2 mod 4.
                 const int wb = warp;
@@ -474,8 +512,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (wb % Fmt<WT>::BOXB) * Fmt<WT>::BB + g * Fmt<WT>::ROWB;
 
                 for (int c = 0; c < KC; ++c) {
-                    float xnext[NH][8];
-                    if (c + 1 < KC) load_x(c + 1, xnext);
                     const int s = qs;
                     const uint32_t par = qph;
                     if (++qs == S) {
@@ -496,25 +532,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (c * kBlocks + wb < nb) {
                         // B: each token's block scaled by a power of two (block_scale), then
-                        // split exactly into three f16 terms; pairs in the A decode's order.
-                        uint32_t sp[NH][4][3];
+                        // split into two f16 terms; pairs in the A decode's order.
+                        uint32_t sp[NH][4][2];
                         float inv_own[NH];
+                        const uint8_t *xst = stages + (size_t)s * L::kStageBytes + L::kWBytes;
     #pragma unroll
                         for (int h = 0; h < NH; ++h) {
+                            // This thread's 8 values of its column's token, in the A decode's
+                            // order (zeros for a padding column).
+                            float xv[8];
+                            float4 u0v = make_float4(0.f, 0.f, 0.f, 0.f), u1v = u0v;
+                            if (tok_ok[h]) {
+                                const float *xp = reinterpret_cast<const float *>(
+                                    xst + xslot[h] * kXChunkBytes) + wb * 32;
+                                u0v = *reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 4 * t : 8 * t));
+                                u1v = *reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 16 + 4 * t : 8 * t + 4));
+                            }
+                            xv[0] = u0v.x; xv[1] = u0v.y; xv[2] = u0v.z; xv[3] = u0v.w;
+                            xv[4] = u1v.x; xv[5] = u1v.y; xv[6] = u1v.z; xv[7] = u1v.w;
                             float mx = 0.f;
     #pragma unroll
-                            for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(xcur[h][j]));
+                            for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(xv[j]));
                             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
                             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
                             float sc;
                             block_scale(mx, sc, inv_own[h]);
                             float xs[8];
     #pragma unroll
-                            for (int j = 0; j < 8; ++j) xs[j] = xcur[h][j] * sc;
-                            split3(xs[0], xs[2], sp[h][0][0], sp[h][0][1], sp[h][0][2]);
-                            split3(xs[1], xs[3], sp[h][1][0], sp[h][1][1], sp[h][1][2]);
-                            split3(xs[4], xs[6], sp[h][2][0], sp[h][2][1], sp[h][2][2]);
-                            split3(xs[5], xs[7], sp[h][3][0], sp[h][3][1], sp[h][3][2]);
+                            for (int j = 0; j < 8; ++j) xs[j] = xv[j] * sc;
+                            split2(xs[0], xs[2], sp[h][0][0], sp[h][0][1]);
+                            split2(xs[1], xs[3], sp[h][1][0], sp[h][1][1]);
+                            split2(xs[4], xs[6], sp[h][2][0], sp[h][2][1]);
+                            split2(xs[5], xs[7], sp[h][3][0], sp[h][3][1]);
                         }
                         // 1/scale of the accumulator columns 2t and 2t+1: that of the threads
                         // whose B column they are (g = 2t, 2t+1).
@@ -535,12 +584,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     const int pr = ks * 2 + rr;
                                     uint32_t v;
                                     if (WIDE) {
-                                        v = sp[nt & 1][pr][nt >> 1];  // n-tile = 2 * split + half
+                                        v = sp[nt & 1][pr][nt >> 1];  // n-tile = 2 * term + half
                                     } else if (packed) {
-                                        v = col_s == 0 ? sp[0][pr][0]
-                                                       : (col_s == 1 ? sp[0][pr][1] : sp[0][pr][2]);
+                                        v = col_s == 0 ? sp[0][pr][0] : sp[0][pr][1];
                                     } else {
-                                        v = sp[0][pr][nt];            // n-tile = split
+                                        v = sp[0][pr][nt];            // n-tile = term
                                     }
                                     bf[ks][nt][rr] = v;
                                 }
@@ -599,13 +647,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     mma_f16(part, a2, bf[1][0][0], bf[1][0][1]);
                                     scale_acc(acc[tt][0], part, d0, d1, inv0[0], inv1[0]);
                                 } else {
-                                    // The three splits of a token sit in the same thread and
-                                    // column of three n-tiles: one accumulator chain sums them.
+                                    // The two terms of a token sit in the same thread and column
+                                    // of two n-tiles: one accumulator chain sums them.
     #pragma unroll
                                     for (int h = 0; h < NH; ++h) {
                                         float part[4];
     #pragma unroll
-                                        for (int sp_i = 0; sp_i < 3; ++sp_i) {
+                                        for (int sp_i = 0; sp_i < 2; ++sp_i) {
                                             const int nt = WIDE ? 2 * sp_i + h : sp_i;
                                             if (sp_i == 0)
                                                 mma_f16_z(part, a1, bf[0][nt][0], bf[0][nt][1]);
@@ -625,11 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[s]);
-    #pragma unroll
-                    for (int h = 0; h < NH; ++h)
-    #pragma unroll
-                        for (int j = 0; j < 8; ++j) xcur[h][j] = xnext[h][j];
                 }
+                cp_async_wait_all();  // staged bias/residual: visible to all after the barrier
                 // Every consumer warp gets here, aborted or not; the flag read after the
                 // barrier is the same in all of them, so they leave (or go on) together.
                 consumers_sync();
@@ -668,18 +713,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll
                         for (int b = 0; b < kRedBufs; ++b) {
                             const float *rp = red + b * RT + r * C;
-                            v += packed ? (rp[i] + rp[P + i]) + rp[2 * P + i] : rp[i];
+                            v += packed ? rp[i] + rp[P + i] : rp[i];
                         }
                         const int yrow = MOE ? s_sorted[seg0 + p0 + i] : p0 + i;
-                        const size_t o = (size_t)yrow * m + row;
-                        const float *bj = a.bias + (MOE ? (size_t)e * m + row : (size_t)row);
-                        a.Y[o] = epilogue(v, a.flags, bj, a.R + o);
+                        a.Y[(size_t)yrow * m + row] = epilogue_vals(v, a.flags, s_bias[r], s_res[idx]);
                     }
                 }
                 consumers_sync();
             };
-            if constexpr (!WIDE) {
-                if (ntok <= 2)
+            if constexpr (MODE == kPacked) {
+                pass(std::true_type{});
+            } else if constexpr (MODE == kMixed) {
+                if (ntok <= 4)
                     pass(std::true_type{});
                 else
                     pass(std::false_type{});
@@ -705,10 +750,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int WT, bool WIDE, int T>
+template <int WT, int MODE, int T>
 constexpr size_t smem_bytes() {
-    using L = Layout<WT, WIDE, T>;
-    return (size_t)L::kStages * L::kStageBytes + L::kRedBytes + 2 * L::kStages * sizeof(uint64_t) +
+    using L = Layout<WT, MODE, T>;
+    return (size_t)L::kStages * L::kStageBytes + L::kRedBytes + L::kEpiBytes +
+           2 * L::kStages * sizeof(uint64_t) +
            kMaxSlots * sizeof(unsigned long long) + (3 * kMaxSlots + 4) * sizeof(int) + 16;
 }
 
@@ -727,20 +773,27 @@ bool make_map(CUtensorMap &map, const StreamArgs &a, int wtype, long long rows, 
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int WT, bool MOE, bool WIDE, int T>
+template <int WT, bool MOE, int MODE, int T>
 cudaError_t launch_inst(const StreamArgs &a, long long rows, int grid, const DeviceInfo &dev,
                         cudaStream_t stream) {
     static std::atomic<unsigned long long> smem_set{0};
-    CUtensorMap map_t, map_1;
-    if (!make_map(map_t, a, WT, rows, T * 16) || !make_map(map_1, a, WT, rows, 16))
-        return cudaErrorInvalidValue;
-    auto kern = gemv_mma_kernel<WT, MOE, WIDE, T>;
-    constexpr size_t bytes = smem_bytes<WT, WIDE, T>();
+    CUtensorMap map_t;
+    if (!make_map(map_t, a, WT, rows, T * 16)) return cudaErrorInvalidValue;
+    auto kern = gemv_mma_kernel<WT, MOE, MODE, T>;
+    constexpr size_t bytes = smem_bytes<WT, MODE, T>();
     static_assert(bytes <= 227 * 1024, "shared memory budget");
     cudaError_t err = ensure_smem(kern, (int)bytes, dev, smem_set);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, bytes, stream>>>(map_t, map_1, a);
+    kern<<<grid, kThreads, bytes, stream>>>(map_t, a);
     return cudaGetLastError();
+}
+
+template <int WT, int MODE>
+cudaError_t launch_gemv_mode(const StreamArgs &a, int grid, long long per, const DeviceInfo &dev,
+                             cudaStream_t stream) {
+    if (per <= 2) return launch_inst<WT, false, MODE, 2>(a, a.m, grid, dev, stream);
+    if (per <= 4) return launch_inst<WT, false, MODE, 4>(a, a.m, grid, dev, stream);
+    return launch_inst<WT, false, MODE, 6>(a, a.m, grid, dev, stream);
 }
 
 template <int WT>
@@ -748,10 +801,9 @@ cudaError_t launch_gemv_wt(const StreamArgs &a, const DeviceInfo &dev, cudaStrea
     const long long tiles = (a.m + 15) / 16;
     const int grid = (int)(tiles < dev.sm_count ? tiles : dev.sm_count);
     const long long per = (tiles + grid - 1) / grid;  // tiles per CTA (max)
-    if (a.n > 8) return launch_inst<WT, false, true, 3>(a, a.m, grid, dev, stream);
-    if (per <= 2) return launch_inst<WT, false, false, 2>(a, a.m, grid, dev, stream);
-    if (per <= 4) return launch_inst<WT, false, false, 4>(a, a.m, grid, dev, stream);
-    return launch_inst<WT, false, false, 6>(a, a.m, grid, dev, stream);
+    if (a.n > 8) return launch_inst<WT, false, kSplit16, 3>(a, a.m, grid, dev, stream);
+    if (a.n > 4) return launch_gemv_mode<WT, kSplit8>(a, grid, per, dev, stream);
+    return launch_gemv_mode<WT, kPacked>(a, grid, per, dev, stream);
 }
 
 }  // namespace
@@ -770,8 +822,8 @@ cudaError_t launch_mma_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev
                            cudaStream_t stream) {
     const long long rows = (long long)a.n_experts * a.m;
     const int grid = dev.sm_count;
-    return wtype == kQ4_0 ? launch_inst<kQ4_0, true, false, 6>(a, rows, grid, dev, stream)
-                          : launch_inst<kQ8_0, true, false, 4>(a, rows, grid, dev, stream);
+    return wtype == kQ4_0 ? launch_inst<kQ4_0, true, kMixed, 6>(a, rows, grid, dev, stream)
+                          : launch_inst<kQ8_0, true, kMixed, 4>(a, rows, grid, dev, stream);
 }
 
 }  // namespace wq

@@ -83,6 +83,17 @@ __device__ __forceinline__ float epilogue(float acc, unsigned flags, const float
     return v;
 }
 
+// The same, with the bias and residual values already loaded (e.g. staged in
+// shared memory); each is used only when its flag is set.
+__device__ __forceinline__ float epilogue_vals(float acc, unsigned flags, float bias_j,
+                                               float res_ij) {
+    float v = acc;
+    if (flags & kBias) v += bias_j;
+    if (flags & kGelu) v = gelu_erf(v);
+    if (flags & kResidual) v += res_ij;
+    return v;
+}
+
 // ------------------------------------------------------- mbarrier + bulk copy --
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
