@@ -67,6 +67,7 @@ __device__ __forceinline__ void load_w_tile(const GemmArgs &a, int j0, int kk, i
 
 template <int WT>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const GemmArgs a) {
+    pdl_enter();
     __shared__ float xs[TK][TI + 4];
     __shared__ float ws[TK][TJ + 4];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -159,6 +160,7 @@ __device__ __forceinline__ void load_w4(const GemmArgs &a, int j, int kk, int q,
 
 template <int WT>
 __global__ void __launch_bounds__(256) gemm_splitk_kernel(const GemmArgs a, int steps_per_rank) {
+    pdl_enter();
     namespace cg = cooperative_groups;
     __shared__ float xs[SK][SK + 4];   // [k][i]
     __shared__ float ws[SK][SK + 4];   // [k][j]
@@ -238,18 +240,21 @@ cudaError_t launch_splitk_wt(const GemmArgs &a, int tiles_m, int tiles_n, int ks
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = (unsigned)ks;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_splitk_kernel<WT>, a, spr);
 }
 
 template <int WT>
 __global__ void dequant_kernel(int m, int k, const uint8_t *W, float *out) {
+    pdl_enter();
     // One thread per 8 weights.
     const long long units = (long long)m * (k / 8);
     const size_t rb = row_bytes(WT, k);
@@ -309,11 +314,10 @@ cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev
     }
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     switch (wtype) {
-    case kBF16: gemm_simt_kernel<kBF16><<<grid, 256, 0, stream>>>(a); break;
-    case kQ8_0: gemm_simt_kernel<kQ8_0><<<grid, 256, 0, stream>>>(a); break;
-    default: gemm_simt_kernel<kQ4_0><<<grid, 256, 0, stream>>>(a); break;
+    case kBF16: return launch_pdl(gemm_simt_kernel<kBF16>, grid, dim3(256), 0, stream, a);
+    case kQ8_0: return launch_pdl(gemm_simt_kernel<kQ8_0>, grid, dim3(256), 0, stream, a);
+    default: return launch_pdl(gemm_simt_kernel<kQ4_0>, grid, dim3(256), 0, stream, a);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out,
@@ -323,11 +327,10 @@ cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
     switch (wtype) {
-    case kBF16: dequant_kernel<kBF16><<<(int)blocks, 256, 0, stream>>>(m, k, W, out); break;
-    case kQ8_0: dequant_kernel<kQ8_0><<<(int)blocks, 256, 0, stream>>>(m, k, W, out); break;
-    default: dequant_kernel<kQ4_0><<<(int)blocks, 256, 0, stream>>>(m, k, W, out); break;
+    case kBF16: return launch_pdl(dequant_kernel<kBF16>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
+    case kQ8_0: return launch_pdl(dequant_kernel<kQ8_0>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
+    default: return launch_pdl(dequant_kernel<kQ4_0>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace wq

@@ -64,6 +64,7 @@ template <int BN, bool ATMA>
 __global__ void __launch_bounds__(Roles<ATMA>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap xmap,
                    const GemmArgs a) {
+    pdl_enter();
     using L = Smem<BN>;
     constexpr int NW = Roles<ATMA>::kWork;
     extern __shared__ uint8_t smem_raw[];
@@ -316,12 +317,12 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
     if (err != cudaSuccess) return err;
     dim3 grid((a.m + BN - 1) / BN, (a.n + BM - 1) / BM);
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-    kern<<<grid, Roles<ATMA>::kThreads, Smem<BN>::kBytes, stream>>>(wmap, xmap, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(Roles<ATMA>::kThreads), Smem<BN>::kBytes, stream, wmap, xmap, a);
 }
 
 // X f32 -> bf16, round to nearest even (the rounding the fused path applies).
 __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict__ xb, size_t n4) {
+    pdl_enter();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
          i += (size_t)gridDim.x * blockDim.x) {
         const float4 v = __ldg(x + i);
@@ -355,9 +356,9 @@ cudaError_t launch_gemm_tc_ws(const GemmArgs &a, void *workspace, const DeviceIn
     long long blocks = (long long)((n4 + 255) / 256);
     const long long cap = (long long)dev.sm_count * 8;
     if (blocks > cap) blocks = cap;
-    x_to_bf16_kernel<<<(int)blocks, 256, 0, stream>>>(reinterpret_cast<const float4 *>(a.X),
-                                                     reinterpret_cast<uint2 *>(workspace), n4);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(x_to_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                                 reinterpret_cast<const float4 *>(a.X),
+                                 reinterpret_cast<uint2 *>(workspace), n4);
     if (err != cudaSuccess) return err;
     if (gemm_tcp_supported(a)) return launch_gemm_tcp(a, workspace, dev, stream);
     return launch_tc<true>(a, workspace, dev, stream);

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap xmap,
                     const __grid_constant__ CUtensorMap ymap,
                     const __grid_constant__ CUtensorMap rmap, const GemmArgs a) {
+    pdl_enter();
     using L = PLayout<BN>;
     constexpr int S = L::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -316,8 +317,8 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
     const long long tiles =
         (long long)((a.n + BM - 1) / BM) * ((a.m + BN - 1) / BN);
     const int grid = (int)(tiles < dev.sm_count ? tiles : dev.sm_count);
-    kern<<<grid, kThreads, PLayout<BN>::kBytes, stream>>>(wmap, xmap, ymap, rmap, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), PLayout<BN>::kBytes, stream, wmap, xmap,
+                      ymap, rmap, a);
 }
 
 }  // namespace

@@ -280,6 +280,7 @@ __device__ __forceinline__ int group_tiles(const Sched &sc, long long u) {
 template <int WT, bool MOE, int MODE, int T>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap_t, const StreamArgs a) {
+    pdl_enter();
     using L = Layout<WT, MODE, T>;
     using MD = Mode<MODE>;
     constexpr int S = L::kStages;
@@ -784,8 +785,7 @@ cudaError_t launch_inst(const StreamArgs &a, long long rows, int grid, const Dev
     static_assert(bytes <= 227 * 1024, "shared memory budget");
     cudaError_t err = ensure_smem(kern, (int)bytes, dev, smem_set);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kThreads, bytes, stream>>>(map_t, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), bytes, stream, map_t, a);
 }
 
 template <int WT, int MODE>

@@ -57,6 +57,7 @@ constexpr size_t kSmemBytes = kSmemStages + kSmemBars + kSmemTot + kSmemMoe;
 
 template <int WT, bool MOE, int NT>
 __global__ void __launch_bounds__(kWarps * 32, 1) stream_kernel(const StreamArgs a) {
+    pdl_enter();
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *stages = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemStages);
@@ -308,8 +309,7 @@ cudaError_t launch_one(const StreamArgs &a, int grid, const DeviceInfo &dev, cud
     auto kern = stream_kernel<WT, MOE, NT>;
     cudaError_t err = ensure_smem(kern, (int)kSmemBytes, dev, smem_set);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kWarps * 32, kSmemBytes, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kWarps * 32), kSmemBytes, stream, a);
 }
 
 template <int WT>

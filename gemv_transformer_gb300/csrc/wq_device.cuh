@@ -94,6 +94,18 @@ __device__ __forceinline__ float epilogue_vals(float acc, unsigned flags, float 
     return v;
 }
 
+// ------------------------------------------------ programmatic dependent launch --
+
+// First statement of every kernel.  Lets the next kernel on the stream (launched
+// with programmatic serialization) be scheduled now, then waits until every grid
+// this one depends on has completed and its memory is visible: nothing below
+// touches global memory before that, so the ordering is that of a plain launch;
+// only launch latency and CTA setup overlap the previous kernel's tail.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------- mbarrier + bulk copy --
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

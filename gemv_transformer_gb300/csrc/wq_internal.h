@@ -62,6 +62,25 @@ wq_status check_gemm_args(int n, int m, int k, int wtype, unsigned flags, const 
                           const void *W, const float *bias, const float *residual,
                           const float *Y);
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel on the stream finishes; it waits for it in pdl_enter()
+// before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Cached per-device facts (current device).  Returns nullptr on a CUDA error.
 const DeviceInfo *device_info();
 unsigned long long wait_limit();
