@@ -13,8 +13,8 @@
 // Grids smaller than one wave (small n and m, e.g. n = 32, m = 512) instead run
 // gemm_splitk_kernel: 32 x 32 output tiles, the k steps of a tile split across the
 // KS CTAs of a thread-block cluster (KS <= 8), each CTA summing its steps the same
-// way; the CTA of cluster rank 0 then adds the KS partials in rank order through
-// distributed shared memory (deterministic) and applies the epilogue.
+// way; each CTA then adds the KS partials of one slice of the tile, in rank order,
+// through distributed shared memory (deterministic) and applies the epilogue.
 #include <cooperative_groups.h>
 
 #include "wq_device.cuh"
@@ -212,24 +212,25 @@ __global__ void __launch_bounds__(256) gemm_splitk_kernel(const GemmArgs a, int 
 #pragma unroll
         for (int v = 0; v < 2; ++v) red[(2 * ty + u) * SK + 2 * tx + v] = acc[u][v];
     cluster.sync();
-    if (rank == 0) {
+    // Every rank finishes a slice of the tile: the partials of ranks 0..KS-1, added
+    // in rank order (deterministic), loaded from their shared memory all at once.
+    const int slice = (SK * SK + KS - 1) / KS;
+    const int end = min(SK * SK, (rank + 1) * slice);
+    for (int idx = rank * slice + tid; idx < end; idx += 256) {
+        float p[8];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int i = i0 + 2 * ty + u;
+        for (int r = 0; r < 8; ++r) p[r] = r < KS ? cluster.map_shared_rank(red, r)[idx] : 0.f;
+        float sum = p[0];
 #pragma unroll
-            for (int v = 0; v < 2; ++v) {
-                const int j = j0 + 2 * tx + v;
-                const int idx = (2 * ty + u) * SK + 2 * tx + v;
-                float sum = red[idx];
-                for (int r = 1; r < KS; ++r) sum += cluster.map_shared_rank(red, r)[idx];
-                if (i < a.n && j < a.m) {
-                    const size_t o = (size_t)i * a.m + j;
-                    a.Y[o] = epilogue(sum, a.flags, a.bias + j, a.R + o);
-                }
-            }
+        for (int r = 1; r < 8; ++r)
+            if (r < KS) sum += p[r];
+        const int i = i0 + idx / SK, j = j0 + idx % SK;
+        if (i < a.n && j < a.m) {
+            const size_t o = (size_t)i * a.m + j;
+            a.Y[o] = epilogue(sum, a.flags, a.bias + j, a.R + o);
         }
     }
-    cluster.sync();  // the other ranks keep their shared memory until rank 0 has read it
+    cluster.sync();  // every rank keeps its shared memory until all slices are read
 }
 
 template <int WT>

@@ -321,12 +321,20 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
 }
 
 // X f32 -> bf16, round to nearest even (the rounding the fused path applies).
+// Four 16-byte loads in flight per thread per step (the copy is latency-bound
+// with one).
 __global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict__ xb, size_t n4) {
     pdl_enter();
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
-         i += (size_t)gridDim.x * blockDim.x) {
-        const float4 v = __ldg(x + i);
-        xb[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += 4 * stride) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (i + u * stride < n4) v[u] = __ldg(x + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (i + u * stride < n4)
+                xb[i + u * stride] = make_uint2(pack_bf16x2(v[u].x, v[u].y), pack_bf16x2(v[u].z, v[u].w));
     }
 }
 
@@ -353,7 +361,7 @@ size_t gemm_tc_workspace_bytes(int n, int k) { return ((size_t)n * k * 2 + 255) 
 cudaError_t launch_gemm_tc_ws(const GemmArgs &a, void *workspace, const DeviceInfo &dev,
                               cudaStream_t stream) {
     const size_t n4 = (size_t)a.n * a.k / 4;
-    long long blocks = (long long)((n4 + 255) / 256);
+    long long blocks = (long long)((n4 + 1023) / 1024);
     const long long cap = (long long)dev.sm_count * 8;
     if (blocks > cap) blocks = cap;
     cudaError_t err = launch_pdl(x_to_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,

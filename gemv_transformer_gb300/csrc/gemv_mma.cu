@@ -216,12 +216,13 @@ __device__ __forceinline__ void block_scale(float mx, float &s, float &inv) {
     inv = __uint_as_float((uint32_t)(254 - sb) << 23);
 }
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar, uint64_t policy) {
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint64_t *bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
+        "l"(policy)
         : "memory");
 }
 
@@ -390,10 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         seg0 = s_seg[ai];
         return s_seg[ai + 1] - seg0;
     };
-    auto tile_row = [&](long long u) -> int {
-        const int ai = (int)(u / sc.tpe), j = (int)(u % sc.tpe) * 16;
-        return MOE ? s_act[ai] * m + j : j;
-    };
+    auto tile_row = [&](long long u) -> int { return (int)(u % sc.tpe) * 16; };
+    auto tile_mat = [&](long long u) -> int { return MOE ? s_act[(int)(u / sc.tpe)] : 0; };
 
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
@@ -430,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint8_t *dst = stages + (size_t)s * L::kStageBytes;
                         for (int bx = 0; bx < Fmt<WT>::NBOX; ++bx) {
                             const int x = (c * Fmt<WT>::NBOX + bx) * (Fmt<WT>::ROWB / 2);
-                            tma_load_2d(dst + bx * L::kBoxBytes, &wmap_t, x, tile_row(u),
+                            tma_load_3d(dst + bx * L::kBoxBytes, &wmap_t, x, tile_row(u), tile_mat(u),
                                         &full[s], policy);
                         }
                         for (int i = 0; i < npass; ++i) {
@@ -759,27 +758,31 @@ constexpr size_t smem_bytes() {
            kMaxSlots * sizeof(unsigned long long) + (3 * kMaxSlots + 4) * sizeof(int) + 16;
 }
 
-bool make_map(CUtensorMap &map, const StreamArgs &a, int wtype, long long rows, int box_rows) {
+// The weight image as a 3-D tensor [matrices][m][row bytes] (one matrix for a GEMV,
+// the experts for MoE): a box that runs past a matrix's last row reads nothing
+// there (the rows are out of bounds and zero-filled), so a short row group at an
+// expert's end does not fetch the next expert's rows.
+bool make_map(CUtensorMap &map, const StreamArgs &a, int wtype, long long matrices, int box_rows) {
     auto encode = encode_fn();
     if (!encode) return false;
     const size_t rb = row_bytes(wtype, a.k);
     const int box = wtype == kQ4_0 ? Fmt<kQ4_0>::ROWB : Fmt<kQ8_0>::ROWB;
-    const cuuint64_t dims[2] = {(cuuint64_t)(rb / 2), (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)rb};
-    const cuuint32_t boxd[2] = {(cuuint32_t)(box / 2), (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t *>(a.W), dims,
+    const cuuint64_t dims[3] = {(cuuint64_t)(rb / 2), (cuuint64_t)a.m, (cuuint64_t)matrices};
+    const cuuint64_t strides[2] = {(cuuint64_t)rb, (cuuint64_t)rb * a.m};
+    const cuuint32_t boxd[3] = {(cuuint32_t)(box / 2), (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint8_t *>(a.W), dims,
                   strides, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int WT, bool MOE, int MODE, int T>
-cudaError_t launch_inst(const StreamArgs &a, long long rows, int grid, const DeviceInfo &dev,
+cudaError_t launch_inst(const StreamArgs &a, long long matrices, int grid, const DeviceInfo &dev,
                         cudaStream_t stream) {
     static std::atomic<unsigned long long> smem_set{0};
     CUtensorMap map_t;
-    if (!make_map(map_t, a, WT, rows, T * 16)) return cudaErrorInvalidValue;
+    if (!make_map(map_t, a, WT, matrices, T * 16)) return cudaErrorInvalidValue;
     auto kern = gemv_mma_kernel<WT, MOE, MODE, T>;
     constexpr size_t bytes = smem_bytes<WT, MODE, T>();
     static_assert(bytes <= 227 * 1024, "shared memory budget");
@@ -791,9 +794,9 @@ cudaError_t launch_inst(const StreamArgs &a, long long rows, int grid, const Dev
 template <int WT, int MODE>
 cudaError_t launch_gemv_mode(const StreamArgs &a, int grid, long long per, const DeviceInfo &dev,
                              cudaStream_t stream) {
-    if (per <= 2) return launch_inst<WT, false, MODE, 2>(a, a.m, grid, dev, stream);
-    if (per <= 4) return launch_inst<WT, false, MODE, 4>(a, a.m, grid, dev, stream);
-    return launch_inst<WT, false, MODE, 6>(a, a.m, grid, dev, stream);
+    if (per <= 2) return launch_inst<WT, false, MODE, 2>(a, 1, grid, dev, stream);
+    if (per <= 4) return launch_inst<WT, false, MODE, 4>(a, 1, grid, dev, stream);
+    return launch_inst<WT, false, MODE, 6>(a, 1, grid, dev, stream);
 }
 
 template <int WT>
@@ -801,7 +804,7 @@ cudaError_t launch_gemv_wt(const StreamArgs &a, const DeviceInfo &dev, cudaStrea
     const long long tiles = (a.m + 15) / 16;
     const int grid = (int)(tiles < dev.sm_count ? tiles : dev.sm_count);
     const long long per = (tiles + grid - 1) / grid;  // tiles per CTA (max)
-    if (a.n > 8) return launch_inst<WT, false, kSplit16, 3>(a, a.m, grid, dev, stream);
+    if (a.n > 8) return launch_inst<WT, false, kSplit16, 3>(a, 1, grid, dev, stream);
     if (a.n > 4) return launch_gemv_mode<WT, kSplit8>(a, grid, per, dev, stream);
     return launch_gemv_mode<WT, kPacked>(a, grid, per, dev, stream);
 }
@@ -820,10 +823,10 @@ cudaError_t launch_mma_gemv(const StreamArgs &a, int wtype, const DeviceInfo &de
 
 cudaError_t launch_mma_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,
                            cudaStream_t stream) {
-    const long long rows = (long long)a.n_experts * a.m;
+    const long long matrices = a.n_experts;
     const int grid = dev.sm_count;
-    return wtype == kQ4_0 ? launch_inst<kQ4_0, true, kMixed, 6>(a, rows, grid, dev, stream)
-                          : launch_inst<kQ8_0, true, kMixed, 4>(a, rows, grid, dev, stream);
+    return wtype == kQ4_0 ? launch_inst<kQ4_0, true, kMixed, 6>(a, matrices, grid, dev, stream)
+                          : launch_inst<kQ8_0, true, kMixed, 4>(a, matrices, grid, dev, stream);
 }
 
 }  // namespace wq
