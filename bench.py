@@ -2,7 +2,8 @@
 """Benchmark of the weight-format GEMM/GEMV path on GB300.
 
 One *step* is one pass of the whole hot path over the five workloads, nine
-launches through the C ABI:
+calls through the C ABI (twelve kernel launches: the three encoder GEMMs first
+round X to bf16 in their workspace):
     bf16 GEMM n=32 (bias+GELU) | Q8_0 GEMV n=1 | Q4_0 GEMV n=1, 4, 8 (+residual) |
     encoder bf16 GEMMs n=1500 qkv/up/down on the tensor cores | MoE Q4_0 routed GEMV.
 The metric is the step's fraction of its roofline: sum over launches of
@@ -11,12 +12,17 @@ measured step time.  Peaks are the measured ones in MEASURED_PEAKS.json.
 
 Timing: inputs resident in HBM; two rotating input sets (a step touches
 ~340 MB, so every buffer is re-read only after ~680 MB, > 5x the 129 MB L2);
-each step is a CUDA graph of the nine launches with a timing event between
-launches; K steps are replayed back to back between a barrier + synchronize and
+each step is a CUDA graph of the nine calls with a timing event between
+calls; K steps are replayed back to back between a barrier + synchronize and
 timed with CUDA events; per-launch durations come from the events of the last
-min(K, 64) steps of that timed region.  `e2e` times the same steps driven from
+min(K, 64) steps of that timed region.  Every kernel is launched with
+programmatic stream serialization, so a kernel's launch overlaps the tail of the
+previous one.  `e2e` times the same steps driven from
 the host through the Python binding, with the activations copied from pinned
 host memory before and the outputs copied back after every step.
+
+`--case NAME [--reps N]` runs only that workload's call N times, untimed (the
+command the committed ncu summaries were taken with).
 
 `--impl reference` times the f64 CPU oracle (the only independent
 implementation of this path; the pages' wgpu kernels cannot run here) on a
@@ -91,6 +97,34 @@ def algorithmic(w):
     if w["flags"] & synth.FLAG_RESIDUAL:
         b += n * m * 4
     return b, 2.0 * n * m * k
+
+
+def kernels_per_call(w):
+    """Kernels one call launches: the workspace tensor-core GEMM converts X to bf16
+    first (two launches); every other call is one launch."""
+    return 2 if w["kind"] == "gemm_tc" else 1
+
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of `python bench.py --case NAME`, keyed by workload, with the SHA-256 of
+# the kernel source it was taken on; reported only while that source is unchanged.
+TRAFFIC = {
+    # one ncu capture: 88,088,576 B read + 2,148,352 B written per launch
+    "moe_q4_0_E64_m1408_k2048_t16x6": {
+        "bytes": 90236928, "source": "gemv_transformer_gb300/csrc/gemv_mma.cu",
+        "sha256": "00e5c1d9b650edf1d0c2eb40ad0fe9434ae74224ddba8bace636689267c54231"},
+}
+
+
+def traffic_for(name):
+    import hashlib
+    rec = TRAFFIC.get(name)
+    if not rec:
+        return None
+    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
+            return None
+    return rec["bytes"]
 
 
 def roofline_us(w, peaks):
@@ -465,7 +499,7 @@ def run_gpu(args):
               "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     rl["frac"] = rl["achieved"] / rl["peak"]
     rl["kernel"] = ws[dom]["name"]
-    rl["traffic"] = None
+    rl["traffic"] = traffic_for(ws[dom]["name"])
     rl["peak_source"] = peaks["source"]
 
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -476,8 +510,10 @@ def run_gpu(args):
                                   "GEMMs n1500 (tcgen05) + MoE Q4_0 E64 top6",
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                       "l2": "inputs larger than L2: 2 rotating input sets of ~340 MB",
-                      "launches_per_step": nl, "workloads": detail},
-           "gpu_launches": nl * args.steps,
+                      "calls_per_step": nl,
+                      "kernels_per_step": sum(kernels_per_call(w) for w in ws),
+                      "workloads": detail},
+           "gpu_launches": sum(kernels_per_call(w) for w in ws) * args.steps,
            "roofline": rl,
            "e2e": {"value": roof_us / (e2e_ms * 1e3) * 100.0, "unit": UNIT,
                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -490,6 +526,31 @@ def run_gpu(args):
     return 0
 
 
+def run_case(args):
+    """Run one workload's C-ABI call `--reps` times, untimed (for profilers)."""
+    import torch
+    torch.cuda.set_device(0)
+    from gemv_transformer_gb300 import build
+    build.build()
+    import gemv_transformer_gb300 as wq
+    wq.load()
+    ws = [w for w in make_workloads() if w["name"] == args.case]
+    if not ws:
+        names = ", ".join(w["name"] for w in make_workloads())
+        raise SystemExit(f"unknown --case {args.case!r}; one of: {names}")
+    lset = Launches(ws, wq, torch, torch.device("cuda", 0))
+    for _ in range(args.reps):
+        st = lset.call(0)
+        if st != 0:
+            raise RuntimeError(f"{args.case}: {wq.wq_status_string(st)}")
+    torch.cuda.synchronize()
+    st = wq.wq_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status: {wq.wq_status_string(st)}")
+    print(f"ran {args.case} x{args.reps}")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -497,7 +558,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["wq", "reference"], default="wq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="run only this workload's call --reps times, untimed (for ncu)")
+    ap.add_argument("--reps", type=int, default=4)
     args = ap.parse_args(argv)
+    if args.case:
+        return run_case(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
