@@ -115,8 +115,11 @@ def dequant(wtype: int, m: int, k: int, W: np.ndarray) -> np.ndarray:
 
 
 def gemm(n, m, k, wtype, flags, X, W, bias=None, residual=None, round_x=False,
-         rows=None, threads=0, bound=True):
+         rows=None, threads=0, bound=True, round_w=False):
     """f64 ``(Y [n][m], S [n][m])`` of ``epi(X . W^T)``.
+
+    ``round_x`` / ``round_w`` feed X / the dequantised W rounded to the nearest
+    bf16 (ties to even): the operands of the tensor-core path.
 
     ``rows=(j0, j1)`` restricts the computed output columns (W rows) to
     ``[j0, j1)``; the rest of Y and S stays NaN.
@@ -126,7 +129,8 @@ def gemm(n, m, k, wtype, flags, X, W, bias=None, residual=None, round_x=False,
     Y = np.full((n, m), np.nan, dtype=np.float64)
     S = np.full((n, m), np.nan, dtype=np.float64) if bound else None
     j0, j1 = (0, m) if rows is None else rows
-    rc = _load().oracle_gemm(n, m, k, wtype, flags, int(bool(round_x)), _ptr(Xc), _ptr(Wc),
+    rnd = int(bool(round_x)) | (int(bool(round_w)) << 1)
+    rc = _load().oracle_gemm(n, m, k, wtype, flags, rnd, _ptr(Xc), _ptr(Wc),
                              _ptr(bc), _ptr(Rc), _ptr(Y), _ptr(S), j0, j1, int(threads))
     if rc != 0:
         raise ValueError("oracle_gemm: bad arguments")

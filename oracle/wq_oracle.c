@@ -173,10 +173,12 @@ static int set_threads(int threads) {
  * Y[i][j] (f64, [n][m]) for all i < n and output rows j in [j0, j1).
  * X f32 [n][k]; W byte image [m][row_bytes]; bias f32 [m] (flag 1);
  * R f32 [n][m] (flag 4, the old Y); S (optional) gets the bound.
- * round_x != 0 feeds bf16-rounded X (tensor-core check).  threads <= 0: all.
+ * round: bit 0 feeds bf16-rounded X, bit 1 bf16-rounded W (each dequantised value
+ * d*q, exact in f64, rounded to the nearest bf16, ties to even): the operands of
+ * the tensor-core path.  threads <= 0: all.
  * Returns 0, or -1 on a bad argument.
  */
-int oracle_gemm(int n, int m, int k, int wtype, unsigned flags, int round_x,
+int oracle_gemm(int n, int m, int k, int wtype, unsigned flags, int round,
                 const float *X, const uint8_t *W, const float *bias, const float *R,
                 double *Y, double *S, int j0, int j1, int threads) {
     if (n < 0 || !shape_ok(wtype, m, k) || j0 < 0 || j1 > m || j0 > j1) return -1;
@@ -184,6 +186,7 @@ int oracle_gemm(int n, int m, int k, int wtype, unsigned flags, int round_x,
     size_t rb = row_bytes(wtype, k);
     int nt = set_threads(threads);
     int bad = 0;
+    const int round_x = round & 1, round_w = (round >> 1) & 1;
 #pragma omp parallel num_threads(nt)
     {
         double *w = (double *)malloc(sizeof(double) * (size_t)k);
@@ -194,6 +197,8 @@ int oracle_gemm(int n, int m, int k, int wtype, unsigned flags, int round_x,
 #pragma omp for schedule(dynamic, 4)
             for (int j = j0; j < j1; ++j) {
                 dequant_row(wtype, W + rb * j, k, w);
+                if (round_w)
+                    for (int t = 0; t < k; ++t) w[t] = oracle_round_bf16(w[t]);
                 for (int i = 0; i < n; ++i) {
                     size_t o = (size_t)i * m + j;
                     dot_epi(k, flags, round_x, X + (size_t)i * k, w, bias ? bias + j : NULL,

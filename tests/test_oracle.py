@@ -281,6 +281,42 @@ def test_round_x_feeds_bf16_rounded_inputs(oracle_mod):
     assert (Ya == Yb).all()
 
 
+@pytest.mark.parametrize("d_bits,q,exact,rounded", [
+    (0x3C01, 3, 3.0029296875, 3.0),            # (1 + 2^-10) * 3: below half a bf16 step
+    (0x3C01, 5, 5.0048828125, 5.0),
+    (0x3C0C, 1, 1.01171875, 1.015625),         # 1 + 1.5 * 2^-7: a tie, to the even neighbour
+    (0x3C00, -7, -7.0, -7.0),                  # exact in bf16: unchanged
+    (0x5BFF, 127, 32496.125, 32512.0),         # 255.875 * 127; bf16 step 128 there
+])
+def test_round_w_rounds_each_dequantised_weight(oracle_mod, d_bits, q, exact, rounded):
+    """round_w=True feeds W = bf16_rne(d*q): a one-hot X picks the weight out."""
+    k = 32
+    d = np.full((1, 1), d_bits, np.uint16)
+    qs = np.zeros((1, k), np.int8)
+    qs[0, 5] = q
+    img = synth.encode_q8_0(d, qs)
+    X = np.zeros((1, k), np.float32)
+    X[0, 5] = 1.0
+    Ye, _ = oracle_mod.gemm(1, 1, k, Q8_0, 0, X, img)
+    Yr, Sr = oracle_mod.gemm(1, 1, k, Q8_0, 0, X, img, round_w=True)
+    assert Ye[0, 0] == exact and Yr[0, 0] == rounded and Sr[0, 0] == abs(rounded)
+
+
+def test_round_w_equals_bf16_rounded_dequantised_image(oracle_mod):
+    """round_w on a Q4_0 image equals round_w-free use of the torch-rounded (RNE)
+    dequantised weights written as bf16 pairs."""
+    g = synth.rng(31)
+    m, k = 24, 96
+    img = synth.draw_q4_0_weights(g, m, k)
+    X = synth.normal_f32(g, (3, k))
+    Wd = oracle_mod.dequant(Q4_0, m, k, img).astype(np.float32)
+    bits = torch.from_numpy(Wd).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    pairs = synth.bf16_pairs(bits)
+    Ya, _ = oracle_mod.gemm(3, m, k, Q4_0, 0, X, img, round_w=True)
+    Yb, _ = oracle_mod.gemm(3, m, k, BF16, 0, X, pairs)
+    assert (Ya == Yb).all()
+
+
 def test_bad_arguments(oracle_mod):
     img = np.zeros((2, 34), np.uint8)
     with pytest.raises(ValueError):
