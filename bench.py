@@ -79,6 +79,14 @@ def make_workloads():
     return ws
 
 
+def extra_workloads():
+    """Measured and reported beside the metric, not part of it: the quantised
+    large-n tensor-core GEMM (a prompt through GGML weights)."""
+    import synth
+    return [synth.workload_quant_prefill(wtype=synth.WTYPE_Q4_0),
+            synth.workload_quant_prefill(wtype=synth.WTYPE_Q8_0)]
+
+
 def algorithmic(w):
     """(bytes, flops) of one launch: every weight byte touched once, X read once,
     Y written once, bias and residual read when flagged, ids read once."""
@@ -100,9 +108,11 @@ def algorithmic(w):
 
 
 def kernels_per_call(w):
-    """Kernels one call launches: the workspace tensor-core GEMM converts X to bf16
-    first (two launches); every other call is one launch."""
-    return 2 if w["kind"] == "gemm_tc" else 1
+    """Kernels one call launches: the workspace tensor-core GEMM converts X (and a
+    quantised W) to bf16 first; every other call is one launch."""
+    if w["kind"] != "gemm_tc":
+        return 1
+    return 2 if w["wtype"] == 0 else 3  # quantised W is dequantised to bf16 first
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
@@ -477,6 +487,29 @@ def run_gpu(args):
         e2e_ms = max(e0.elapsed_time(e1), (time.perf_counter() - w0) * 1e3) / k_e2e
         barrier(world)
 
+        # Beside the metric: each extra workload alone, event-timed over back-to-back calls.
+        extra = []
+        for w in extra_workloads():
+            lset = Launches([w], wq, torch, device)
+            for _ in range(3):
+                lset.call(0)
+            x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 20
+            x0.record()
+            for _ in range(reps):
+                st = lset.call(0)
+                if st != 0:
+                    raise RuntimeError(f"{w['name']}: {wq.wq_status_string(st)}")
+            x1.record()
+            torch.cuda.synchronize()
+            t = x0.elapsed_time(x1) * 1e3 / reps
+            b, f = algorithmic(w)
+            r_us, bound = roofline_us(w, peaks)
+            extra.append({"name": w["name"], "us": round(t, 3), "TFLOP_s": round(f / t / 1e6, 2),
+                          "bound": bound, "roofline_pct": round(r_us / t * 100, 1),
+                          "kernels_per_call": kernels_per_call(w)})
+            del lset
+
     ms_step = max_over_ranks(el_ms / args.steps, world, device)
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     roof_us = sum(r[0] for r in roof)
@@ -512,7 +545,8 @@ def run_gpu(args):
                       "l2": "inputs larger than L2: 2 rotating input sets of ~340 MB",
                       "calls_per_step": nl,
                       "kernels_per_step": sum(kernels_per_call(w) for w in ws),
-                      "workloads": detail},
+                      "workloads": detail,
+                      "beside_the_metric": extra},
            "gpu_launches": sum(kernels_per_call(w) for w in ws) * args.steps,
            "roofline": rl,
            "e2e": {"value": roof_us / (e2e_ms * 1e3) * 100.0, "unit": UNIT,
@@ -534,9 +568,9 @@ def run_case(args):
     build.build()
     import gemv_transformer_gb300 as wq
     wq.load()
-    ws = [w for w in make_workloads() if w["name"] == args.case]
+    ws = [w for w in make_workloads() + extra_workloads() if w["name"] == args.case]
     if not ws:
-        names = ", ".join(w["name"] for w in make_workloads())
+        names = ", ".join(w["name"] for w in make_workloads() + extra_workloads())
         raise SystemExit(f"unknown --case {args.case!r}; one of: {names}")
     lset = Launches(ws, wq, torch, torch.device("cuda", 0))
     for _ in range(args.reps):

@@ -358,8 +358,70 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, const DeviceInfo &dev, cudaStream_
 
 size_t gemm_tc_workspace_bytes(int n, int k) { return ((size_t)n * k * 2 + 255) & ~(size_t)255; }
 
-cudaError_t launch_gemm_tc_ws(const GemmArgs &a, void *workspace, const DeviceInfo &dev,
-                              cudaStream_t stream) {
+// Quantised W -> bf16 [m][k]: each dequantised weight d*q (Q8_0) or d*(q-8) (Q4_0),
+// exact in f32, rounded to the nearest bf16 (ties to even).  One thread per
+// 32-weight block; a block starts 2-byte aligned, so it is read as 16-bit words.
+template <int WT>
+__global__ void w_to_bf16_kernel(const uint8_t *__restrict__ W, int m, int k,
+                                 uint4 *__restrict__ wb) {
+    pdl_enter();
+    const int nb = k / 32;
+    const long long blocks = (long long)m * nb;
+    const size_t rb = row_bytes(WT, k);
+    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < blocks;
+         u += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(u / nb), b = (int)(u % nb);
+        const uint16_t *bp = reinterpret_cast<const uint16_t *>(
+            W + (size_t)j * rb + (size_t)b * (WT == kQ8_0 ? 34 : 18));
+        const float d = half_bits_to_f32(bp[0]);
+        float w[32];
+        if (WT == kQ8_0) {
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {
+                const uint32_t v = bp[1 + h];
+                w[2 * h] = d * (float)(int8_t)(v & 0xFFu);
+                w[2 * h + 1] = d * (float)(int8_t)(v >> 8);
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t v = bp[1 + h];  // bytes 2h, 2h+1 of the 16 code bytes
+                w[2 * h] = d * (float)((int)(v & 0xFu) - 8);
+                w[2 * h + 1] = d * (float)((int)((v >> 8) & 0xFu) - 8);
+                w[16 + 2 * h] = d * (float)((int)((v >> 4) & 0xFu) - 8);
+                w[16 + 2 * h + 1] = d * (float)((int)(v >> 12) - 8);
+            }
+        }
+        uint4 *o = wb + ((size_t)j * k + (size_t)b * 32) / 8;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            o[c] = make_uint4(pack_bf16x2(w[8 * c], w[8 * c + 1]), pack_bf16x2(w[8 * c + 2], w[8 * c + 3]),
+                              pack_bf16x2(w[8 * c + 4], w[8 * c + 5]), pack_bf16x2(w[8 * c + 6], w[8 * c + 7]));
+    }
+}
+
+size_t gemm_tc_w_workspace_bytes(int m, int k) {
+    return ((size_t)m * k * 2 + 255) & ~(size_t)255;
+}
+
+cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
+                              const DeviceInfo &dev, cudaStream_t stream) {
+    GemmArgs g = a;
+    if (wtype != kBF16) {
+        // The weights first: bf16 after X in the workspace, then the bf16 GEMM.
+        uint8_t *wb = static_cast<uint8_t *>(workspace) + gemm_tc_workspace_bytes(a.n, a.k);
+        const long long blocks = (long long)a.m * (a.k / 32);
+        long long grid = (blocks + 255) / 256;
+        if (grid > (long long)dev.sm_count * 8) grid = (long long)dev.sm_count * 8;
+        cudaError_t err =
+            wtype == kQ8_0
+                ? launch_pdl(w_to_bf16_kernel<kQ8_0>, dim3((unsigned)grid), dim3(256), 0, stream,
+                             a.W, a.m, a.k, reinterpret_cast<uint4 *>(wb))
+                : launch_pdl(w_to_bf16_kernel<kQ4_0>, dim3((unsigned)grid), dim3(256), 0, stream,
+                             a.W, a.m, a.k, reinterpret_cast<uint4 *>(wb));
+        if (err != cudaSuccess) return err;
+        g.W = wb;
+    }
     const size_t n4 = (size_t)a.n * a.k / 4;
     long long blocks = (long long)((n4 + 1023) / 1024);
     const long long cap = (long long)dev.sm_count * 8;
@@ -368,8 +430,8 @@ cudaError_t launch_gemm_tc_ws(const GemmArgs &a, void *workspace, const DeviceIn
                                  reinterpret_cast<const float4 *>(a.X),
                                  reinterpret_cast<uint2 *>(workspace), n4);
     if (err != cudaSuccess) return err;
-    if (gemm_tcp_supported(a)) return launch_gemm_tcp(a, workspace, dev, stream);
-    return launch_tc<true>(a, workspace, dev, stream);
+    if (gemm_tcp_supported(g)) return launch_gemm_tcp(g, workspace, dev, stream);
+    return launch_tc<true>(g, workspace, dev, stream);
 }
 
 }  // namespace wq

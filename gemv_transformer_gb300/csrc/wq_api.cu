@@ -52,9 +52,7 @@ wq_status check_common(int n, int m, int k, int wtype, unsigned flags, const flo
 wq_status check_gemm_args(int n, int m, int k, int wtype, unsigned flags, const float *X,
                           const void *W, const float *bias, const float *residual,
                           const float *Y) {
-    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
-    if (s == WQ_OK && (flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
-    return s;
+    return check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
 }
 
 const DeviceInfo *device_info() {
@@ -126,9 +124,10 @@ wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X
                   const float *bias, const float *residual, float *Y, wq_stream_t stream) {
     wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
     if (s != WQ_OK) return s;
-    if ((flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
     if (n <= WQ_GEMV_MAX_N)
         return gemv_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream);
+    // Tensor cores with quantised W need the bf16 copy of W: wq_gemm_ws.
+    if ((flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
     const DeviceInfo *dev = device_info();
     if (!dev) return WQ_ERR_CUDA;
     GemmArgs a{};
@@ -149,8 +148,9 @@ wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X
 
 size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned flags) {
     if (n <= 0 || !shape_ok(wtype, m, k)) return 0;
-    if (!(flags & WQ_TC_BF16) || wtype != kBF16 || n <= WQ_GEMV_MAX_N) return 0;
-    return gemm_tc_workspace_bytes(n, k);
+    if (!(flags & WQ_TC_BF16) || n <= WQ_GEMV_MAX_N) return 0;
+    const size_t x = gemm_tc_workspace_bytes(n, k);
+    return wtype == kBF16 ? x : x + gemm_tc_w_workspace_bytes(m, k);
 }
 
 wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float *X,
@@ -158,7 +158,6 @@ wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float
                      void *workspace, size_t workspace_bytes, wq_stream_t stream) {
     wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
     if (s != WQ_OK) return s;
-    if ((flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
     const size_t need = wq_gemm_workspace_bytes(n, m, k, wtype, flags);
     if (need == 0)
         return wq_gemm(n, m, k, wtype, flags, X, W, bias, residual, Y, stream);
@@ -178,7 +177,7 @@ wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float
     a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
     a.status = dev->status;
     a.wait_limit = wait_limit();
-    return cuda_status(launch_gemm_tc_ws(a, workspace, *dev, (cudaStream_t)stream));
+    return cuda_status(launch_gemm_tc_ws(a, wtype, workspace, *dev, (cudaStream_t)stream));
 }
 
 wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtype,

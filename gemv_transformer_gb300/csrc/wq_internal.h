@@ -101,8 +101,9 @@ size_t gemm_tc_workspace_bytes(int n, int k);
 bool gemm_tcp_supported(const GemmArgs &a);
 cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
                             cudaStream_t stream);
-cudaError_t launch_gemm_tc_ws(const GemmArgs &a, void *workspace, const DeviceInfo &dev,
-                              cudaStream_t stream);
+size_t gemm_tc_w_workspace_bytes(int m, int k);
+cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
+                              const DeviceInfo &dev, cudaStream_t stream);
 cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out,
                            cudaStream_t stream);
 

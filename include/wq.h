@@ -83,9 +83,11 @@ enum {
     WQ_BIAS = 1u,
     WQ_GELU = 2u,
     WQ_RESIDUAL = 4u,
-    /* wq_gemm only, WQ_BF16 weights only: run the contraction on the tcgen05
-     * tensor cores with X rounded to bf16 (round to nearest even) and f32
-     * accumulation.  Without it every path multiplies exact f32 products. */
+    /* n > WQ_GEMV_MAX_N only: run the contraction on the tcgen05 tensor cores with
+     * X rounded to bf16 (round to nearest even) and f32 accumulation; quantised
+     * weights are dequantised and rounded to bf16 the same way (wq_gemm_ws and
+     * wq_gemm_noalloc only).  Without it every path multiplies exact f32
+     * products; smaller n ignore it (the GEMV kernels are exact). */
     WQ_TC_BF16 = 256u
 };
 
@@ -112,7 +114,8 @@ typedef enum {
  * Errors: WQ_ERR_INVALID_ARG for n, m, k <= 0; k % 32 != 0 (Q8_0/Q4_0) or
  * k % 8 != 0 (bf16); null X, W or Y; null bias/residual when its flag is set;
  * X or W not 16-byte aligned; unknown flag bits or wtype.  WQ_ERR_UNSUPPORTED for
- * WQ_TC_BF16 with a quantised wtype.  WQ_ERR_CUDA if the launch fails.
+ * WQ_TC_BF16 with a quantised wtype and n > WQ_GEMV_MAX_N (that needs the bf16
+ * copy of W in a workspace: wq_gemm_ws).  WQ_ERR_CUDA if the launch fails.
  */
 WQ_API wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X, const void *W,
                   const float *bias, const float *residual, float *Y, wq_stream_t stream);
@@ -123,6 +126,12 @@ WQ_API wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const f
  * operands to the tcgen05 kernel by TMA; that is faster than rounding X inside the
  * GEMM, where the f32 X in flight does not fit on chip.  The results are
  * identical to wq_gemm's (same rounding, same accumulation order per output).
+ * With WQ_TC_BF16 and Q8_0/Q4_0 weights (the quantised large-n GEMM, e.g. a
+ * prompt of many tokens through GGML weights) W is dequantised into the
+ * workspace as well, each weight d*q (or d*(q-8)) rounded to the nearest bf16,
+ * and the same tcgen05 kernel runs on the bf16 copy; both operands are then
+ * within 2^-8 of their exact values, inside the 8e-3 sum|x||w| contract of
+ * WQ_TC_BF16.
  * workspace: device memory of at least wq_gemm_workspace_bytes(n, m, k, wtype,
  * flags) bytes, 256-byte aligned, not overlapping any other argument; it is
  * overwritten and may be reused once the stream has passed this call.  When that
@@ -134,9 +143,10 @@ WQ_API wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, cons
                             const void *W, const float *bias, const float *residual, float *Y,
                             void *workspace, size_t workspace_bytes, wq_stream_t stream);
 
-/* Workspace bytes wq_gemm_ws needs for this call: 2*n*k rounded up to 256 when the
- * call takes the tensor-core path (WQ_TC_BF16, WQ_BF16 weights, n > WQ_GEMV_MAX_N),
- * else 0.  0 also for an invalid shape. */
+/* Workspace bytes wq_gemm_ws needs for this call when it takes the tensor-core
+ * path (WQ_TC_BF16, n > WQ_GEMV_MAX_N): 2*n*k rounded up to 256 (bf16 X), plus
+ * 2*m*k rounded up to 256 (bf16 W) for Q8_0/Q4_0 weights; else 0.  0 also for an
+ * invalid shape. */
 WQ_API size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned flags);
 
 /* Size of the fixed device scratch array behind wq_gemm_noalloc (one per device). */
@@ -148,9 +158,10 @@ WQ_API size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned f
  * block or fail (a serving loop with a frozen memory budget), a host application
  * that owns the device allocator, a runtime with no allocator.  None of the pages
  * this library follows has a counterpart; it is a library convenience.
- * The bf16 copy of X lives in a statically reserved device array of
- * WQ_GEMM_NOALLOC_SCRATCH_BYTES (16 MiB) per device, so the tensor-core route
- * takes 2*n*k <= 16 MiB (n*k <= 8,388,608; e.g. 1500 x 4096).  The call allocates
+ * The bf16 copy of X (and of W, for quantised weights) lives in a statically
+ * reserved device array of WQ_GEMM_NOALLOC_SCRATCH_BYTES (16 MiB) per device, so
+ * the tensor-core route takes wq_gemm_workspace_bytes(...) <= 16 MiB (bf16
+ * weights: n*k <= 8,388,608, e.g. 1500 x 4096).  The call allocates
  * nothing, by any route.  Nothing in the array needs to start at zero: each call
  * writes every byte it later reads.
  * Set-up: the first call on a device (with that device current) looks up the

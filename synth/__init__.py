@@ -227,3 +227,13 @@ def workload_moe(seed=5, n_experts=64, m=1408, k=2048, n_tok=16, topk=6):
                 wtype=WTYPE_Q4_0, n_tok=n_tok, topk=topk, n_experts=n_experts, m=m, k=k,
                 flags=0, W=bank, X=normal_f32(g, (n_tok, k)),
                 ids=moe_ids(g, n_tok, topk, n_experts), bias=None, residual=None)
+
+
+def workload_quant_prefill(seed=6, wtype=WTYPE_Q4_0, n=512, m=14336, k=4096):
+    """A prompt of n tokens through one quantised projection on the tensor cores
+    (the large-n row after the five workloads): X ~ N(0,1), GGML weights as above."""
+    g = rng(seed * 10 + wtype)
+    tag = "q4_0" if wtype == WTYPE_Q4_0 else "q8_0"
+    return dict(name=f"{tag}_tc_prefill_n{n}_m{m}_k{k}", kind="gemm_tc", wtype=wtype, n=n, m=m,
+                k=k, flags=0, W=draw_weights(g, wtype, m, k), X=normal_f32(g, (n, k)),
+                bias=None, residual=None)

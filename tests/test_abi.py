@@ -86,7 +86,10 @@ def test_workspace_sizes_and_errors(lib):
     assert wq.wq_gemm_workspace_bytes(1500, 3072, 1000, wq.WQ_BF16, TC) == 3_000_064  # -> 256
     assert wq.wq_gemm_workspace_bytes(16, 3072, 1024, wq.WQ_BF16, TC) == 0   # GEMV route
     assert wq.wq_gemm_workspace_bytes(1500, 3072, 1024, wq.WQ_BF16, 0) == 0  # f32-FMA route
-    assert wq.wq_gemm_workspace_bytes(1500, 3072, 1024, wq.WQ_Q8_0, TC) == 0
+    # quantised W on the tensor cores: bf16 X, then bf16 W, each rounded up to 256 bytes
+    assert wq.wq_gemm_workspace_bytes(1500, 3072, 1024, wq.WQ_Q8_0, TC) == 3_072_000 + 6_291_456
+    assert wq.wq_gemm_workspace_bytes(1500, 100, 1024, wq.WQ_Q4_0, TC) == 3_072_000 + 204_800
+    assert wq.wq_gemm_workspace_bytes(16, 3072, 1024, wq.WQ_Q4_0, TC) == 0   # GEMV route
     need = wq.wq_gemm_workspace_bytes(32, 64, 64, wq.WQ_BF16, TC)
     call = lambda ws, nb: wq.wq_gemm_ws(32, 64, 64, wq.WQ_BF16, TC, A, A, None, None, A, ws, nb, 0)
     assert call(None, need) == wq.WQ_ERR_INVALID_ARG          # missing

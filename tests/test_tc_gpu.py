@@ -169,3 +169,52 @@ def test_tc_wait_limit_expires_without_hang(oracle_mod, ws):
     status_ok()
     Yref, S = oracle_mod.gemm(n, m, k, BF16, 0, X, img, round_x=True, rows=(0, 64))
     assert_within(Y.cpu().numpy().reshape(n, m)[:, :64], Yref[:, :64], S[:, :64], tau_exact(k))
+
+
+# ----------------------------------------------- quantised W on the tensor cores --
+
+def run_tcq(n, m, k, wtype, flags, X, img, bias=None, R=None):
+    Y = Guarded(n * m)
+    need = wq.wq_gemm_workspace_bytes(n, m, k, wtype, flags | TC)
+    assert need >= 2 * n * k + 2 * m * k
+    work = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = wq.wq_gemm_ws(n, m, k, wtype, flags | TC, dev(X), weights_dev(img, wtype, m, k),
+                       dev(bias) if bias is not None else None,
+                       dev(R) if R is not None else None, Y.view, work, need)
+    wq.check(st, "wq_gemm_ws(TC, quantised)")
+    torch.cuda.synchronize()
+    status_ok()
+    return Y.result().reshape(n, m)
+
+
+@pytest.mark.parametrize("wtype", [wq.WQ_Q8_0, wq.WQ_Q4_0])
+@pytest.mark.parametrize("shape,flags", [((17, 32, 32), 0), ((130, 256, 128), BIAS),
+                                         ((300, 520, 1056), BIAS | GELU), ((257, 300, 224), RES),
+                                         ((1500, 1024, 1024), BIAS | RES)])
+def test_tc_quantised_weights(oracle_mod, wtype, shape, flags):
+    """X and the dequantised W both rounded to bf16: within 8e-3 sum|x||w| of the exact
+    result, and within the accumulation bound of the oracle fed the same roundings."""
+    n, m, k = shape
+    g = synth.rng(n * 7 + m + wtype)
+    X = synth.normal_f32(g, (n, k))
+    img = synth.draw_weights(g, wtype, m, k)
+    bias = synth.normal_f32(g, (m,), 0.1) if flags & BIAS else None
+    R = synth.normal_f32(g, (n, m)) if flags & RES else None
+    Y = run_tcq(n, m, k, wtype, flags, X, img, bias, R)
+    rows = (0, m) if m <= 520 else (m // 2 - 32, m // 2 + 32)
+    j0, j1 = rows
+    for rnd, tau in ((False, TAU_TC), (True, tau_exact(k))):
+        Yref, S = oracle_mod.gemm(n, m, k, wtype, flags, X, img, bias=bias, residual=R,
+                                  round_x=rnd, round_w=rnd, rows=rows)
+        assert_within(Y[:, j0:j1], Yref[:, j0:j1], S[:, j0:j1], tau, gelu=bool(flags & GELU),
+                      bias=None if bias is None else bias[j0:j1],
+                      R=None if R is None else R[:, j0:j1],
+                      what=f"tc quantised wtype={wtype} {shape} flags={flags} rounded={rnd}")
+
+
+def test_tc_quantised_needs_workspace_entry_point():
+    n, m, k = 64, 64, 64
+    Xd = torch.zeros(n * k, device="cuda")
+    Wd = torch.zeros(wq.wq_weight_bytes(wq.WQ_Q8_0, m, k), dtype=torch.uint8, device="cuda")
+    Y = torch.zeros(n * m, device="cuda")
+    assert wq.wq_gemm(n, m, k, wq.WQ_Q8_0, TC, Xd, Wd, None, None, Y) == wq.WQ_ERR_UNSUPPORTED
