@@ -34,7 +34,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_ranks_take_the_max_step_time():
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
         assert dict(out) == {0: 2.5, 1: 2.5}
