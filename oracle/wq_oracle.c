@@ -25,6 +25,10 @@
  *     0.5*v*(1+erf(v/sqrt 2)); flag 4 adds the old Y[r][c]; in that order.
  *     The oracle takes erf exactly (C99 erf in f64); the page's kernel uses the
  *     Abramowitz-Stegun 7.1.26 rational approximation of it.
+ *   - more activations: wavo 0.3.0 src/gpu/mod.rs, enum Epilogue and its test
+ *     reference epilogue(): Silu v/(1+exp(-v)), Relu max(v, 0), Tanh tanh(v); here
+ *     flags 8, 16, 32, in the activation's place (after bias, before residual);
+ *     at most one activation per call.
  *   - MoE: hanzo-ml 0.11.13, moe_matvec_gpu: y[s, r] = sum_k W[ids[s], r, k] x[s, k]
  *     over one bank [E][rows][k]; here x is per token and slot (t, s) reads
  *     token t's row, output [t][s][m].
@@ -41,7 +45,8 @@
 #endif
 
 enum { O_BF16 = 0, O_Q8_0 = 1, O_Q4_0 = 2 };
-enum { O_BIAS = 1u, O_GELU = 2u, O_RESIDUAL = 4u };
+enum { O_BIAS = 1u, O_GELU = 2u, O_RESIDUAL = 4u, O_SILU = 8u, O_RELU = 16u, O_TANH = 32u };
+#define O_ACTS (O_GELU | O_SILU | O_RELU | O_TANH)
 
 /* IEEE 754 binary16 -> f64, from its bit fields (1 sign, 5 exponent, 10 fraction). */
 double oracle_half_to_f64(uint16_t h) {
@@ -154,7 +159,11 @@ static void dot_epi(int k, unsigned flags, int round_x, const float *x, const do
     }
     double v = acc;
     if (flags & O_BIAS) v += (double)*bias_j;
+    /* the activation: at most one of wavo's Epilogue::{Gelu, Silu, Relu, Tanh} */
     if (flags & O_GELU) v = oracle_gelu(v);
+    else if (flags & O_SILU) v = v / (1.0 + exp(-v));
+    else if (flags & O_RELU) v = v > 0.0 ? v : 0.0;
+    else if (flags & O_TANH) v = tanh(v);
     if (flags & O_RESIDUAL) v += (double)*res_ij;
     *y = v;
     if (s) *s = bound;
@@ -182,6 +191,7 @@ int oracle_gemm(int n, int m, int k, int wtype, unsigned flags, int round,
                 const float *X, const uint8_t *W, const float *bias, const float *R,
                 double *Y, double *S, int j0, int j1, int threads) {
     if (n < 0 || !shape_ok(wtype, m, k) || j0 < 0 || j1 > m || j0 > j1) return -1;
+    if (__builtin_popcount(flags & O_ACTS) > 1) return -1;
     if (((flags & O_BIAS) && !bias) || ((flags & O_RESIDUAL) && !R)) return -1;
     size_t rb = row_bytes(wtype, k);
     int nt = set_threads(threads);
@@ -223,6 +233,7 @@ int oracle_moe(int n_tok, int topk, int n_experts, int m, int k, int wtype, unsi
     if (n_tok < 0 || topk <= 0 || n_experts <= 0 || !shape_ok(wtype, m, k)) return -1;
     if (q0 < 0 || q1 > n_tok * topk || q0 > q1) return -1;
     if (((flags & O_BIAS) && !bias) || ((flags & O_RESIDUAL) && !R)) return -1;
+    if (__builtin_popcount(flags & O_ACTS) > 1) return -1;
     for (int q = q0; q < q1; ++q)
         if (ids[q] < 0 || ids[q] >= n_experts) return -2;
     size_t rb = row_bytes(wtype, k);

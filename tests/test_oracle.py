@@ -317,6 +317,54 @@ def test_round_w_equals_bf16_rounded_dequantised_image(oracle_mod):
     assert (Ya == Yb).all()
 
 
+SILU, RELU, TANH = 8, 16, 32
+
+
+@pytest.mark.parametrize("flag,x,want", [
+    (SILU, 0.0, 0.0),
+    (SILU, float(np.float32(np.log(3.0))), None),   # sigma(ln 3) = 3/4: checked below
+    (RELU, -3.0, 0.0), (RELU, 2.5, 2.5), (RELU, 0.0, 0.0),
+    (TANH, 0.0, 0.0),
+    (TANH, float(np.float32(np.log(2.0))), None),   # tanh(ln 2) = 3/5: checked below
+])
+def test_activation_closed_forms(oracle_mod, flag, x, want):
+    """wavo's Silu / Relu / Tanh epilogues through a one-hot GEMM (Y = act(x))."""
+    k = 32
+    img = synth.bf16_pairs(np.where(np.arange(k) == 0, 0x3F80, 0).astype(np.uint16)[None, :])
+    X = np.zeros((1, k), np.float32)
+    X[0, 0] = x
+    Y, _ = oracle_mod.gemm(1, 1, k, BF16, flag, X, img)
+    if want is not None:
+        assert Y[0, 0] == want
+    elif flag == SILU:  # x = f32(ln 3): x * 3/4 up to the f32 rounding of ln 3
+        assert abs(Y[0, 0] - 0.75 * np.log(3.0)) < 1e-7
+    else:               # tanh(f32(ln 2)) = 0.6 up to that rounding
+        assert abs(Y[0, 0] - 0.6) < 1e-7
+
+
+@pytest.mark.parametrize("flag", [SILU, TANH])
+def test_activation_symmetries(oracle_mod, flag):
+    """silu(x) - silu(-x) = x (sigma(x) + sigma(-x) = 1); tanh is odd."""
+    k = 32
+    img = synth.bf16_pairs(np.where(np.arange(k) == 0, 0x3F80, 0).astype(np.uint16)[None, :])
+    for x in (0.3, 1.7, 6.0):
+        X = np.zeros((2, k), np.float32)
+        X[0, 0], X[1, 0] = x, -x
+        Y, _ = oracle_mod.gemm(2, 1, k, BF16, flag, X, img)
+        if flag == SILU:
+            assert abs((Y[0, 0] - Y[1, 0]) - np.float32(x)) < 1e-15
+        else:
+            assert Y[0, 0] == -Y[1, 0]
+
+
+def test_one_activation_per_call(oracle_mod):
+    img = np.zeros((1, 64), np.uint8)
+    X = np.zeros((1, 32), np.float32)
+    for flags in (2 | 8, 8 | 16, 16 | 32, 2 | 32):
+        with pytest.raises(ValueError):
+            oracle_mod.gemm(1, 1, 32, BF16, flags, X, img)
+
+
 def test_bad_arguments(oracle_mod):
     img = np.zeros((2, 34), np.uint8)
     with pytest.raises(ValueError):
