@@ -224,13 +224,12 @@ __global__ void __launch_bounds__(Roles<ATMA>::kThreads, 1)
                 float v[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
                 const int jb = j0 + c0;
-                if (a.flags & (kBias | kGelu)) {
+                if (a.flags & (kBias | kActs)) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         float t = v[c];
                         if (a.flags & kBias) t += (jb + c < a.m) ? __ldg(a.bias + jb + c) : 0.f;
-                        if (a.flags & kGelu) t = gelu_erf(t);
-                        v[c] = t;
+                        v[c] = activate(t, a.flags);
                     }
                 }
                 // Row `lane` of the 32x32 block into shared memory...

@@ -213,8 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float bc = __shfl_sync(0xFFFFFFFFu, bl, c);
                     float x = v[c];
                     if (a.flags & kBias) x += bc;
-                    if (a.flags & kGelu) x = gelu_erf(x);
-                    v[c] = x;
+                    v[c] = activate(x, a.flags);
                 }
                 if (a.flags & kResidual) {
                     bool w = mbar_wait(&rbar[ew], rphase, limit);

@@ -40,7 +40,9 @@ bool shape_ok(int wtype, int m, int k) {
 wq_status check_common(int n, int m, int k, int wtype, unsigned flags, const float *X,
                        const void *W, const float *bias, const float *residual, const float *Y) {
     if (n <= 0 || !shape_ok(wtype, m, k)) return WQ_ERR_INVALID_ARG;
-    if (flags & ~(unsigned)(WQ_BIAS | WQ_GELU | WQ_RESIDUAL | WQ_TC_BF16)) return WQ_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(WQ_EPILOGUE_FLAGS | WQ_TC_BF16)) return WQ_ERR_INVALID_ARG;
+    const unsigned acts = flags & (WQ_GELU | WQ_SILU | WQ_RELU | WQ_TANH);
+    if (acts & (acts - 1)) return WQ_ERR_INVALID_ARG;  // more than one activation
     if (!X || !W || !Y) return WQ_ERR_INVALID_ARG;
     if ((flags & WQ_BIAS) && !bias) return WQ_ERR_INVALID_ARG;
     if ((flags & WQ_RESIDUAL) && !residual) return WQ_ERR_INVALID_ARG;
@@ -104,7 +106,7 @@ static wq_status gemv_impl(int n, int m, int k, int wtype, unsigned flags, const
     a.n = n;
     a.m = m;
     a.k = k;
-    a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
+    a.flags = flags & WQ_EPILOGUE_FLAGS;
     a.status = dev->status;
     a.wait_limit = wait_limit();
     if (mma_gemv_supported(wtype, k))
@@ -139,7 +141,7 @@ wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X
     a.n = n;
     a.m = m;
     a.k = k;
-    a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
+    a.flags = flags & WQ_EPILOGUE_FLAGS;
     a.status = dev->status;
     a.wait_limit = wait_limit();
     if (flags & WQ_TC_BF16) return cuda_status(launch_gemm_tc(a, *dev, (cudaStream_t)stream));
@@ -174,7 +176,7 @@ wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float
     a.n = n;
     a.m = m;
     a.k = k;
-    a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
+    a.flags = flags & WQ_EPILOGUE_FLAGS;
     a.status = dev->status;
     a.wait_limit = wait_limit();
     return cuda_status(launch_gemm_tc_ws(a, wtype, workspace, *dev, (cudaStream_t)stream));
@@ -201,7 +203,7 @@ wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtyp
     a.n = n_tok;
     a.m = m;
     a.k = k;
-    a.flags = flags & (WQ_BIAS | WQ_GELU | WQ_RESIDUAL);
+    a.flags = flags & WQ_EPILOGUE_FLAGS;
     a.topk = topk;
     a.n_experts = n_experts;
     a.status = dev->status;

@@ -18,7 +18,8 @@
 namespace wq {
 
 enum WType : int { kBF16 = 0, kQ8_0 = 1, kQ4_0 = 2 };
-enum Flag : unsigned { kBias = 1u, kGelu = 2u, kResidual = 4u };
+enum Flag : unsigned { kBias = 1u, kGelu = 2u, kResidual = 4u, kSilu = 8u, kRelu = 16u, kTanh = 32u };
+constexpr unsigned kActs = kGelu | kSilu | kRelu | kTanh;  // at most one per call
 enum DevStatus : unsigned { kStTimeout = 4u, kStBadExpert = 5u };
 
 // Bytes of one row of k weights in each format.
@@ -73,12 +74,22 @@ __device__ __forceinline__ float gelu_erf(float v) {
     return 0.5f * v * (1.0f + erff(v * 0.70710678118654752440f));
 }
 
+// The activation of the epilogue (wavo 0.3.0 src/gpu/mod.rs, enum Epilogue: Gelu,
+// Silu v/(1+exp(-v)), Relu max(v, 0), Tanh); none when no activation flag is set.
+__device__ __forceinline__ float activate(float v, unsigned flags) {
+    if (!(flags & kActs)) return v;
+    if (flags & kGelu) return gelu_erf(v);
+    if (flags & kSilu) return v / (1.0f + expf(-v));
+    if (flags & kRelu) return fmaxf(v, 0.0f);
+    return tanhf(v);
+}
+
 // acc -> Y value.  `res` is read only with kResidual.
 __device__ __forceinline__ float epilogue(float acc, unsigned flags, const float *bias_j,
                                           const float *res_ij) {
     float v = acc;
     if (flags & kBias) v += __ldg(bias_j);
-    if (flags & kGelu) v = gelu_erf(v);
+    v = activate(v, flags);
     if (flags & kResidual) v += *res_ij;  // may alias Y: plain load
     return v;
 }
@@ -89,7 +100,7 @@ __device__ __forceinline__ float epilogue_vals(float acc, unsigned flags, float 
                                                float res_ij) {
     float v = acc;
     if (flags & kBias) v += bias_j;
-    if (flags & kGelu) v = gelu_erf(v);
+    v = activate(v, flags);
     if (flags & kResidual) v += res_ij;
     return v;
 }

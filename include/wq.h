@@ -78,11 +78,19 @@ typedef enum {
 
 /* Epilogue flags, the bit values and order of cortiq-engine's ae_put:
  * v = acc; if BIAS v += bias[j]; if GELU v = 0.5 v (1 + erf(v / sqrt 2));
- * if RESIDUAL v += residual[i][j]; Y[i][j] = v. */
+ * if RESIDUAL v += residual[i][j]; Y[i][j] = v.
+ * SILU, RELU and TANH are wavo 0.3.0's other Epilogue activations (src/gpu/mod.rs,
+ * enum Epilogue): v / (1 + exp(-v)), max(v, 0), tanh(v), in GELU's place.  At
+ * most one of GELU, SILU, RELU, TANH per call (else WQ_ERR_INVALID_ARG); wavo's
+ * GeluResidual is GELU | RESIDUAL. */
 enum {
     WQ_BIAS = 1u,
     WQ_GELU = 2u,
     WQ_RESIDUAL = 4u,
+    WQ_SILU = 8u,
+    WQ_RELU = 16u,
+    WQ_TANH = 32u,
+    WQ_EPILOGUE_FLAGS = 63u,
     /* n > WQ_GEMV_MAX_N only: run the contraction on the tcgen05 tensor cores with
      * X rounded to bf16 (round to nearest even) and f32 accumulation; quantised
      * weights are dequantised and rounded to bf16 the same way (wq_gemm_ws and

@@ -59,7 +59,10 @@ A = 0x10000  # a 16-byte aligned fake device address: never dereferenced below
     lambda: wq.wq_gemm(1, 8, 36, wq.WQ_Q4_0, 0, A, A, None, None, A, 0),
     lambda: wq.wq_gemm(1, 8, 12, wq.WQ_BF16, 0, A, A, None, None, A, 0),
     lambda: wq.wq_gemm(1, 8, 32, 3, 0, A, A, None, None, A, 0),
-    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 8, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 64, A, A, None, None, A, 0),      # unknown flag
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, wq.WQ_GELU | wq.WQ_SILU, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, wq.WQ_RELU | wq.WQ_TANH, A, A, None, None, A, 0),
+    lambda: wq.wq_gemv(1, 8, 32, wq.WQ_Q8_0, wq.WQ_SILU | wq.WQ_TANH, A, A, None, None, A, 0),
     lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 0, None, A, None, None, A, 0),
     lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 0, A, None, None, None, A, 0),
     lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 0, A, A, None, None, None, 0),

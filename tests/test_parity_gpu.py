@@ -120,6 +120,39 @@ def test_gemv_epilogues(oracle_mod, wtype, flags):
     check_against_oracle(oracle_mod, wq.wq_gemv, wtype, 3, 261, 2048, flags, seed=flags)
 
 
+ACTS = [wq.WQ_SILU, wq.WQ_RELU, wq.WQ_TANH]
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "relu", "tanh"])
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("fn,n,k", [(wq.wq_gemv, 3, 512), (wq.wq_gemv, 2, 96),
+                                    (wq.wq_gemm, 40, 256)], ids=["gemv-mma", "gemv-ragged", "simt"])
+def test_wavo_activations(oracle_mod, act, wtype, fn, n, k):
+    """wavo's Silu / Relu / Tanh epilogues, with bias and residual (bias, act, residual)."""
+    m = 130
+    X, img, bias, R = case(act + n + wtype, wtype, n, m, k, BIAS | RES)
+    Y = run_gemm(fn, n, m, k, wtype, BIAS | RES | act, X, img, bias, R)
+    Yref, S = oracle_mod.gemm(n, m, k, wtype, BIAS | RES | act, X, img, bias=bias, residual=R)
+    assert_within(Y, Yref, S, TAU, gelu=True, bias=bias, R=R,
+                  what=f"{fn.__name__} act={act} wtype={wtype} n={n} k={k}")
+
+
+@pytest.mark.parametrize("act", ACTS, ids=["silu", "relu", "tanh"])
+def test_moe_activations(oracle_mod, act):
+    nt, tk, E, m, k = 5, 3, 9, 70, 512
+    g = synth.rng(act)
+    X = synth.normal_f32(g, (nt, k))
+    img = synth.draw_weights(g, Q4_0, E * m, k)
+    ids = synth.moe_ids(g, nt, tk, E)
+    Y = Guarded(nt * tk * m)
+    wq.check(wq.wq_moe_gemv(nt, tk, E, m, k, Q4_0, act, dev(X), weights_dev(img, Q4_0, E * m, k),
+                            dev(ids), None, None, Y.view), "moe")
+    torch.cuda.synchronize()
+    status_ok()
+    Yref, S = oracle_mod.moe(nt, tk, E, m, k, Q4_0, act, X, img, ids)
+    assert_within(Y.result(), Yref, S, TAU, gelu=True, what=f"moe act={act}")
+
+
 @pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
 def test_gemv_residual_in_place(oracle_mod, wtype):
     check_against_oracle(oracle_mod, wq.wq_gemv, wtype, 4, 190, 1024, BIAS | GELU | RES,

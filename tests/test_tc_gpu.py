@@ -67,7 +67,7 @@ def check_tc(oracle_mod, n, m, k, flags, seed, rows=None, inplace=False, std=0.0
     R = synth.normal_f32(g, (n, m)) if flags & RES else None
     Y = run_tc(n, m, k, flags, X, img, bias, R, inplace=inplace, ws=ws)
     j0, j1 = rows if rows else (0, m)
-    gelu = bool(flags & GELU)
+    gelu = bool(flags & (GELU | wq.WQ_SILU | wq.WQ_RELU | wq.WQ_TANH))
     for round_x, tau in ((False, TAU_TC), (True, tau_exact(k))):
         Yref, S = oracle_mod.gemm(n, m, k, BF16, flags, X, img, bias=bias, residual=R,
                                   round_x=round_x, rows=(j0, j1))
@@ -87,7 +87,8 @@ def test_tc_shapes(oracle_mod, shape, ws):
 
 
 @pytest.mark.parametrize("ws", [False, True], ids=["fused", "workspace"])
-@pytest.mark.parametrize("flags", [0, BIAS, GELU, BIAS | GELU, RES, BIAS | RES, BIAS | GELU | RES])
+@pytest.mark.parametrize("flags", [0, BIAS, GELU, BIAS | GELU, RES, BIAS | RES, BIAS | GELU | RES,
+                                   BIAS | wq.WQ_SILU, BIAS | wq.WQ_RELU | RES, wq.WQ_TANH | RES])
 def test_tc_epilogues(oracle_mod, flags, ws):
     check_tc(oracle_mod, 200, 384, 320, flags, seed=flags, ws=ws)
 
