@@ -10,8 +10,12 @@
 //     column block t / RB, so CTAs running together share W columns in L2);
 //   * TMEM holds two accumulators: the MMA warp fills one tile's accumulator
 //     while the epilogue warps drain the other, so output writes overlap MMAs;
-//   * warp 0 streams A (X bf16) and B (W) tiles by TMA through a 3-4 stage ring
-//     across tile boundaries; warp 1 issues tcgen05.mma (M=128, N=BN, K=16);
+//   * warps 0 and 1 stream A (X bf16) and B (W) tiles by TMA through a stage
+//     ring across tile boundaries, each warp its own operand (a TMA issue holds
+//     its thread for a while, so two issuers keep more bytes in flight); a stage
+//     spans KS 128-byte swizzle atoms of k (64 bf16 each), since the bytes the
+//     TMA unit of one SM delivers per stage grow with the stage size;
+//   * warp 2 issues tcgen05.mma (M=128, N=BN, K=16);
 //   * 16 epilogue warps (4 per TMEM lane quarter) take 32x32 blocks: tcgen05.ld,
 //     bias (one coalesced load per block, broadcast by shuffles) and erf-GELU in
 //     registers, the block into a 128-byte-swizzled shared buffer, residual added
@@ -34,14 +38,18 @@ namespace {
 using namespace tc;
 
 constexpr int kEpi = 16;                       // epilogue warps
-constexpr int kThreads = (2 + kEpi) * 32;
-constexpr int kABytes = BM * BK * 2;           // 16 KB
+constexpr int kRoles = 3;                      // A producer, B producer, MMA issuer
+constexpr int kThreads = (kRoles + kEpi) * 32;
+constexpr int kAtomA = BM * BK * 2;            // one 128-row swizzle atom of A: 16 KB
 constexpr int kStgBytes = 32 * 32 * 4;         // one 32x32 f32 block
 
-template <int BN>
+template <int BN, int KS>
 struct PLayout {
-    static constexpr int kBBytes = BN * BK * 2;
-    static constexpr int kStages = BN == 256 ? 3 : 4;
+    static constexpr int kABytes = KS * kAtomA;            // A of a stage
+    static constexpr int kBBytes = KS * BN * BK * 2;       // B of a stage
+    static constexpr int kFit = (216 * 1024 - kEpi * kStgBytes) / (kABytes + kBBytes);
+    static constexpr int kStages = kFit > 6 ? 6 : kFit;
+    static_assert(kStages >= 2, "at least two stages");
     static constexpr size_t kA = 0;
     static constexpr size_t kB = kA + (size_t)kStages * kABytes;
     static constexpr size_t kStg = kB + (size_t)kStages * kBBytes;
@@ -52,14 +60,14 @@ struct PLayout {
     static constexpr size_t kBytes = kMisc + 16 + 1024;
 };
 
-template <int BN>
+template <int BN, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcp_kernel(const __grid_constant__ CUtensorMap wmap,
                     const __grid_constant__ CUtensorMap xmap,
                     const __grid_constant__ CUtensorMap ymap,
                     const __grid_constant__ CUtensorMap rmap, const GemmArgs a) {
     pdl_enter();
-    using L = PLayout<BN>;
+    using L = PLayout<BN, KS>;
     constexpr int S = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -79,12 +87,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int RB = (a.n + BM - 1) / BM, CB = (a.m + BN - 1) / BN;
     const int tiles = RB * CB;
-    const int KB = (a.k + BK - 1) / BK;
+    const int KB = (a.k + KS * BK - 1) / (KS * BK);  // stages per tile
     const uint64_t limit = a.wait_limit;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);  // one expect_tx arrival per producer
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -96,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (warp == 1) {  // TMEM: two accumulators of BN f32 columns x 128 lanes
+    if (warp == 2) {  // TMEM: two accumulators of BN f32 columns x 128 lanes
         asm volatile(
             "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                 smem_addr(tmem_slot)),
@@ -109,13 +117,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- producer
+    if (warp < 2) {
+        // --------------------------------------------------------- producers
+        // Warp 0 loads A (X rows), warp 1 loads B (W rows); KS atoms per stage.
         if (lane == 0) {
-            long long q = 0;  // stage loads issued
+            const bool isA = warp == 0;
+            const CUtensorMap *map = isA ? &xmap : &wmap;
+            const int atom = isA ? kAtomA : BN * BK * 2;
+            uint8_t *base = isA ? sA : sB;
+            const int sbytes = isA ? L::kABytes : L::kBBytes;
+            long long q = 0;  // stages issued
             bool ok = true;
             for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                const int i0 = (t % RB) * BM, j0 = (t / RB) * BN;
+                const int y = isA ? (t % RB) * BM : (t / RB) * BN;
                 for (int kb = 0; kb < KB; ++kb, ++q) {
                     const int s = (int)(q % S);
                     if (q >= S && !wait_or_abort(&empty[s], (uint32_t)(((q / S) - 1) & 1),
@@ -123,15 +137,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(kABytes + L::kBBytes));
-                    tma_load_2d(sA + (size_t)s * kABytes, &xmap, kb * BK, i0, &full[s]);
-                    tma_load_2d(sB + (size_t)s * L::kBBytes, &wmap, kb * BK, j0, &full[s]);
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)sbytes);
+                    uint8_t *dst = base + (size_t)s * sbytes;
+#pragma unroll
+                    for (int u = 0; u < KS; ++u)
+                        tma_load_2d(dst + u * atom, map, (kb * KS + u) * BK, y, &full[s]);
                 }
             }
             for (long long d = (q > S ? q - S : 0); d < q; ++d)
                 mbar_wait(&full[d % S], (uint32_t)((d / S) & 1), kDrainPolls);
         }
-    } else if (warp == 1) {
+    } else if (warp == 2) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16(BM, BN);
@@ -155,12 +171,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_addr(sA + (size_t)s * kABytes);
+                    const uint32_t a0 = smem_addr(sA + (size_t)s * L::kABytes);
                     const uint32_t b0 = smem_addr(sB + (size_t)s * L::kBBytes);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        tc_mma(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32),
-                               idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    for (int u = 0; u < KS; ++u)
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            tc_mma(d, smem_desc_sw128(a0 + u * kAtomA + kk * 32),
+                                   smem_desc_sw128(b0 + u * (BN * BK * 2) + kk * 32), idesc,
+                                   (kb > 0 || u > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(&empty[s]);
                 }
                 if (ok) tc_commit(&tfull[b]);
@@ -172,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------- epilogue
-        const int ew = warp - 2;                   // 0..15
+        const int ew = warp - kRoles;              // 0..15
         const int q = warp & 3;                    // TMEM lane quarter of this warp
         constexpr int CW = BN / (kEpi / 4);        // columns per warp per tile
         const int cg = ew >> 2;                    // which column group
@@ -257,9 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) bulk_wait0();
         __syncwarp();
     }
+    __syncwarp();  // every role's lanes meet before the block-wide barrier
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 2) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(2 * BN)
@@ -295,9 +315,10 @@ bool encode_2d(CUtensorMap &map, CUtensorMapDataType dt, int esize, const void *
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, int KS>
 cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
                       cudaStream_t stream) {
+    using L = PLayout<BN, KS>;
     static std::atomic<unsigned long long> smem_set{0};
     CUtensorMap wmap, xmap, ymap, rmap;
     if (!encode_2d(wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W, a.k, a.m, BK, BN) ||
@@ -310,14 +331,15 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
     } else {
         rmap = ymap;  // unused
     }
-    auto kern = gemm_tcp_kernel<BN>;
-    cudaError_t err = ensure_smem(kern, (int)PLayout<BN>::kBytes, dev, smem_set);
+    auto kern = gemm_tcp_kernel<BN, KS>;
+    static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
+    cudaError_t err = ensure_smem(kern, (int)L::kBytes, dev, smem_set);
     if (err != cudaSuccess) return err;
     const long long tiles =
         (long long)((a.n + BM - 1) / BM) * ((a.m + BN - 1) / BN);
     const int grid = (int)(tiles < dev.sm_count ? tiles : dev.sm_count);
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), PLayout<BN>::kBytes, stream, wmap, xmap,
-                      ymap, rmap, a);
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, stream, wmap, xmap, ymap,
+                      rmap, a);
 }
 
 }  // namespace
@@ -335,8 +357,8 @@ cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo 
     const long long rows = (a.n + BM - 1) / BM;
     const long long w256 = (rows * ((a.m + 255) / 256) + dev.sm_count - 1) / dev.sm_count;
     const long long w128 = (rows * ((a.m + 127) / 128) + dev.sm_count - 1) / dev.sm_count;
-    if (w256 * 2 <= w128) return launch_bn<256>(a, xb, dev, stream);
-    return launch_bn<128>(a, xb, dev, stream);
+    if (w256 * 2 <= w128) return launch_bn<256, 1>(a, xb, dev, stream);
+    return launch_bn<128, 2>(a, xb, dev, stream);
 }
 
 }  // namespace wq
