@@ -70,6 +70,8 @@ def _load():
             lib.oracle_moe.argtypes = [ci, ci, ci, ci, ci, ci, cu, vp, vp, vp, vp, vp, vp, vp,
                                        ci, ci, ci]
             lib.oracle_moe.restype = ci
+            lib.oracle_layer_norm.argtypes = [ci, ci, vp, vp, vp]
+            lib.oracle_layer_norm.restype = ci
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ci
             _lib = lib
@@ -102,6 +104,17 @@ def round_bf16(x: float) -> float:
 
 def gelu(v: float) -> float:
     return float(_load().oracle_gelu(float(v)))
+
+
+def layer_norm(X: np.ndarray, gb: np.ndarray) -> np.ndarray:
+    """f64 row LayerNorm of f32 X [n][k] with gb = [gamma (k) | beta (k)], eps 1e-5."""
+    Xc, gc = _c(X, np.float32), _c(gb, np.float32)
+    n, k = Xc.shape
+    assert gc.size == 2 * k
+    Y = np.empty((n, k), dtype=np.float64)
+    if _load().oracle_layer_norm(n, k, _ptr(Xc), _ptr(gc), _ptr(Y)) != 0:
+        raise ValueError("oracle_layer_norm: bad arguments")
+    return Y
 
 
 def dequant(wtype: int, m: int, k: int, W: np.ndarray) -> np.ndarray:

@@ -265,3 +265,25 @@ int oracle_moe(int n_tok, int topk, int n_experts, int m, int k, int wtype, unsi
 }
 
 int oracle_max_threads(void) { return set_threads(0); }
+
+/*
+ * Row LayerNorm, cortiq-engine 0.8.49 src/gpu_wgpu/nemotron_audio.rs, kernel ae_ln
+ * (and wavo 0.3.0's test reference layer_norm): for each row of X f32 [n][k],
+ * mean = sum x / k, var = sum (x - mean)^2 / k (two passes), and
+ * Y = (x - mean) / sqrt(var + 1e-5) * g + b, in f64.  gb = [g (k) | b (k)].
+ */
+int oracle_layer_norm(int n, int k, const float *X, const float *gb, double *Y) {
+    if (n < 0 || k <= 0 || !X || !gb || !Y) return -1;
+    for (int i = 0; i < n; ++i) {
+        const float *x = X + (size_t)i * k;
+        double mean = 0.0, var = 0.0;
+        for (int t = 0; t < k; ++t) mean += (double)x[t];
+        mean /= k;
+        for (int t = 0; t < k; ++t) var += ((double)x[t] - mean) * ((double)x[t] - mean);
+        var /= k;
+        const double rstd = 1.0 / sqrt(var + 1e-5);
+        for (int t = 0; t < k; ++t)
+            Y[(size_t)i * k + t] = ((double)x[t] - mean) * rstd * (double)gb[t] + (double)gb[k + t];
+    }
+    return 0;
+}

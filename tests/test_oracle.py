@@ -365,6 +365,37 @@ def test_one_activation_per_call(oracle_mod):
             oracle_mod.gemm(1, 1, 32, BF16, flags, X, img)
 
 
+def test_layer_norm_closed_forms(oracle_mod):
+    """cortiq-engine ae_ln: (x - mean) / sqrt(var + 1e-5) * g + b, biased variance."""
+    k = 4
+    gb = np.array([1, 1, 1, 1, 0, 0, 0, 0], np.float32)
+    X = np.array([[1, 3, 1, 3],          # mean 2, var 1
+                  [5, 5, 5, 5],          # constant row: var 0 -> 0 (then + b)
+                  [0, 0, 0, 8]], np.float32)  # mean 2, var (3*4 + 36)/4 = 12
+    Y = oracle_mod.layer_norm(X, gb)
+    r1 = 1.0 / np.sqrt(1.0 + 1e-5)
+    assert np.array_equal(Y[0], np.array([-r1, r1, -r1, r1]))
+    assert np.array_equal(Y[1], np.zeros(4))
+    r3 = 1.0 / np.sqrt(12.0 + 1e-5)
+    assert np.allclose(Y[2], np.array([-2, -2, -2, 6]) * r3, rtol=1e-15, atol=0)
+    # gamma scales, beta shifts, per column
+    gb2 = np.array([2, -1, 0.5, 1, 10, 20, 30, 40], np.float32)
+    Y2 = oracle_mod.layer_norm(X[:1], gb2)
+    assert np.array_equal(Y2[0], np.array([-2 * r1 + 10, -r1 + 20, -0.5 * r1 + 30, r1 + 40]))
+
+
+def test_layer_norm_invariants(oracle_mod):
+    """Unit gamma, zero beta: every row has mean 0 and variance var/(var + eps)."""
+    g = synth.rng(8)
+    X = synth.normal_f32(g, (5, 1000), 3.0) + np.float32(7.0)
+    gb = np.concatenate([np.ones(1000, np.float32), np.zeros(1000, np.float32)])
+    Y = oracle_mod.layer_norm(X, gb)
+    x = X.astype(np.float64)
+    var = x.var(axis=1)
+    assert np.allclose(Y.mean(axis=1), 0.0, atol=1e-12)
+    assert np.allclose((Y ** 2).mean(axis=1), var / (var + 1e-5), rtol=1e-12)
+
+
 def test_bad_arguments(oracle_mod):
     img = np.zeros((2, 34), np.uint8)
     with pytest.raises(ValueError):
