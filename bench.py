@@ -84,7 +84,8 @@ def extra_workloads():
     large-n tensor-core GEMM (a prompt through GGML weights)."""
     import synth
     return [synth.workload_quant_prefill(wtype=synth.WTYPE_Q4_0),
-            synth.workload_quant_prefill(wtype=synth.WTYPE_Q8_0)]
+            synth.workload_quant_prefill(wtype=synth.WTYPE_Q8_0),
+            synth.workload_ln_qkv()]
 
 
 def algorithmic(w):
@@ -110,6 +111,8 @@ def algorithmic(w):
 def kernels_per_call(w):
     """Kernels one call launches: the workspace tensor-core GEMM converts X (and a
     quantised W) to bf16 first; every other call is one launch."""
+    if w["kind"] == "gemm_ln_tc":
+        return 2  # LayerNorm into the workspace, then the GEMM
     if w["kind"] != "gemm_tc":
         return 1
     return 2 if w["wtype"] == 0 else 3  # quantised W is dequantised to bf16 first
@@ -336,6 +339,11 @@ class Launches:
                       if w["residual"] is not None else None)
             b["ids"] = torch.from_numpy(w["ids"]).to(device) if w["kind"] == "moe" else None
             b["ws"] = None
+            b["ln_gb"] = torch.from_numpy(w["ln_gb"]).to(device) if "ln_gb" in w else None
+            if w["kind"] == "gemm_ln_tc":
+                need = wq.wq_gemm_ln_workspace_bytes(w["n"], m, k, w["wtype"],
+                                                     w["flags"] | wq.WQ_TC_BF16)
+                b["ws"] = torch.empty(need, dtype=torch.uint8, device=device)
             if w["kind"] == "gemm_tc":
                 need = wq.wq_gemm_workspace_bytes(w["n"], m, k, w["wtype"],
                                                   w["flags"] | wq.WQ_TC_BF16)
@@ -349,6 +357,11 @@ class Launches:
             return wq.wq_moe_gemv(w["n_tok"], w["topk"], w["n_experts"], w["m"], w["k"],
                                   w["wtype"], w["flags"], b["X"], b["W"], b["ids"], b["bias"],
                                   b["R"], b["Y"], stream)
+        if w["kind"] == "gemm_ln_tc":
+            flags = w["flags"] | wq.WQ_TC_BF16
+            return wq.wq_gemm_ln_ws(w["n"], w["m"], w["k"], w["wtype"], flags, b["X"], b["ln_gb"],
+                                    b["W"], b["bias"], b["R"], b["Y"], b["ws"], b["ws"].numel(),
+                                    stream)
         if w["kind"] == "gemm_tc":
             flags = w["flags"] | wq.WQ_TC_BF16
             return wq.wq_gemm_ws(w["n"], w["m"], w["k"], w["wtype"], flags, b["X"], b["W"],

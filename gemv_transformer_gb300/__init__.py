@@ -27,7 +27,8 @@ WQ_GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20
 WQ_GEMV_MAX_N = 16
 WQ_MOE_MAX_SLOTS = 256
 
-EXPORTS = ("wq_gemm", "wq_gemm_ws", "wq_gemm_workspace_bytes", "wq_gemm_noalloc", "wq_gemv",
+EXPORTS = ("wq_gemm", "wq_gemm_ws", "wq_gemm_workspace_bytes", "wq_gemm_noalloc",
+           "wq_gemm_ln_ws", "wq_gemm_ln_workspace_bytes", "wq_gemv",
            "wq_moe_gemv", "wq_weight_bytes", "wq_dequantize", "wq_get_device_status", "wq_status_string",
            "wq_set_wait_limit")
 
@@ -54,6 +55,10 @@ def _open(path: str):
     lib.wq_gemm.restype = ci
     lib.wq_gemv.argtypes = gemm_args
     lib.wq_gemv.restype = ci
+    lib.wq_gemm_ln_ws.argtypes = gemm_args[:6] + [vp] + gemm_args[6:-1] + [vp, sz, vp]
+    lib.wq_gemm_ln_ws.restype = ci
+    lib.wq_gemm_ln_workspace_bytes.argtypes = [ci, ci, ci, ci, cu]
+    lib.wq_gemm_ln_workspace_bytes.restype = sz
     lib.wq_gemm_noalloc.argtypes = gemm_args
     lib.wq_gemm_noalloc.restype = ci
     lib.wq_gemm_ws.argtypes = gemm_args[:-1] + [vp, sz, vp]
@@ -116,6 +121,17 @@ def wq_gemm_noalloc(n, m, k, wtype, flags, X, W, bias=None, residual=None, Y=Non
                     stream=None) -> int:
     return load().wq_gemm_noalloc(n, m, k, wtype, flags, _p(X), _p(W), _p(bias), _p(residual),
                                   _p(Y), _s(stream))
+
+
+def wq_gemm_ln_ws(n, m, k, wtype, flags, X, ln_gb, W, bias=None, residual=None, Y=None,
+                  workspace=None, workspace_bytes=0, stream=None) -> int:
+    return load().wq_gemm_ln_ws(n, m, k, wtype, flags, _p(X), _p(ln_gb), _p(W), _p(bias),
+                                _p(residual), _p(Y), _p(workspace), int(workspace_bytes),
+                                _s(stream))
+
+
+def wq_gemm_ln_workspace_bytes(n, m, k, wtype, flags) -> int:
+    return int(load().wq_gemm_ln_workspace_bytes(n, m, k, wtype, flags))
 
 
 def wq_gemm_workspace_bytes(n, m, k, wtype, flags) -> int:

@@ -404,7 +404,7 @@ size_t gemm_tc_w_workspace_bytes(int m, int k) {
 }
 
 cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
-                              const DeviceInfo &dev, cudaStream_t stream) {
+                              const DeviceInfo &dev, cudaStream_t stream, bool x_ready) {
     GemmArgs g = a;
     if (wtype != kBF16) {
         // The weights first: bf16 after X in the workspace, then the bf16 GEMM.
@@ -421,14 +421,16 @@ cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
         if (err != cudaSuccess) return err;
         g.W = wb;
     }
-    const size_t n4 = (size_t)a.n * a.k / 4;
-    long long blocks = (long long)((n4 + 1023) / 1024);
-    const long long cap = (long long)dev.sm_count * 8;
-    if (blocks > cap) blocks = cap;
-    cudaError_t err = launch_pdl(x_to_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
-                                 reinterpret_cast<const float4 *>(a.X),
-                                 reinterpret_cast<uint2 *>(workspace), n4);
-    if (err != cudaSuccess) return err;
+    if (!x_ready) {  // else the workspace already holds bf16 X (e.g. a fused LayerNorm)
+        const size_t n4 = (size_t)a.n * a.k / 4;
+        long long blocks = (long long)((n4 + 1023) / 1024);
+        const long long cap = (long long)dev.sm_count * 8;
+        if (blocks > cap) blocks = cap;
+        cudaError_t err = launch_pdl(x_to_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0,
+                                     stream, reinterpret_cast<const float4 *>(a.X),
+                                     reinterpret_cast<uint2 *>(workspace), n4);
+        if (err != cudaSuccess) return err;
+    }
     if (gemm_tcp_supported(g)) return launch_gemm_tcp(g, workspace, dev, stream);
     return launch_tc<true>(g, workspace, dev, stream);
 }

@@ -182,6 +182,48 @@ wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float
     return cuda_status(launch_gemm_tc_ws(a, wtype, workspace, *dev, (cudaStream_t)stream));
 }
 
+size_t wq_gemm_ln_workspace_bytes(int n, int m, int k, int wtype, unsigned flags) {
+    if (n <= 0 || !shape_ok(wtype, m, k)) return 0;
+    const size_t tc = wq_gemm_workspace_bytes(n, m, k, wtype, flags);
+    if (tc) return tc;                                   // bf16 LN(X) (+ bf16 W)
+    return ((size_t)n * k * 4 + 255) & ~(size_t)255;     // f32 LN(X)
+}
+
+wq_status wq_gemm_ln_ws(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                        const float *ln_gb, const void *W, const float *bias,
+                        const float *residual, float *Y, void *workspace,
+                        size_t workspace_bytes, wq_stream_t stream) {
+    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
+    if (s != WQ_OK) return s;
+    if (!ln_gb) return WQ_ERR_INVALID_ARG;
+    const size_t need = wq_gemm_ln_workspace_bytes(n, m, k, wtype, flags);
+    if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < need)
+        return WQ_ERR_INVALID_ARG;
+    if ((const void *)residual == workspace || (const void *)Y == workspace)
+        return WQ_ERR_INVALID_ARG;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return WQ_ERR_CUDA;
+    const bool tc = wq_gemm_workspace_bytes(n, m, k, wtype, flags) != 0;
+    cudaError_t err = launch_layer_norm(X, ln_gb, n, k, workspace, tc, *dev, (cudaStream_t)stream);
+    if (err != cudaSuccess) return WQ_ERR_CUDA;
+    if (!tc)  // the f32 normalised rows feed the exact f32 paths, as wq_gemm
+        return wq_gemm(n, m, k, wtype, flags & ~(unsigned)WQ_TC_BF16,
+                       static_cast<const float *>(workspace), W, bias, residual, Y, stream);
+    GemmArgs a{};
+    a.X = X;  // not read: the GEMM takes the bf16 rows from the workspace
+    a.W = static_cast<const uint8_t *>(W);
+    a.bias = bias;
+    a.R = residual;
+    a.Y = Y;
+    a.n = n;
+    a.m = m;
+    a.k = k;
+    a.flags = flags & WQ_EPILOGUE_FLAGS;
+    a.status = dev->status;
+    a.wait_limit = wait_limit();
+    return cuda_status(launch_gemm_tc_ws(a, wtype, workspace, *dev, (cudaStream_t)stream, true));
+}
+
 wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtype,
                       unsigned flags, const float *X, const void *Wbank, const int32_t *ids,
                       const float *bias, const float *residual, float *Y, wq_stream_t stream) {

@@ -103,7 +103,9 @@ cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo 
                             cudaStream_t stream);
 size_t gemm_tc_w_workspace_bytes(int m, int k);
 cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
-                              const DeviceInfo &dev, cudaStream_t stream);
+                              const DeviceInfo &dev, cudaStream_t stream, bool x_ready = false);
+cudaError_t launch_layer_norm(const float *X, const float *gb, int n, int k, void *out,
+                              bool bf16_out, const DeviceInfo &dev, cudaStream_t stream);
 cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out,
                            cudaStream_t stream);
 

@@ -188,6 +188,29 @@ WQ_API wq_status wq_gemm_noalloc(int n, int m, int k, int wtype, unsigned flags,
                                  wq_stream_t stream);
 
 /*
+ * Y = epi( LayerNorm(X) . W^T ): the row LayerNorm of cortiq-engine 0.8.49
+ * src/gpu_wgpu/nemotron_audio.rs, kernel ae_ln (y = (x - mean) / sqrt(var + 1e-5)
+ * * g + b per row, biased variance), fused into the pass that prepares X for the
+ * contraction -- the encoder block's "LN, then projection".
+ * ln_gb: f32 [2*k] on the device, gamma (k values) then beta (k values), as the
+ * kernel's weight buffer.  Everything else as wq_gemm_ws.  The normalised rows are
+ * written to the workspace (f32; bf16, rounded to nearest even, on the
+ * tensor-core route) and the contraction reads them from there.
+ * workspace: at least wq_gemm_ln_workspace_bytes(...) bytes, 256-byte aligned,
+ * overlapping no other argument.
+ * Errors: as wq_gemm_ws, plus WQ_ERR_INVALID_ARG for a null ln_gb.
+ */
+WQ_API wq_status wq_gemm_ln_ws(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                               const float *ln_gb, const void *W, const float *bias,
+                               const float *residual, float *Y, void *workspace,
+                               size_t workspace_bytes, wq_stream_t stream);
+
+/* Workspace bytes wq_gemm_ln_ws needs: wq_gemm_workspace_bytes(...) on the
+ * tensor-core route, else 4*n*k (the f32 normalised rows), rounded up to 256.
+ * 0 for an invalid shape. */
+WQ_API size_t wq_gemm_ln_workspace_bytes(int n, int m, int k, int wtype, unsigned flags);
+
+/*
  * Same contract as wq_gemm for small n (1 <= n <= WQ_GEMV_MAX_N): the
  * HBM-bound path that streams each weight byte once (hanzo-ml matvec_q*_gpu).
  * WQ_TC_BF16 is rejected (WQ_ERR_INVALID_ARG).

@@ -237,3 +237,16 @@ def workload_quant_prefill(seed=6, wtype=WTYPE_Q4_0, n=512, m=14336, k=4096):
     return dict(name=f"{tag}_tc_prefill_n{n}_m{m}_k{k}", kind="gemm_tc", wtype=wtype, n=n, m=m,
                 k=k, flags=0, W=draw_weights(g, wtype, m, k), X=normal_f32(g, (n, k)),
                 bias=None, residual=None)
+
+
+def workload_ln_qkv(seed=7, n=1500, d=1024):
+    """The encoder block's first step: row LayerNorm of X, then the fused qkv
+    projection with bias on the tensor cores (X with a mean and a scale; gamma
+    ~ N(1, 0.1), beta ~ N(0, 0.1))."""
+    g = rng(seed)
+    return dict(name=f"ln_bf16_tc_qkv_n{n}_m{3 * d}_k{d}", kind="gemm_ln_tc", wtype=WTYPE_BF16,
+                n=n, m=3 * d, k=d, flags=FLAG_BIAS, X=normal_f32(g, (n, d), 3.0) + np.float32(1.5),
+                ln_gb=np.concatenate([normal_f32(g, (d,), 0.1) + np.float32(1.0),
+                                      normal_f32(g, (d,), 0.1)]),
+                W=draw_bf16_weights(g, 3 * d, d, 0.03), bias=normal_f32(g, (3 * d,), 0.1),
+                residual=None)

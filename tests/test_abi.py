@@ -112,6 +112,22 @@ def test_noalloc_rejects_requests_beyond_its_scratch(lib):
         wq.WQ_ERR_INVALID_ARG
 
 
+def test_layernorm_workspace_sizes_and_errors(lib):
+    TC = wq.WQ_TC_BF16
+    # tensor-core route: as wq_gemm_workspace_bytes; else the f32 normalised rows
+    assert wq.wq_gemm_ln_workspace_bytes(1500, 3072, 1024, wq.WQ_BF16, TC) == 1500 * 1024 * 2
+    assert wq.wq_gemm_ln_workspace_bytes(1500, 3072, 1024, wq.WQ_BF16, 0) == 1500 * 1024 * 4
+    assert wq.wq_gemm_ln_workspace_bytes(3, 64, 96, wq.WQ_Q8_0, 0) == 1280   # 1152 -> 256
+    assert wq.wq_gemm_ln_workspace_bytes(0, 64, 96, wq.WQ_Q8_0, 0) == 0
+    need = wq.wq_gemm_ln_workspace_bytes(4, 64, 64, wq.WQ_BF16, 0)
+    call = lambda gb, ws, nb: wq.wq_gemm_ln_ws(4, 64, 64, wq.WQ_BF16, 0, A, gb, A, None, None,
+                                               A + 4096, ws, nb, 0)
+    assert call(None, A + 65536, need) == wq.WQ_ERR_INVALID_ARG      # no gamma/beta
+    assert call(A, None, need) == wq.WQ_ERR_INVALID_ARG              # no workspace
+    assert call(A, A + 65536 + 16, need) == wq.WQ_ERR_INVALID_ARG    # not 256-byte aligned
+    assert call(A, A + 65536, need - 1) == wq.WQ_ERR_INVALID_ARG     # too small
+
+
 def test_unsupported_requests(lib):
     assert wq.wq_gemm(32, 8, 32, wq.WQ_Q8_0, wq.WQ_TC_BF16, A, A, None, None, A, 0) == \
         wq.WQ_ERR_UNSUPPORTED
