@@ -107,6 +107,24 @@ def test_gemv_tensor_core_wide_range_x(oracle_mod, wtype, n):
     assert_within(Y, Yref, S, TAU, what=f"wide-range X wtype={wtype} n={n}")
 
 
+@pytest.mark.parametrize("wtype", [Q8_0, Q4_0])
+@pytest.mark.parametrize("n,m,k", [(1, 151936, 4096),   # a vocabulary-sized output projection
+                                   (4, 2048, 16384)])   # a long reduction
+def test_gemv_at_size_limits(oracle_mod, wtype, n, m, k):
+    """Large m and large k through the tensor-core GEMV; the oracle checks bands of
+    rows at both ends and in the middle."""
+    g = synth.rng(m + k + wtype)
+    X = synth.normal_f32(g, (n, k))
+    img = synth.draw_weights(g, wtype, m, k)
+    Y = run_gemm(wq.wq_gemv, n, m, k, wtype, 0, X, img)
+    assert np.isfinite(Y).all()
+    for j0 in (0, m // 2 - 40, m - 96):
+        rows = (j0, j0 + 96)
+        Yref, S = oracle_mod.gemm(n, m, k, wtype, 0, X, img, rows=rows)
+        sl = slice(*rows)
+        assert_within(Y[:, sl], Yref[:, sl], S[:, sl], TAU, what=f"size limits rows {rows}")
+
+
 @pytest.mark.parametrize("shape", [(1, 1, 8), (1, 37, 16), (2, 130, 1032), (3, 300, 2056),
                                    (4, 65, 4104), (8, 200, 520), (16, 33, 1000)])
 def test_gemv_bf16(oracle_mod, shape):
