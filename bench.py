@@ -12,12 +12,13 @@ measured step time.  Peaks are the measured ones in MEASURED_PEAKS.json.
 
 Timing: inputs resident in HBM; two rotating input sets (a step touches
 ~340 MB, so every buffer is re-read only after ~680 MB, > 5x the 129 MB L2);
-each step is a CUDA graph of the nine calls with a timing event between
-calls; K steps are replayed back to back between a barrier + synchronize and
-timed with CUDA events; per-launch durations come from the events of the last
-min(K, 64) steps of that timed region.  Every kernel is launched with
-programmatic stream serialization, so a kernel's launch overlaps the tail of the
-previous one.  `e2e` times the same steps driven from
+each step is a CUDA graph of the nine calls back to back; K steps are
+replayed back to back between a barrier + synchronize and timed with CUDA
+events.  Every kernel is launched with programmatic stream serialization, so a
+kernel's launch and set-up overlap the tail of the previous one, across calls
+too.  Per-call durations come from a separate replay of min(K, 64) copies of
+the step graph with a timing event between calls (an event between two kernels
+ends that overlap, so these per-call times include one launch gap each).  `e2e` times the same steps driven from
 the host through the Python binding, with the activations copied from pinned
 host memory before and the outputs copied back after every step.
 
@@ -435,8 +436,18 @@ def run_gpu(args):
                     ev[i + 1].record()
             graphs.append(gr)
             events.append(ev)
+        # The timed steps: the same calls with no event between them.
+        plain = []
+        for g in range(min(2, ng)):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(nl):
+                    st = sets[g % 2].call(i)
+                    if st != 0:
+                        raise RuntimeError(f"capture {ws[i]['name']}: {wq.wq_status_string(st)}")
+            plain.append(gr)
         for s in range(max(3, args.warmup)):
-            graphs[s % ng].replay()
+            plain[s % len(plain)].replay()
         torch.cuda.synchronize()
 
         clocks = ClockSampler(local)
@@ -447,7 +458,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         t_start.record()
         for s in range(args.steps):
-            graphs[s % ng].replay()
+            plain[s % len(plain)].replay()
         t_end.record()
         torch.cuda.synchronize()
         barrier(world)
@@ -457,9 +468,12 @@ def run_gpu(args):
         if st != 0:
             raise RuntimeError(f"device status after timed steps: {wq.wq_status_string(st)}")
 
-        # Per-launch durations from the events of the last min(K, 64) steps.
+        # Per-call durations: one replay of each event graph.
         per = np.zeros((ng, nl))
         if in_graph_events:
+            for g in range(ng):
+                graphs[g].replay()
+            torch.cuda.synchronize()
             for g in range(ng):
                 for i in range(nl):
                     per[g, i] = events[g][i].elapsed_time(events[g][i + 1]) * 1e3

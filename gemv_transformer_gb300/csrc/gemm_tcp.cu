@@ -16,6 +16,13 @@
 //     spans KS 128-byte swizzle atoms of k (64 bf16 each), since the bytes the
 //     TMA unit of one SM delivers per stage grow with the stage size;
 //   * warp 2 issues tcgen05.mma (M=128, N=BN, K=16);
+//   * pair mode (a cluster of two CTAs on two SMs, cta_group::2): a tile is
+//     256 x BN; each CTA stages its own 128 rows of A and BN/2 rows of B, the
+//     even-rank CTA issues M = 256 MMAs over both CTAs' shared memory, and each
+//     CTA's TMEM receives its 128 rows of the accumulator.  Per SM this halves
+//     the operand bytes per MMA flop relative to a 128 x BN tile, and operand
+//     delivery (bytes in flight per SM over the L2 latency) is what bounds the
+//     one-SM schedule;
 //   * 16 epilogue warps (4 per TMEM lane quarter) take 32x32 blocks: tcgen05.ld,
 //     bias (one coalesced load per block, broadcast by shuffles) and erf-GELU in
 //     registers, the block into a 128-byte-swizzled shared buffer, residual added
@@ -43,12 +50,14 @@ constexpr int kThreads = (kRoles + kEpi) * 32;
 constexpr int kAtomA = BM * BK * 2;            // one 128-row swizzle atom of A: 16 KB
 constexpr int kStgBytes = 32 * 32 * 4;         // one 32x32 f32 block
 
-template <int BN, int KS>
+template <int BN, int KS, bool PAIR>
 struct PLayout {
+    static constexpr int kBRows = PAIR ? BN / 2 : BN;     // W rows this CTA stages
     static constexpr int kABytes = KS * kAtomA;            // A of a stage
-    static constexpr int kBBytes = KS * BN * BK * 2;       // B of a stage
+    static constexpr int kBAtom = kBRows * BK * 2;         // one swizzle atom of B
+    static constexpr int kBBytes = KS * kBAtom;            // B of a stage
     static constexpr int kFit = (216 * 1024 - kEpi * kStgBytes) / (kABytes + kBBytes);
-    static constexpr int kStages = kFit > 6 ? 6 : kFit;
+    static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static_assert(kStages >= 2, "at least two stages");
     static constexpr size_t kA = 0;
     static constexpr size_t kB = kA + (size_t)kStages * kABytes;
@@ -60,15 +69,18 @@ struct PLayout {
     static constexpr size_t kBytes = kMisc + 16 + 1024;
 };
 
-template <int BN, int KS>
+template <int BN, int KS, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcp_kernel(const __grid_constant__ CUtensorMap wmap,
                     const __grid_constant__ CUtensorMap xmap,
                     const __grid_constant__ CUtensorMap ymap,
                     const __grid_constant__ CUtensorMap rmap, const GemmArgs a) {
-    pdl_enter();
-    using L = PLayout<BN, KS>;
+    // Barriers, tensor memory and descriptors are set up before waiting for the
+    // previous grid (they touch nothing it writes); global memory after.
+    pdl_launch();
+    using L = PLayout<BN, KS, PAIR>;
     constexpr int S = L::kStages;
+    constexpr int TM = PAIR ? 2 * BM : BM;  // tile rows
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -85,19 +97,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int RB = (a.n + BM - 1) / BM, CB = (a.m + BN - 1) / BN;
+    // Pair mode: CTA `rank` of pair `unit`; otherwise every CTA is its own unit.
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const bool leader = rank == 0;
+    const int RB = (a.n + TM - 1) / TM, CB = (a.m + BN - 1) / BN;
     const int tiles = RB * CB;
     const int KB = (a.k + KS * BK - 1) / (KS * BK);  // stages per tile
     const uint64_t limit = a.wait_limit;
 
+    if (threadIdx.x == 32) {
+        prefetch_tmap(&xmap);
+        prefetch_tmap(&wmap);
+        prefetch_tmap(&ymap);
+        if (a.flags & kResidual) prefetch_tmap(&rmap);
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 2);  // one expect_tx arrival per producer
+            // One expect_tx arrival per producer of this CTA; in pair mode the
+            // even CTA's producers expect the bytes of both CTAs' copies.
+            mbar_init(&full[s], 2);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], kEpi);
+            mbar_init(&tempty[b], PAIR ? 2 * kEpi : kEpi);  // both CTAs' epilogue warps
         }
         for (int w = 0; w < kEpi; ++w) mbar_init(&rbar[w], 1);
         mbar_init(drain, 1);
@@ -105,16 +130,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 2) {  // TMEM: two accumulators of BN f32 columns x 128 lanes
-        asm volatile(
-            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                smem_addr(tmem_slot)),
-            "r"(2 * BN)
-            : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {   // one warp of each CTA of the pair allocates collectively
+            asm volatile(
+                "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                    smem_addr(tmem_slot)),
+                "r"(2 * BN)
+                : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile(
+                "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                    smem_addr(tmem_slot)),
+                "r"(2 * BN)
+                : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if (PAIR)
+        cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
+    else
+        __syncthreads();
     tc_fence_after();
+    pdl_wait();
     const uint32_t tmem = *tmem_slot;
 
     if (warp < 2) {
@@ -123,13 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const bool isA = warp == 0;
             const CUtensorMap *map = isA ? &xmap : &wmap;
-            const int atom = isA ? kAtomA : BN * BK * 2;
+            const int atom = isA ? kAtomA : L::kBAtom;
             uint8_t *base = isA ? sA : sB;
             const int sbytes = isA ? L::kABytes : L::kBBytes;
             long long q = 0;  // stages issued
             bool ok = true;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                const int y = isA ? (t % RB) * BM : (t / RB) * BN;
+            for (int t = unit; t < tiles && ok; t += units) {
+                const int y = isA ? (t % RB) * TM + (int)rank * BM
+                                  : (t / RB) * BN + (int)rank * L::kBRows;
                 for (int kb = 0; kb < KB; ++kb, ++q) {
                     const int s = (int)(q % S);
                     if (q >= S && !wait_or_abort(&empty[s], (uint32_t)(((q / S) - 1) & 1),
@@ -137,29 +177,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)sbytes);
                     uint8_t *dst = base + (size_t)s * sbytes;
+                    if (PAIR) {
+                        // Copies of both CTAs complete on the even CTA's full[s].
+                        if (leader) mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * sbytes));
+                        const uint32_t bar = map_to_rank(&full[s], 0);
 #pragma unroll
-                    for (int u = 0; u < KS; ++u)
-                        tma_load_2d(dst + u * atom, map, (kb * KS + u) * BK, y, &full[s]);
+                        for (int u = 0; u < KS; ++u)
+                            tma_load_2d_pair(dst + u * atom, map, (kb * KS + u) * BK, y, bar);
+                    } else {
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)sbytes);
+#pragma unroll
+                        for (int u = 0; u < KS; ++u)
+                            tma_load_2d(dst + u * atom, map, (kb * KS + u) * BK, y, &full[s]);
+                    }
                 }
             }
-            for (long long d = (q > S ? q - S : 0); d < q; ++d)
-                mbar_wait(&full[d % S], (uint32_t)((d / S) & 1), kDrainPolls);
+            if (!PAIR || leader) {
+                for (long long d = (q > S ? q - S : 0); d < q; ++d)
+                    mbar_wait(&full[d % S], (uint32_t)((d / S) & 1), kDrainPolls);
+            } else if (!ok) {
+                // The odd CTA's copies complete on its peer's barriers, which it
+                // cannot poll: after an abort it gives them ample time to land
+                // before the final cluster barrier lets the peer exit.  Without
+                // an abort every copy is consumed by an MMA before that barrier.
+                for (int i = 0; i < 256; ++i) __nanosleep(1000);
+            }
         }
     } else if (warp == 2) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(BM, BN);
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_bf16(TM, BN);
             long long q = 0;
             int it = 0;  // local tile index
             bool ok = true;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++it) {
+            for (int t = unit; t < tiles && ok; t += units, ++it) {
                 const int b = it & 1;
-                if (it >= 2 && !wait_or_abort(&tempty[b], (uint32_t)(((it >> 1) - 1) & 1),
-                                              abort_flag, limit, a.status)) {
-                    ok = false;
-                    break;
+                if (it >= 2) {
+                    const uint32_t ph = (uint32_t)(((it >> 1) - 1) & 1);
+                    ok = PAIR ? wait_or_abort_cluster(&tempty[b], ph, abort_flag, limit, a.status)
+                              : wait_or_abort(&tempty[b], ph, abort_flag, limit, a.status);
+                    if (!ok) break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * BN);
@@ -176,16 +234,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < KS; ++u)
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            tc_mma(d, smem_desc_sw128(a0 + u * kAtomA + kk * 32),
-                                   smem_desc_sw128(b0 + u * (BN * BK * 2) + kk * 32), idesc,
-                                   (kb > 0 || u > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&empty[s]);
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t ad = smem_desc_sw128(a0 + u * kAtomA + kk * 32);
+                            const uint64_t bd = smem_desc_sw128(b0 + u * L::kBAtom + kk * 32);
+                            const uint32_t acc = (kb > 0 || u > 0 || kk > 0) ? 1u : 0u;
+                            if (PAIR)
+                                tc_mma_pair(d, ad, bd, idesc, acc);
+                            else
+                                tc_mma(d, ad, bd, idesc, acc);
+                        }
+                    if (PAIR)
+                        tc_commit_pair_mc(&empty[s], 3);  // frees the stage in both CTAs
+                    else
+                        tc_commit(&empty[s]);
                 }
-                if (ok) tc_commit(&tfull[b]);
+                if (ok) {
+                    if (PAIR)
+                        tc_commit_pair_mc(&tfull[b], 3);
+                    else
+                        tc_commit(&tfull[b]);
+                }
             }
-            if (!ok) {
-                tc_commit(drain);  // completes when every MMA issued so far is done
+            // Completes when every MMA issued so far, and the arrivals committed
+            // before it, are done: needed after an abort, and in pair mode so
+            // that no commit still targets the odd CTA when the pair exits.
+            if (PAIR) {
+                tc_commit_pair(drain);
+                mbar_wait(drain, 0, kDrainPolls);
+            } else if (!ok) {
+                tc_commit(drain);
                 mbar_wait(drain, 0, kDrainPolls);
             }
         }
@@ -200,36 +277,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         bool stored = false;
         int it = 0;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++it) {
+        const uint32_t tempty_at = PAIR ? map_to_rank(&tempty[0], 0) : 0u;
+        for (int t = unit; t < tiles && ok; t += units, ++it) {
             const int b = it & 1;
-            const int i0 = (t % RB) * BM, j0 = (t / RB) * BN;
+            const int i0 = (t % RB) * TM + (int)rank * BM, j0 = (t / RB) * BN + cg * CW;
             const int r0 = i0 + q * 32;            // first row of this warp's blocks
+            constexpr int NB = CW / 32;            // 32-column blocks per warp per tile
+            // Everything that does not need the accumulator is fetched while the
+            // MMAs still run: this warp's bias values (lane c holds column c of
+            // each block) and the first block's old Y (residual) by TMA.
+            float bl[NB];
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const int jc = j0 + u * 32 + lane;
+                bl[u] = ((a.flags & kBias) && jc < a.m) ? __ldg(a.bias + jc) : 0.f;
+            }
+            // The staging block is free once the previous store has read it.
+            if (stored) {
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+            }
+            if ((a.flags & kResidual) && lane == 0) {
+                mbar_arrive_expect_tx(&rbar[ew], (uint32_t)kStgBytes);
+                tma_load_2d(stg, &rmap, j0, r0, &rbar[ew]);
+            }
             if (!wait_or_abort(&tfull[b], (uint32_t)((it >> 1) & 1), abort_flag, limit,
                                a.status)) {
+                if ((a.flags & kResidual) && lane == 0)
+                    mbar_wait(&rbar[ew], rphase, kDrainPolls);  // the copy lands first
+                __syncwarp();
                 ok = false;
                 break;
             }
             tc_fence_after();
-            for (int c0 = cg * CW; c0 < (cg + 1) * CW && ok; c0 += 32) {
-                const int jb = j0 + c0;
-                const float bl = ((a.flags & kBias) && jb + lane < a.m) ? __ldg(a.bias + jb + lane)
-                                                                         : 0.f;
-                // The staging block is free once the previous store has read it.
-                if (stored) {
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                if (!ok) break;
+                const int jb = j0 + u * 32;
+                if (u > 0) {
                     if (lane == 0) bulk_wait_read0();
                     __syncwarp();
-                }
-                if (a.flags & kResidual) {  // old Y block into the staging buffer
-                    if (lane == 0) {
+                    if ((a.flags & kResidual) && lane == 0) {
                         mbar_arrive_expect_tx(&rbar[ew], (uint32_t)kStgBytes);
                         tma_load_2d(stg, &rmap, jb, r0, &rbar[ew]);
                     }
                 }
                 float v[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c0), v);
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) +
+                              (uint32_t)(b * BN + cg * CW + u * 32),
+                          v);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float bc = __shfl_sync(0xFFFFFFFFu, bl, c);
+                    const float bc = __shfl_sync(0xFFFFFFFFu, bl[u], c);
                     float x = v[c];
                     if (a.flags & kBias) x += bc;
                     v[c] = activate(x, a.flags);
@@ -271,19 +370,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             // This accumulator may be refilled.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && ok) mbar_arrive(&tempty[b]);
+            if (lane == 0 && ok) {
+                if (PAIR)  // the even CTA's MMA warp waits for both CTAs' epilogues
+                    mbar_arrive_cluster(tempty_at + (uint32_t)(b * sizeof(uint64_t)));
+                else
+                    mbar_arrive(&tempty[b]);
+            }
         }
         if (lane == 0) bulk_wait0();
         __syncwarp();
     }
     __syncwarp();  // every role's lanes meet before the block-wide barrier
     tc_fence_before();
-    __syncthreads();
+    if (PAIR)
+        cluster_sync_all();  // neither CTA leaves while the other may still signal it
+    else
+        __syncthreads();
     if (warp == 2) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(2 * BN)
-                     : "memory");
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(2 * BN)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                         "r"(2 * BN)
+                         : "memory");
     }
 }
 
@@ -315,13 +427,47 @@ bool encode_2d(CUtensorMap &map, CUtensorMapDataType dt, int esize, const void *
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int KS>
+// Pairs of SMs that can hold a pair-mode CTA cluster at once on this device, or 0.
+template <typename Kernel>
+int max_pairs(Kernel kern, int smem, const DeviceInfo &dev) {
+    static std::atomic<int> cached[64];
+    std::atomic<int> &c = cached[dev.ordinal & 63];
+    int v = c.load(std::memory_order_acquire);
+    if (v != 0) return v < 0 ? 0 : v;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        c.store(-1, std::memory_order_release);
+        return 0;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(2 * (dev.sm_count / 2)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        clusters = 0;
+    }
+    c.store(clusters > 0 ? clusters : -1, std::memory_order_release);
+    return clusters;
+}
+
+template <int BN, int KS, bool PAIR>
 cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
-                      cudaStream_t stream) {
-    using L = PLayout<BN, KS>;
+                      cudaStream_t stream, int pairs = 0) {
+    using L = PLayout<BN, KS, PAIR>;
+    constexpr int TM = PAIR ? 2 * BM : BM;
     static std::atomic<unsigned long long> smem_set{0};
     CUtensorMap wmap, xmap, ymap, rmap;
-    if (!encode_2d(wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W, a.k, a.m, BK, BN) ||
+    if (!encode_2d(wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W, a.k, a.m, BK, L::kBRows) ||
         !encode_2d(xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xb, a.k, a.n, BK, BM) ||
         !encode_2d(ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.Y, a.m, a.n, 32, 32))
         return cudaErrorInvalidValue;
@@ -331,15 +477,32 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
     } else {
         rmap = ymap;  // unused
     }
-    auto kern = gemm_tcp_kernel<BN, KS>;
+    auto kern = gemm_tcp_kernel<BN, KS, PAIR>;
     static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
     cudaError_t err = ensure_smem(kern, (int)L::kBytes, dev, smem_set);
     if (err != cudaSuccess) return err;
-    const long long tiles =
-        (long long)((a.n + BM - 1) / BM) * ((a.m + BN - 1) / BN);
-    const int grid = (int)(tiles < dev.sm_count ? tiles : dev.sm_count);
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, stream, wmap, xmap, ymap,
-                      rmap, a);
+    const long long tiles = (long long)((a.n + TM - 1) / TM) * ((a.m + BN - 1) / BN);
+    if (!PAIR) {
+        const int grid = (int)(tiles < dev.sm_count ? tiles : dev.sm_count);
+        return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, stream, wmap, xmap, ymap,
+                          rmap, a);
+    }
+    const int np = (int)(tiles < pairs ? tiles : pairs);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(2 * np));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, wmap, xmap, ymap, rmap, a);
 }
 
 }  // namespace
@@ -353,12 +516,34 @@ bool gemm_tcp_supported(const GemmArgs &a) {
 
 cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
                             cudaStream_t stream) {
-    // Tile width: the one with fewer (tiles per SM, rounded up) x tile time.
-    const long long rows = (a.n + BM - 1) / BM;
-    const long long w256 = (rows * ((a.m + 255) / 256) + dev.sm_count - 1) / dev.sm_count;
-    const long long w128 = (rows * ((a.m + 127) / 128) + dev.sm_count - 1) / dev.sm_count;
-    if (w256 * 2 <= w128) return launch_bn<256, 1>(a, xb, dev, stream);
-    return launch_bn<128, 2>(a, xb, dev, stream);
+    // Schedule with the smallest estimate of
+    //   rounds x (64-k steps x step time + epi / 2) + epi / 2,
+    // rounds = tiles per SM (or SM pair) rounded up; the step times are measured
+    // on GB300 (128 x 128 on one SM 0.275 us and 128 x 256 0.45 us, both bound
+    // by operand delivery; 256 x 256 on an SM pair 0.33 us, bound by the MMA);
+    // epi = the time to drain one tile's accumulator, 1.5 us per 128 x 128 f32
+    // block of output per SM (twice that with an exp- or erf-based activation),
+    // about half of which overlaps the next tile's MMAs.
+    const double ks = (double)((a.k + BK - 1) / BK);
+    const double e = (a.flags & (kGelu | kSilu | kTanh)) ? 3.0 : 1.5;
+    const long long rows = (a.n + BM - 1) / BM, rows2 = (a.n + 2 * BM - 1) / (2 * BM);
+    const long long sm = dev.sm_count;
+    auto est = [&](long long tiles, long long units, double step, double epi) {
+        const double rounds = (double)((tiles + units - 1) / units);
+        return rounds * (ks * step + 0.5 * epi) + 0.5 * epi;
+    };
+    const double t128 = est(rows * ((a.m + 127) / 128), sm, 0.275, e);
+    const double t256 = est(rows * ((a.m + 255) / 256), sm, 0.45, 2 * e);
+    if (a.n > BM) {
+        using LP = PLayout<256, 1, true>;
+        const int pairs = max_pairs(gemm_tcp_kernel<256, 1, true>, (int)LP::kBytes, dev);
+        if (pairs > 0) {
+            const double tp = est(rows2 * ((a.m + 255) / 256), pairs, 0.33, 2 * e);
+            if (tp < t128 && tp < t256) return launch_bn<256, 1, true>(a, xb, dev, stream, pairs);
+        }
+    }
+    if (t256 < t128) return launch_bn<256, 1, false>(a, xb, dev, stream);
+    return launch_bn<128, 2, false>(a, xb, dev, stream);
 }
 
 }  // namespace wq

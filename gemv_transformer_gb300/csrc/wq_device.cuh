@@ -117,6 +117,15 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// The two halves of pdl_enter() for kernels that first set up on-chip state
+// (barriers, tensor memory) that no earlier grid touches: the setup then
+// overlaps the previous kernel's tail, and every thread calls pdl_wait()
+// before its first global-memory access.
+__device__ __forceinline__ void pdl_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------- mbarrier + bulk copy --
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

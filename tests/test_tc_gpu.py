@@ -80,7 +80,8 @@ def check_tc(oracle_mod, n, m, k, flags, seed, rows=None, inplace=False, std=0.0
 
 @pytest.mark.parametrize("ws", [False, True], ids=["fused", "workspace"])
 @pytest.mark.parametrize("shape", [(17, 16, 8), (128, 128, 64), (130, 256, 128), (300, 520, 1032),
-                                   (257, 300, 200), (1000, 1000, 512), (64, 2048, 256)])
+                                   (257, 300, 200), (1000, 1000, 512), (64, 2048, 256),
+                                   (1400, 3000, 264)])
 def test_tc_shapes(oracle_mod, shape, ws):
     n, m, k = shape
     check_tc(oracle_mod, n, m, k, BIAS, seed=n + m + k, ws=ws)
@@ -98,7 +99,7 @@ def test_tc_residual_in_place_ragged_m(oracle_mod, ws):
     check_tc(oracle_mod, 150, 203, 264, BIAS | RES, seed=3, inplace=True, ws=ws)
 
 
-@pytest.mark.parametrize("shape", [(300, 520, 1032), (1500, 1024, 4096)])
+@pytest.mark.parametrize("shape", [(300, 520, 1032), (1500, 1024, 4096), (1400, 3000, 264)])
 def test_tc_workspace_path_bit_identical(shape):
     """Both tensor-core paths round X the same way and accumulate in the same
     order, so their outputs agree bit for bit."""
@@ -136,12 +137,15 @@ def test_tc_deterministic():
     assert (Y1.view(np.int32) == Y2.view(np.int32)).all()
 
 
-@pytest.mark.parametrize("ws", [False, True], ids=["fused", "workspace"])
-def test_tc_wait_limit_expires_without_hang(oracle_mod, ws):
+@pytest.mark.parametrize("ws,shape", [(False, (512, 1024, 4096)), (True, (512, 1024, 4096)),
+                                      (True, (1400, 3000, 256))],
+                         ids=["fused", "workspace", "workspace-pair"])
+def test_tc_wait_limit_expires_without_hang(oracle_mod, ws, shape):
     """A one-poll wait limit aborts the tensor-core kernel's CTAs at their first
     unfilled stage: they record WQ_ERR_DEVICE_TIMEOUT, drain their TMA copies and
-    MMAs, free TMEM and return; the next call with the default limit is correct."""
-    n, m, k = 512, 1024, 4096
+    MMAs, free TMEM and return; the next call with the default limit is correct.
+    The last case runs the SM-pair schedule (256-row tiles over two CTAs)."""
+    n, m, k = shape
     g = synth.rng(6)
     X = synth.normal_f32(g, (n, k))
     img = synth.draw_bf16_weights(g, m, k, 0.03)
