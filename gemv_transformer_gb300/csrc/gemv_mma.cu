@@ -55,7 +55,6 @@ constexpr int kCW = 16;                  // consumer warps (one block of each ch
 constexpr int kThreads = (kCW + 1) * 32; // + one producer warp
 constexpr int kBlocks = 16;              // blocks (of 32 weights) per chunk
 constexpr int kMaxSlots = 256;
-constexpr int kRedBufs = 4;              // partial-sum buffers of the ordered reduction
 
 // A stage holds, for every row of the group, the 16 blocks (512 weights) of one
 // chunk, loaded as NBOX tall TMA boxes (the box inner size is at most 256 u16, so
@@ -102,9 +101,16 @@ struct Layout {
     static constexpr int kBoxBytes = T * kTileBytes;            // the group's rows, one box
     static constexpr int kWBytes = Fmt<WT>::NBOX * kBoxBytes;   // weights of a stage
     static constexpr int kStageBytes = kWBytes + Mode<MODE>::P_MAX * kXChunkBytes;
-    static constexpr int kRedBytes = kRedBufs * T * 16 * Mode<MODE>::C * 4;
     // epilogue inputs staged at the start of a pass: residual [P_MAX][T*16], bias [T*16]
     static constexpr int kEpiBytes = (T * 16 * Mode<MODE>::P_MAX + T * 16) * 4;
+    // Partial-sum buffers of the ordered reduction: 8 (two rounds of warps, three
+    // barriers per pass) when they cost no pipeline stage, else 4 (four rounds).
+    static constexpr int stages_with(int bufs) {
+        return (200 * 1024 - bufs * T * 16 * Mode<MODE>::C * 4 - kEpiBytes) / kStageBytes;
+    }
+    static constexpr int kRedBufs =
+        (stages_with(8) >= 8 || stages_with(8) == stages_with(4)) ? 8 : 4;
+    static constexpr int kRedBytes = kRedBufs * T * 16 * Mode<MODE>::C * 4;
     static constexpr int kBudget = 200 * 1024 - kRedBytes - kEpiBytes;
     static constexpr int kStages = (kBudget / kStageBytes) > 8 ? 8 : (kBudget / kStageBytes);
     static_assert(kStages >= 2, "at least two stages");
@@ -281,7 +287,9 @@ __device__ __forceinline__ int group_tiles(const Sched &sc, long long u) {
 template <int WT, bool MOE, int MODE, int T>
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap_t, const StreamArgs a) {
-    pdl_enter();
+    // The barriers and the weight map's descriptor are set up before waiting for
+    // the previous grid (they touch nothing it writes); global memory after.
+    pdl_launch();
     using L = Layout<WT, MODE, T>;
     using MD = Mode<MODE>;
     constexpr int S = L::kStages;
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *stages = smem;
     float *red = reinterpret_cast<float *>(smem + (size_t)S * L::kStageBytes);  // [4][T*16][C]
-    float *s_res = red + kRedBufs * T * 16 * C;      // [P_MAX][T*16]
+    float *s_res = red + L::kRedBufs * T * 16 * C;   // [P_MAX][T*16]
     float *s_bias = s_res + T * 16 * P_MAX;           // [T*16]
     uint64_t *full = reinterpret_cast<uint64_t *>(s_bias + T * 16);
     uint64_t *empty = full + S;
@@ -320,6 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0u;
         fence_mbar_init();
     }
+    if (threadIdx.x == kCW * 32)  // the producer's thread
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap_t)) : "memory");
+    pdl_wait();
     Sched sc;
     sc.tpe = (m + 15) / 16;
     if (MOE) {
@@ -674,34 +685,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[s]);
                 }
+                // Ordered reduction: warp w adds into buffer w % NB, in kCW / NB rounds.
+                // Round 0 needs no barrier before it (the buffers were last read before
+                // the previous pass's final barrier); an aborted warp's writes are
+                // harmless, as the pass ends at the next barrier.
+                constexpr int NB = L::kRedBufs;
+                const int RT = T * 16 * C;
+                auto round = [&](int rnd) {
+                    if (warp / NB != rnd) return;
+                    float *buf = red + (warp % NB) * RT;
+    #pragma unroll
+                    for (int tt = 0; tt < T; ++tt) {
+                        if (tt < ntiles) {
+    #pragma unroll
+                            for (int j = 0; j < NA; ++j) {
+    #pragma unroll
+                                for (int r = 0; r < 4; ++r) {
+                                    const int row = tt * 16 + g + (r >= 2 ? 8 : 0);
+                                    const int col = j * 8 + 2 * t + (r & 1);
+                                    float *dst = &buf[row * C + col];
+                                    *dst = (rnd == 0) ? acc[tt][j][r] : *dst + acc[tt][j][r];
+                                }
+                            }
+                        }
+                    }
+                };
+                round(0);
                 cp_async_wait_all();  // staged bias/residual: visible to all after the barrier
                 // Every consumer warp gets here, aborted or not; the flag read after the
                 // barrier is the same in all of them, so they leave (or go on) together.
                 consumers_sync();
                 ok = *abort_flag == 0u;
                 if (!ok) return;
-
-                // Ordered reduction: warp w adds into buffer w % 4, in 4 rounds.
-                const int RT = T * 16 * C;
-                for (int rnd = 0; rnd < kCW / kRedBufs; ++rnd) {
-                    if (warp / kRedBufs == rnd) {
-                        float *buf = red + (warp % kRedBufs) * RT;
-    #pragma unroll
-                        for (int tt = 0; tt < T; ++tt) {
-                            if (tt < ntiles) {
-    #pragma unroll
-                                for (int j = 0; j < NA; ++j) {
-    #pragma unroll
-                                    for (int r = 0; r < 4; ++r) {
-                                        const int row = tt * 16 + g + (r >= 2 ? 8 : 0);
-                                        const int col = j * 8 + 2 * t + (r & 1);
-                                        float *dst = &buf[row * C + col];
-                                        *dst = (rnd == 0) ? acc[tt][j][r] : *dst + acc[tt][j][r];
-                                    }
-                                }
-                            }
-                        }
-                    }
+                for (int rnd = 1; rnd < kCW / NB; ++rnd) {
+                    round(rnd);
                     consumers_sync();
                 }
                 const int R = ntiles * 16;
@@ -711,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (row < m) {
                         float v = 0.f;
     #pragma unroll
-                        for (int b = 0; b < kRedBufs; ++b) {
+                        for (int b = 0; b < NB; ++b) {
                             const float *rp = red + b * RT + r * C;
                             v += packed ? rp[i] + rp[P + i] : rp[i];
                         }
