@@ -23,6 +23,16 @@
 //     the operand bytes per MMA flop relative to a 128 x BN tile, and operand
 //     delivery (bytes in flight per SM over the L2 latency) is what bounds the
 //     one-SM schedule;
+//   * helper mode (a cluster of h + 1 CTAs, h = 2 or 3, for shapes with too few
+//     tiles to fill the SMs): CTAs 0..h-1 each own one 128 x 128 tile and run
+//     the first h / (h + 1) of its k stages; CTA h runs the rest of all h tiles,
+//     each into a TMEM accumulator of its own, and as each finishes writes that
+//     partial accumulator into the owner tile's block of Y (scratch until the
+//     owner's epilogue overwrites it; so Y must not overlap the residual) and
+//     signals the owner through a cluster barrier; the owner loads it back into
+//     its idle A stage buffers and adds it before its epilogue.  The sum order
+//     is fixed, so results are deterministic; e.g. 128 SMs work on 96 tiles
+//     instead of 96 SMs;
 //   * 16 epilogue warps (4 per TMEM lane quarter) take 32x32 blocks: tcgen05.ld,
 //     bias (one coalesced load per block, broadcast by shuffles) and erf-GELU in
 //     registers, the block into a 128-byte-swizzled shared buffer, residual added
@@ -50,8 +60,13 @@ constexpr int kThreads = (kRoles + kEpi) * 32;
 constexpr int kAtomA = BM * BK * 2;            // one 128-row swizzle atom of A: 16 KB
 constexpr int kStgBytes = 32 * 32 * 4;         // one 32x32 f32 block
 
-template <int BN, int KS, bool PAIR>
+// Schedules: one SM per tile, an SM pair per 256-row tile, or two tile owners
+// and a helper per cluster of three.
+enum Sched : int { kData = 0, kPair = 1, kHelp = 2 };
+
+template <int BN, int KS, int SCH>
 struct PLayout {
+    static constexpr bool PAIR = SCH == kPair;
     static constexpr int kBRows = PAIR ? BN / 2 : BN;     // W rows this CTA stages
     static constexpr int kABytes = KS * kAtomA;            // A of a stage
     static constexpr int kBAtom = kBRows * BK * 2;         // one swizzle atom of B
@@ -63,13 +78,23 @@ struct PLayout {
     static constexpr size_t kB = kA + (size_t)kStages * kABytes;
     static constexpr size_t kStg = kB + (size_t)kStages * kBBytes;
     static constexpr size_t kBars = kStg + (size_t)kEpi * kStgBytes;
-    // full[S], empty[S], tfull[2], tempty[2], rbar[kEpi], drain
-    static constexpr int kNumBars = 2 * kStages + 4 + kEpi + 1;
+    // full[S], empty[S], tfull[4], tempty[2], rbar[kEpi], drain, pbar[kEpi], recv[kEpi]
+    static constexpr int kNumBars = 2 * kStages + 6 + kEpi + 1 + kEpi + kEpi;
+    // Helper mode: a 128 x BN f32 partial accumulator fits the A stage buffers.
+    static_assert(SCH != kHelp || (BN == 128 && kStages * kABytes >= BM * BN * 4),
+                  "helper hand-over buffer");
     static constexpr size_t kMisc = kBars + kNumBars * sizeof(uint64_t);
     static constexpr size_t kBytes = kMisc + 16 + 1024;
 };
 
-template <int BN, int KS, bool PAIR>
+// Helper mode: the owners' share of a tile's KB stages.  The helper's share is
+// three quarters of an even split (KB / (h + 1) per tile), since each hand-over
+// (a 64 KB store while its next segment streams in) costs it about two stages.
+__host__ __device__ constexpr int help_split(int KB, int h) {
+    return KB - ((3 * KB) / (4 * (h + 1)) > 1 ? (3 * KB) / (4 * (h + 1)) : 1);
+}
+
+template <int BN, int KS, int SCH>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcp_kernel(const __grid_constant__ CUtensorMap wmap,
                     const __grid_constant__ CUtensorMap xmap,
@@ -78,7 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Barriers, tensor memory and descriptors are set up before waiting for the
     // previous grid (they touch nothing it writes); global memory after.
     pdl_launch();
-    using L = PLayout<BN, KS, PAIR>;
+    using L = PLayout<BN, KS, SCH>;
+    constexpr bool PAIR = SCH == kPair, HELP = SCH == kHelp;
     constexpr int S = L::kStages;
     constexpr int TM = PAIR ? 2 * BM : BM;  // tile rows
     extern __shared__ uint8_t smem_raw[];
@@ -89,23 +115,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sStg = smem + L::kStg;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBars);
     uint64_t *empty = full + S;
-    uint64_t *tfull = empty + S;
-    uint64_t *tempty = tfull + 2;
+    uint64_t *tfull = empty + S;   // [4]: helper mode uses one per segment
+    uint64_t *tempty = tfull + 4;
     uint64_t *rbar = tempty + 2;
     uint64_t *drain = rbar + kEpi;
+    uint64_t *pbar = drain + 1;    // helper mode, in an owner: warp w's partial block loaded
+    uint64_t *recv = pbar + kEpi;  // helper mode, in an owner: warp w's partial block is in Y
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kMisc);
     volatile uint32_t *abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Pair mode: CTA `rank` of pair `unit`; otherwise every CTA is its own unit.
-    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    // Pair and helper modes: CTA `rank` of cluster `unit`; otherwise every CTA is
+    // its own unit.
+    const uint32_t rank = (PAIR || HELP) ? cluster_ctarank() : 0u;
+    const int csize = PAIR ? 2 : (HELP ? (int)cluster_nctarank() : 1);
+    const int h = csize - 1;       // helper mode: tile owners per cluster
+    const int unit = (int)blockIdx.x / csize;
+    const int units = (int)gridDim.x / csize;
     const bool leader = rank == 0;
+    const bool helper = HELP && (int)rank == h;
     const int RB = (a.n + TM - 1) / TM, CB = (a.m + BN - 1) / BN;
     const int tiles = RB * CB;
     const int KB = (a.k + KS * BK - 1) / (KS * BK);  // stages per tile
     const uint64_t limit = a.wait_limit;
+    // This CTA's work as segments: (tile, k stages [kb0, kb1)), in processing
+    // order.  Helper mode: owner r takes stages [0, ks) of tile h * unit + r, the
+    // helper stages [ks, KB) of all h tiles.
+    const int ks_own = HELP ? help_split(KB, h) : KB;
+    int nseg;
+    if (HELP) {
+        const int left = tiles - h * unit;
+        nseg = helper ? (left < h ? left : h) : ((int)rank < left ? 1 : 0);
+        if (nseg < 0) nseg = 0;
+    } else {
+        nseg = unit < tiles ? (tiles - unit + units - 1) / units : 0;
+    }
+    auto seg_tile = [&](int i) {
+        return HELP ? h * unit + (helper ? i : (int)rank) : unit + i * units;
+    };
+    // TMEM accumulator and tfull barrier of segment i (helper mode: one each).
+    auto seg_buf = [&](int i) { return HELP ? i : (i & 1); };
+    const int kb0 = helper ? ks_own : 0;
+    const int kb1 = (HELP && !helper) ? ks_own : KB;
 
     if (threadIdx.x == 32) {
         prefetch_tmap(&xmap);
@@ -120,16 +171,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[s], 2);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&tfull[b], 1);
+        for (int b = 0; b < 4; ++b) mbar_init(&tfull[b], 1);
+        for (int b = 0; b < 2; ++b)
             mbar_init(&tempty[b], PAIR ? 2 * kEpi : kEpi);  // both CTAs' epilogue warps
-        }
         for (int w = 0; w < kEpi; ++w) mbar_init(&rbar[w], 1);
         mbar_init(drain, 1);
+        for (int w = 0; w < kEpi; ++w) mbar_init(&pbar[w], 1);
+        for (int w = 0; w < kEpi; ++w) mbar_init(&recv[w], 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (warp == 2) {  // TMEM: two accumulators of BN f32 columns x 128 lanes
+    // TMEM: two accumulators of BN f32 columns x 128 lanes (a helper: one per
+    // segment, up to three, in a power-of-two allocation).
+    const uint32_t ncols = helper ? 512u : (uint32_t)(2 * BN);
+    if (warp == 2) {
         if (PAIR) {   // one warp of each CTA of the pair allocates collectively
             asm volatile(
                 "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -141,15 +196,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile(
                 "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                     smem_addr(tmem_slot)),
-                "r"(2 * BN)
+                "r"(ncols)
                 : "memory");
             asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         }
     }
     tc_fence_before();
     __syncwarp();
-    if (PAIR)
-        cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
+    if (PAIR || HELP)
+        cluster_sync_all();  // every CTA's barriers exist before any remote arrival
     else
         __syncthreads();
     tc_fence_after();
@@ -167,10 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sbytes = isA ? L::kABytes : L::kBBytes;
             long long q = 0;  // stages issued
             bool ok = true;
-            for (int t = unit; t < tiles && ok; t += units) {
-                const int y = isA ? (t % RB) * TM + (int)rank * BM
-                                  : (t / RB) * BN + (int)rank * L::kBRows;
-                for (int kb = 0; kb < KB; ++kb, ++q) {
+            for (int i = 0; i < nseg && ok; ++i) {
+                const int t = seg_tile(i);
+                const int y = isA ? (t % RB) * TM + (PAIR ? (int)rank * BM : 0)
+                                  : (t / RB) * BN + (PAIR ? (int)rank * L::kBRows : 0);
+                for (int kb = kb0; kb < kb1; ++kb, ++q) {
                     const int s = (int)(q % S);
                     if (q >= S && !wait_or_abort(&empty[s], (uint32_t)(((q / S) - 1) & 1),
                                                  abort_flag, limit, a.status)) {
@@ -206,14 +262,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 2) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0 && leader) {
+        if (lane == 0 && (leader || !PAIR)) {
             constexpr uint32_t idesc = idesc_bf16(TM, BN);
             long long q = 0;
-            int it = 0;  // local tile index
             bool ok = true;
-            for (int t = unit; t < tiles && ok; t += units, ++it) {
-                const int b = it & 1;
-                if (it >= 2) {
+            for (int it = 0; it < nseg && ok; ++it) {
+                const int b = seg_buf(it);
+                if (!HELP && it >= 2) {
                     const uint32_t ph = (uint32_t)(((it >> 1) - 1) & 1);
                     ok = PAIR ? wait_or_abort_cluster(&tempty[b], ph, abort_flag, limit, a.status)
                               : wait_or_abort(&tempty[b], ph, abort_flag, limit, a.status);
@@ -221,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * BN);
-                for (int kb = 0; kb < KB; ++kb, ++q) {
+                for (int kb = kb0; kb < kb1; ++kb, ++q) {
                     const int s = (int)(q % S);
                     if (!wait_or_abort(&full[s], (uint32_t)((q / S) & 1), abort_flag, limit,
                                        a.status)) {
@@ -237,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int kk = 0; kk < BK / 16; ++kk) {
                             const uint64_t ad = smem_desc_sw128(a0 + u * kAtomA + kk * 32);
                             const uint64_t bd = smem_desc_sw128(b0 + u * L::kBAtom + kk * 32);
-                            const uint32_t acc = (kb > 0 || u > 0 || kk > 0) ? 1u : 0u;
+                            const uint32_t acc = (kb > kb0 || u > 0 || kk > 0) ? 1u : 0u;
                             if (PAIR)
                                 tc_mma_pair(d, ad, bd, idesc, acc);
                             else
@@ -276,11 +331,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t rphase = 0;
         bool ok = true;
         bool stored = false;
-        int it = 0;
+        bool hfail = false;  // helper mode: a segment could not be served
         const uint32_t tempty_at = PAIR ? map_to_rank(&tempty[0], 0) : 0u;
-        for (int t = unit; t < tiles && ok; t += units, ++it) {
-            const int b = it & 1;
-            const int i0 = (t % RB) * TM + (int)rank * BM, j0 = (t / RB) * BN + cg * CW;
+        for (int it = 0; it < nseg && ok; ++it) {
+            const int t = seg_tile(it);
+            const int b = seg_buf(it);
+            const uint32_t tph = HELP ? 0u : (uint32_t)((it >> 1) & 1);
+            if (HELP && helper) {
+                // Helper: as each segment's MMAs finish, its partial accumulator goes
+                // to the owner tile's block of Y (staging buffer + TMA store); once
+                // the store is complete the owner's warp is signalled.  An owner that
+                // cannot be served (an expired wait here) is told so: its abort flag
+                // is set before the signal.
+                const int r = t - h * unit;
+                const int hr = (t % RB) * BM + q * 32, hc = (t / RB) * BN + cg * CW;
+                // After a failure every later owner is declined too (each is signalled).
+                bool serve = !hfail && wait_or_abort(&tfull[b], 0u, abort_flag, limit, a.status);
+                serve = __all_sync(0xFFFFFFFFu, serve);
+                if (serve) {
+                    tc_fence_after();
+                    float v[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + cg * CW),
+                              v);
+                    if (stored) {
+                        if (lane == 0) bulk_wait_read0();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    fence_proxy_async_smem();  // generic-proxy writes -> TMA store reads
+                    __syncwarp();
+                    stored = true;
+                }
+                if (lane == 0) {
+                    if (serve) {
+                        tma_store_2d(&ymap, hc, hr, stg);
+                        bulk_commit();
+                        bulk_wait0();                // the block is in Y
+                        fence_proxy_async_global();
+                    } else {
+                        st_cluster_u32(map_to_rank((const void *)abort_flag, (uint32_t)r), 1u);
+                    }
+                    mbar_arrive_cluster(map_to_rank(&recv[ew], (uint32_t)r));
+                }
+                __syncwarp();
+                if (!serve) hfail = true;
+                if (it == nseg - 1 && hfail) ok = false;
+                continue;
+            }
+            const int i0 = (t % RB) * TM + (PAIR ? (int)rank * BM : 0);
+            const int j0 = (t / RB) * BN + cg * CW;
             const int r0 = i0 + q * 32;            // first row of this warp's blocks
             constexpr int NB = CW / 32;            // 32-column blocks per warp per tile
             // Everything that does not need the accumulator is fetched while the
@@ -301,8 +403,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&rbar[ew], (uint32_t)kStgBytes);
                 tma_load_2d(stg, &rmap, j0, r0, &rbar[ew]);
             }
-            if (!wait_or_abort(&tfull[b], (uint32_t)((it >> 1) & 1), abort_flag, limit,
-                               a.status)) {
+            bool got = wait_or_abort(&tfull[b], tph, abort_flag, limit, a.status);
+            got = __all_sync(0xFFFFFFFFu, got);
+            if (HELP && nseg > 0) {
+                // Owner: the helper always signals (its partial is in Y, or it set
+                // this CTA's abort flag), so this wait is long but always ends.  The
+                // partial comes back by TMA into the A stage buffers, idle once this
+                // CTA's MMAs are done.
+                bool in = false;
+                for (uint64_t i = 0; i < kDrainPolls && !in; ++i) in = mbar_try_wait_cluster(&recv[ew], 0u);
+                in = __all_sync(0xFFFFFFFFu, in);
+                got = got && in && *abort_flag == 0u;
+                if (got) {
+                    if (lane == 0) {
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(&pbar[ew], (uint32_t)kStgBytes);
+                        tma_load_2d(sA + ew * kStgBytes, &ymap, j0, r0, &pbar[ew]);
+                    }
+                    bool w = mbar_wait(&pbar[ew], 0u, limit);
+                    w = __all_sync(0xFFFFFFFFu, w);
+                    if (!w) {
+                        if (lane == 0) {
+                            if (!*abort_flag) record_status(a.status, kStTimeout);
+                            *abort_flag = 1u;
+                            mbar_wait(&pbar[ew], 0u, kDrainPolls);
+                        }
+                        __syncwarp();
+                        got = false;
+                    }
+                }
+            }
+            if (!got) {
                 if ((a.flags & kResidual) && lane == 0)
                     mbar_wait(&rbar[ew], rphase, kDrainPolls);  // the copy lands first
                 __syncwarp();
@@ -326,6 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) +
                               (uint32_t)(b * BN + cg * CW + u * 32),
                           v);
+                if (HELP) {  // + the helper's part: k stages [ks, KB) after [0, ks)
+                    const uint8_t *pp = sA + ew * kStgBytes + lane * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 pv =
+                            *reinterpret_cast<const float4 *>(pp + ((j ^ (lane & 7)) << 4));
+                        v[4 * j] += pv.x;
+                        v[4 * j + 1] += pv.y;
+                        v[4 * j + 2] += pv.z;
+                        v[4 * j + 3] += pv.w;
+                    }
+                }
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const float bc = __shfl_sync(0xFFFFFFFFu, bl[u], c);
@@ -382,8 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();  // every role's lanes meet before the block-wide barrier
     tc_fence_before();
-    if (PAIR)
-        cluster_sync_all();  // neither CTA leaves while the other may still signal it
+    if (PAIR || HELP)
+        cluster_sync_all();  // no CTA leaves while another may still signal or write it
     else
         __syncthreads();
     if (warp == 2) {
@@ -394,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : "memory");
         else
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                         "r"(2 * BN)
+                         "r"(ncols)
                          : "memory");
     }
 }
@@ -427,11 +570,12 @@ bool encode_2d(CUtensorMap &map, CUtensorMapDataType dt, int esize, const void *
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Pairs of SMs that can hold a pair-mode CTA cluster at once on this device, or 0.
+// Clusters of `csize` CTAs of `kern` that the device holds at once, or 0 (cached
+// per device and cluster size).
 template <typename Kernel>
-int max_pairs(Kernel kern, int smem, const DeviceInfo &dev) {
-    static std::atomic<int> cached[64];
-    std::atomic<int> &c = cached[dev.ordinal & 63];
+int max_clusters(Kernel kern, int smem, int csize, const DeviceInfo &dev) {
+    static std::atomic<int> cached[8][64];
+    std::atomic<int> &c = cached[csize & 7][dev.ordinal & 63];
     int v = c.load(std::memory_order_acquire);
     if (v != 0) return v < 0 ? 0 : v;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -441,12 +585,12 @@ int max_pairs(Kernel kern, int smem, const DeviceInfo &dev) {
         return 0;
     }
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(2 * (dev.sm_count / 2)));
+    cfg.gridDim = dim3((unsigned)(csize * (dev.sm_count / csize)));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = (unsigned)csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -460,11 +604,11 @@ int max_pairs(Kernel kern, int smem, const DeviceInfo &dev) {
     return clusters;
 }
 
-template <int BN, int KS, bool PAIR>
+template <int BN, int KS, int SCH>
 cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
-                      cudaStream_t stream, int pairs = 0) {
-    using L = PLayout<BN, KS, PAIR>;
-    constexpr int TM = PAIR ? 2 * BM : BM;
+                      cudaStream_t stream, int clusters = 0) {
+    using L = PLayout<BN, KS, SCH>;
+    constexpr int TM = SCH == kPair ? 2 * BM : BM;
     static std::atomic<unsigned long long> smem_set{0};
     CUtensorMap wmap, xmap, ymap, rmap;
     if (!encode_2d(wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W, a.k, a.m, BK, L::kBRows) ||
@@ -477,25 +621,29 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
     } else {
         rmap = ymap;  // unused
     }
-    auto kern = gemm_tcp_kernel<BN, KS, PAIR>;
+    auto kern = gemm_tcp_kernel<BN, KS, SCH>;
     static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
     cudaError_t err = ensure_smem(kern, (int)L::kBytes, dev, smem_set);
     if (err != cudaSuccess) return err;
     const long long tiles = (long long)((a.n + TM - 1) / TM) * ((a.m + BN - 1) / BN);
-    if (!PAIR) {
+    if (SCH == kData) {
         const int grid = (int)(tiles < dev.sm_count ? tiles : dev.sm_count);
         return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, stream, wmap, xmap, ymap,
                           rmap, a);
     }
-    const int np = (int)(tiles < pairs ? tiles : pairs);
+    // Pair mode: up to `clusters` pairs walk the tiles.  Helper mode: `clusters`
+    // is h, one cluster of h + 1 CTAs per h tiles.
+    const int csize = SCH == kPair ? 2 : clusters + 1;
+    const long long nc =
+        SCH == kPair ? (tiles < clusters ? tiles : clusters) : (tiles + clusters - 1) / clusters;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(2 * np));
+    cfg.gridDim = dim3((unsigned)(csize * nc));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = L::kBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = (unsigned)csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -518,32 +666,65 @@ cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo 
                             cudaStream_t stream) {
     // Schedule with the smallest estimate of
     //   rounds x (64-k steps x step time + epi / 2) + epi / 2,
-    // rounds = tiles per SM (or SM pair) rounded up; the step times are measured
-    // on GB300 (128 x 128 on one SM 0.275 us and 128 x 256 0.45 us, both bound
-    // by operand delivery; 256 x 256 on an SM pair 0.33 us, bound by the MMA);
-    // epi = the time to drain one tile's accumulator, 1.5 us per 128 x 128 f32
-    // block of output per SM (twice that with an exp- or erf-based activation),
-    // about half of which overlaps the next tile's MMAs.
+    // rounds = tiles per SM (or SM pair, or cluster) rounded up; the step times
+    // are measured on GB300 (128 x 128 on one SM 0.275 us and 128 x 256 0.45 us,
+    // both bound by operand delivery; 256 x 256 on an SM pair 0.33 us, bound by
+    // the MMA); epi = the time to drain one tile's accumulator, 1.5 us per
+    // 128 x 128 f32 block of output per SM (twice that with an exp- or erf-based
+    // activation), about half of which overlaps the next tile's MMAs.  The helper
+    // schedule with h owners runs the owners' share of the steps of a 128 x 128
+    // tile plus about 1 us of hand-over, when all its clusters fit at once.
     const double ks = (double)((a.k + BK - 1) / BK);
     const double e = (a.flags & (kGelu | kSilu | kTanh)) ? 3.0 : 1.5;
     const long long rows = (a.n + BM - 1) / BM, rows2 = (a.n + 2 * BM - 1) / (2 * BM);
     const long long sm = dev.sm_count;
-    auto est = [&](long long tiles, long long units, double step, double epi) {
+    auto est = [&](long long tiles, long long units, double steps, double step, double epi) {
         const double rounds = (double)((tiles + units - 1) / units);
-        return rounds * (ks * step + 0.5 * epi) + 0.5 * epi;
+        return rounds * (steps * step + 0.5 * epi) + 0.5 * epi;
     };
-    const double t128 = est(rows * ((a.m + 127) / 128), sm, 0.275, e);
-    const double t256 = est(rows * ((a.m + 255) / 256), sm, 0.45, 2 * e);
+    const long long tiles128 = rows * ((a.m + 127) / 128);
+    const double t128 = est(tiles128, sm, ks, 0.275, e);
+    const double t256 = est(rows * ((a.m + 255) / 256), sm, ks, 0.45, 2 * e);
+    double best = t128 < t256 ? t128 : t256;
+    int pick = t128 < t256 ? 0 : 1;
+    using LP = PLayout<256, 1, kPair>;
+    using LH = PLayout<128, 2, kHelp>;
+    int pairs = 0;
     if (a.n > BM) {
-        using LP = PLayout<256, 1, true>;
-        const int pairs = max_pairs(gemm_tcp_kernel<256, 1, true>, (int)LP::kBytes, dev);
+        pairs = max_clusters(gemm_tcp_kernel<256, 1, kPair>, (int)LP::kBytes, 2, dev);
         if (pairs > 0) {
-            const double tp = est(rows2 * ((a.m + 255) / 256), pairs, 0.33, 2 * e);
-            if (tp < t128 && tp < t256) return launch_bn<256, 1, true>(a, xb, dev, stream, pairs);
+            const double tp = est(rows2 * ((a.m + 255) / 256), pairs, ks, 0.33, 2 * e);
+            if (tp < best) {
+                best = tp;
+                pick = 2;
+            }
         }
     }
-    if (t256 < t128) return launch_bn<256, 1, false>(a, xb, dev, stream);
-    return launch_bn<128, 2, false>(a, xb, dev, stream);
+    const long long kb128 = (a.k + 2 * BK - 1) / (2 * BK);  // 128-k stages
+    // The helper schedule parks partial sums in Y: only when Y is not the residual.
+    const size_t ybytes = (size_t)a.n * a.m * sizeof(float);
+    const uintptr_t y0 = (uintptr_t)a.Y, r0 = (uintptr_t)a.R;
+    const bool y_free = !(a.flags & kResidual) || r0 + ybytes <= y0 || y0 + ybytes <= r0;
+    int owners = 0;
+    for (int hh = 2; hh <= 3 && y_free && kb128 >= hh + 1 && tiles128 >= hh; ++hh) {
+        // Only when every cluster is resident at once (one round).
+        const int fit = max_clusters(gemm_tcp_kernel<128, 2, kHelp>, (int)LH::kBytes, hh + 1, dev);
+        const long long need = (tiles128 + hh - 1) / hh;
+        if (fit <= 0 || need > fit) continue;
+        const double steps = 2.0 * (double)help_split((int)kb128, hh);
+        const double th = est(need, need, steps, 0.275, e) + 1.0;
+        if (th < best) {
+            best = th;
+            pick = 3;
+            owners = hh;
+        }
+    }
+    switch (pick) {
+        case 1: return launch_bn<256, 1, kData>(a, xb, dev, stream);
+        case 2: return launch_bn<256, 1, kPair>(a, xb, dev, stream, pairs);
+        case 3: return launch_bn<128, 2, kHelp>(a, xb, dev, stream, owners);
+        default: return launch_bn<128, 2, kData>(a, xb, dev, stream);
+    }
 }
 
 }  // namespace wq

@@ -86,6 +86,54 @@ __device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
     return r;
 }
 
+// 16-byte store into the shared memory of a CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float x, float y, float z, float w) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(x), "f"(y),
+                 "f"(z), "f"(w)
+                 : "memory");
+}
+
+// Bulk copy from this CTA's shared memory into another CTA's of the cluster
+// (destination and barrier as shared::cluster addresses), counted on that
+// barrier; both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, const void *src,
+                                               uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+        " [%0], [%1], %2, [%3];" ::"r"(dst_cluster),
+        "r"(smem_addr(src)), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Complete `bytes` of expected transactions on a barrier of a CTA of the
+// cluster without a copy (a producer that will not deliver them).
+__device__ __forceinline__ void mbar_complete_tx_cluster(uint32_t bar_cluster, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;" ::"r"(
+                     bar_cluster),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy view of global memory with its
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
 // Every thread of every CTA in the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
