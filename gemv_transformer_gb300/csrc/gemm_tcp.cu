@@ -183,13 +183,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // TMEM: two accumulators of BN f32 columns x 128 lanes (a helper: one per
     // segment, up to three, in a power-of-two allocation).
-    const uint32_t ncols = helper ? 512u : (uint32_t)(2 * BN);
+    constexpr uint32_t kCols = 2 * BN <= 256 ? 256u : 512u;
+    const uint32_t ncols = helper ? 512u : kCols;
     if (warp == 2) {
         if (PAIR) {   // one warp of each CTA of the pair allocates collectively
             asm volatile(
                 "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                     smem_addr(tmem_slot)),
-                "r"(2 * BN)
+                "r"(ncols)
                 : "memory");
             asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
         } else {
@@ -325,7 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- epilogue
         const int ew = warp - kRoles;              // 0..15
         const int q = warp & 3;                    // TMEM lane quarter of this warp
-        constexpr int CW = BN / (kEpi / 4);        // columns per warp per tile
+        // A lane quarter's BN columns are 32-column blocks; warp cg of the quarter
+        // takes blocks cg, cg + 4, ... (BN = 192: two warps take two, two take one).
+        constexpr int NBQ = BN / 32;
+        constexpr int NB = (NBQ + 3) / 4;          // blocks per warp at most
         const int cg = ew >> 2;                    // which column group
         uint8_t *stg = sStg + ew * kStgBytes;
         uint32_t rphase = 0;
@@ -344,14 +348,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // cannot be served (an expired wait here) is told so: its abort flag
                 // is set before the signal.
                 const int r = t - h * unit;
-                const int hr = (t % RB) * BM + q * 32, hc = (t / RB) * BN + cg * CW;
+                const int hr = (t % RB) * BM + q * 32, hc = (t / RB) * BN + cg * 32;
                 // After a failure every later owner is declined too (each is signalled).
                 bool serve = !hfail && wait_or_abort(&tfull[b], 0u, abort_flag, limit, a.status);
                 serve = __all_sync(0xFFFFFFFFu, serve);
                 if (serve) {
                     tc_fence_after();
                     float v[32];
-                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + cg * CW),
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + cg * 32),
                               v);
                     if (stored) {
                         if (lane == 0) bulk_wait_read0();
@@ -382,17 +386,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
             const int i0 = (t % RB) * TM + (PAIR ? (int)rank * BM : 0);
-            const int j0 = (t / RB) * BN + cg * CW;
+            const int jt = (t / RB) * BN;          // the tile's first column
+            const int j0 = jt + cg * 32;           // this warp's first block
             const int r0 = i0 + q * 32;            // first row of this warp's blocks
-            constexpr int NB = CW / 32;            // 32-column blocks per warp per tile
             // Everything that does not need the accumulator is fetched while the
             // MMAs still run: this warp's bias values (lane c holds column c of
             // each block) and the first block's old Y (residual) by TMA.
             float bl[NB];
 #pragma unroll
             for (int u = 0; u < NB; ++u) {
-                const int jc = j0 + u * 32 + lane;
-                bl[u] = ((a.flags & kBias) && jc < a.m) ? __ldg(a.bias + jc) : 0.f;
+                const int jc = jt + (cg + 4 * u) * 32 + lane;
+                bl[u] = ((a.flags & kBias) && cg + 4 * u < NBQ && jc < a.m) ? __ldg(a.bias + jc)
+                                                                              : 0.f;
             }
             // The staging block is free once the previous store has read it.
             if (stored) {
@@ -443,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int u = 0; u < NB; ++u) {
-                if (!ok) break;
-                const int jb = j0 + u * 32;
+                if (!ok || cg + 4 * u >= NBQ) break;
+                const int jb = jt + (cg + 4 * u) * 32;
                 if (u > 0) {
                     if (lane == 0) bulk_wait_read0();
                     __syncwarp();
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 float v[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) +
-                              (uint32_t)(b * BN + cg * CW + u * 32),
+                              (uint32_t)(b * BN + (cg + 4 * u) * 32),
                           v);
                 if (HELP) {  // + the helper's part: k stages [ks, KB) after [0, ks)
                     const uint8_t *pp = sA + ew * kStgBytes + lane * 128;
@@ -533,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (PAIR)
             asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                         "r"(2 * BN)
+                         "r"(ncols)
                          : "memory");
         else
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -669,7 +674,7 @@ cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo 
     // rounds = tiles per SM (or SM pair, or cluster) rounded up; the step times
     // are measured on GB300 (128 x 128 on one SM 0.275 us and 128 x 256 0.45 us,
     // both bound by operand delivery; 256 x 256 on an SM pair 0.33 us, bound by
-    // the MMA); epi = the time to drain one tile's accumulator, 1.5 us per
+    // the MMA, and 256 x 192 taken as three quarters of that); epi = the time to drain one tile's accumulator, 1.5 us per
     // 128 x 128 f32 block of output per SM (twice that with an exp- or erf-based
     // activation), about half of which overlaps the next tile's MMAs.  The helper
     // schedule with h owners runs the owners' share of the steps of a 128 x 128
@@ -693,10 +698,20 @@ cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo 
     if (a.n > BM) {
         pairs = max_clusters(gemm_tcp_kernel<256, 1, kPair>, (int)LP::kBytes, 2, dev);
         if (pairs > 0) {
-            const double tp = est(rows2 * ((a.m + 255) / 256), pairs, ks, 0.33, 2 * e);
+            // An exp- or erf-based epilogue competes with the pair's MMA-bound
+            // mainloop more than with a one-SM tile's operand-bound one (measured
+            // on the encoder up projection): charge it twice.
+            const double pe = (a.flags & (kGelu | kSilu | kTanh)) ? 2.0 * e : e;
+            const double tp = est(rows2 * ((a.m + 255) / 256), pairs, ks, 0.33, 2 * pe);
             if (tp < best) {
                 best = tp;
                 pick = 2;
+            }
+            // 256 x 192 pair tiles: three quarters of the MMA work per step.
+            const double tq = est(rows2 * ((a.m + 191) / 192), pairs, ks, 0.25, 1.5 * pe);
+            if (tq < best) {
+                best = tq;
+                pick = 4;
             }
         }
     }
@@ -723,6 +738,7 @@ cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo 
         case 1: return launch_bn<256, 1, kData>(a, xb, dev, stream);
         case 2: return launch_bn<256, 1, kPair>(a, xb, dev, stream, pairs);
         case 3: return launch_bn<128, 2, kHelp>(a, xb, dev, stream, owners);
+        case 4: return launch_bn<192, 1, kPair>(a, xb, dev, stream, pairs);
         default: return launch_bn<128, 2, kData>(a, xb, dev, stream);
     }
 }

@@ -99,6 +99,32 @@ def test_tc_residual_in_place_ragged_m(oracle_mod, ws):
     check_tc(oracle_mod, 150, 203, 264, BIAS | RES, seed=3, inplace=True, ws=ws)
 
 
+@pytest.mark.parametrize("cols", [(0, 300), (3700, 4000)])
+def test_tc_pair_schedule_192_wide_ragged(oracle_mod, cols):
+    """256 x 192 SM-pair tiles (chosen when 256-wide tiles would need as many
+    rounds): ragged rows (1500), columns (4000 = 20 x 192 + 160) and k (520)."""
+    check_tc(oracle_mod, 1500, 4000, 520, BIAS | RES, seed=19, ws=True, rows=cols)
+
+
+@pytest.mark.parametrize("inplace", [False, True], ids=["separate", "in-place"])
+def test_tc_helper_schedule_residual(oracle_mod, inplace):
+    """A shape with fewer 128 x 128 tiles than SMs and a long k (the helper-cluster
+    schedule, which parks partial sums in Y): with a separate residual it runs
+    that schedule; with Y as the residual it must take another (Y holds old
+    values the epilogue still reads), and both are correct."""
+    check_tc(oracle_mod, 700, 1000, 2048, BIAS | RES, seed=11, inplace=inplace, ws=True,
+             rows=(0, 300))
+
+
+@pytest.mark.parametrize("shape,flags", [((600, 1100, 2048), BIAS | GELU), ((1280, 1280, 2056), BIAS)])
+def test_tc_helper_schedule_odd_tiles(oracle_mod, shape, flags):
+    """Helper clusters whose last cluster has fewer tiles than owners (45 tiles for
+    two owners per cluster, 100 for three: idle owners and a helper with fewer
+    segments), with ragged rows and columns and, in the second, a ragged k."""
+    n, m, k = shape
+    check_tc(oracle_mod, n, m, k, flags, seed=n + 5, ws=True, rows=(0, 260))
+
+
 @pytest.mark.parametrize("shape", [(1000, 1000, 512), (257, 300, 200), (1400, 3000, 264)])
 def test_tc_workspace_path_bit_identical(shape):
     """Both tensor-core paths round X the same way and accumulate in the same
