@@ -12,7 +12,7 @@ Parity pins: every function is pinned by the ``not gpu`` tests in
 ``tests/test_oracle.py`` (hand-worked blocks, exhaustive comparisons against
 numpy/torch format conversions, identity and one-hot weights, the wavo probe's
 closed form, exact integer brute force, erf-GELU closed forms, MoE routing
-closed forms).
+closed forms, embedding gathers from tables with closed-form rows).
 """
 from __future__ import annotations
 
@@ -72,6 +72,8 @@ def _load():
             lib.oracle_moe.restype = ci
             lib.oracle_layer_norm.argtypes = [ci, ci, vp, vp, vp]
             lib.oracle_layer_norm.restype = ci
+            lib.oracle_embed.argtypes = [ci, ci, ci, ci, vp, vp, vp, vp, vp, vp]
+            lib.oracle_embed.restype = ci
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ci
             _lib = lib
@@ -167,3 +169,19 @@ def moe(n_tok, topk, n_experts, m, k, wtype, flags, X, Wbank, ids, bias=None, re
     if rc != 0:
         raise ValueError("oracle_moe: bad arguments")
     return Y, S
+
+
+def embed(n_ids, rows, k, wtype, W, ids, pos=None, bias=None, init=None):
+    """f64 ``(out [n_ids][k], valid [n_ids])``: row ``ids[t]`` of the table ``W``
+    (``rows`` x ``k``) + ``pos[t]`` + ``bias``.  Rows of invalid ids keep ``init``
+    (NaN when not given)."""
+    Wc, ic = _c(W, np.uint8), _c(ids, np.int32)
+    pc, bc = _c(pos, np.float32), _c(bias, np.float32)
+    out = (np.full((n_ids, k), np.nan, dtype=np.float64) if init is None
+           else np.array(init, dtype=np.float64).reshape(n_ids, k).copy())
+    valid = np.zeros(n_ids, dtype=np.int32)
+    rc = _load().oracle_embed(n_ids, rows, k, wtype, _ptr(Wc), _ptr(ic), _ptr(pc), _ptr(bc),
+                              _ptr(out), _ptr(valid))
+    if rc != 0:
+        raise ValueError("oracle_embed: bad arguments")
+    return out, valid.astype(bool)

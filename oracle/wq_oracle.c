@@ -287,3 +287,35 @@ int oracle_layer_norm(int n, int k, const float *X, const float *gb, double *Y) 
     }
     return 0;
 }
+
+/*
+ * Embedding row gather, wavo 0.3.0 src/gpu/mod.rs, Recorder::embed (and its test
+ * gemv_and_embed): row ids[t] of the weight table W (rows x k, any weight format),
+ * dequantised, plus the positional values pos[t][j] and the table's bias[j] for
+ * the k columns j, added in that order:
+ *   out[t][j] = W[ids[t]][j] + pos[t][j] + bias[j]     (pos / bias optional).
+ * f64.  An id outside [0, rows) leaves its row of out as it was and clears
+ * valid[t]; valid[t] = 1 otherwise.  Returns 0, or -1 on a bad shape/type.
+ */
+int oracle_embed(int n_ids, int rows, int k, int wtype, const uint8_t *W, const int32_t *ids,
+                 const float *pos, const float *bias, double *out, int *valid) {
+    if (n_ids < 0 || rows <= 0 || !shape_ok(wtype, rows, k) || !W || !ids || !out || !valid)
+        return -1;
+    size_t rb = row_bytes(wtype, k);
+    double *w = (double *)malloc(sizeof(double) * (size_t)k);
+    if (!w) return -1;
+    for (int t = 0; t < n_ids; ++t) {
+        const int id = ids[t];
+        valid[t] = id >= 0 && id < rows;
+        if (!valid[t]) continue;
+        dequant_row(wtype, W + rb * (size_t)id, k, w);
+        for (int j = 0; j < k; ++j) {
+            double v = w[j];
+            if (pos) v += (double)pos[(size_t)t * k + j];
+            if (bias) v += (double)bias[j];
+            out[(size_t)t * k + j] = v;
+        }
+    }
+    free(w);
+    return 0;
+}

@@ -444,3 +444,60 @@ def test_synth_ids_distinct_and_in_range():
     ids = synth.moe_ids(synth.rng(5), 16, 6, 64)
     assert ids.shape == (16, 6) and ids.min() >= 0 and ids.max() < 64
     assert all(len(set(row)) == 6 for row in ids.tolist())
+
+
+# ------------------------------------------------------- embedding row gather --
+# wavo 0.3.0 src/gpu/mod.rs, Recorder::embed: out = W[id] + pos + bias.  Closed
+# forms: tables whose row r holds a value that depends only on r (and on the
+# column), so the gathered rows, and their sums with pos and bias, are known
+# without dequantising anything.
+
+def _embed_tables(rows, k):
+    """One table per format whose element (r, j) is known in closed form."""
+    r = np.arange(rows)[:, None] * np.ones((1, k))
+    j = np.ones((rows, 1)) * (np.arange(k)[None, :] % 4)
+    v_bf16 = r + j                                  # small integers: exact in bf16
+    bf = synth.bf16_pairs(synth.bf16_bits_rne(v_bf16.astype(np.float32)))
+    # Q8_0: d = 1, q = (r % 100) - 50 + j  ->  value q
+    q8 = ((r % 100) - 50 + j).astype(np.int8)
+    img8 = synth.encode_q8_0(np.full((rows, k // 32), synth.f16_bits(1.0)[()], np.uint16), q8)
+    # Q4_0: d = 0.5, code = 8 + (r % 8) - j  ->  value 0.5 * ((r % 8) - j)
+    c4 = (8 + (r % 8) - j).astype(np.uint8)
+    img4 = synth.encode_q4_0(np.full((rows, k // 32), synth.f16_bits(0.5)[()], np.uint16), c4)
+    return {BF16: (bf, v_bf16), Q8_0: (img8, q8.astype(np.float64)),
+            Q4_0: (img4, 0.5 * ((r % 8) - j))}
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+def test_embed_gathers_rows_in_closed_form(oracle_mod, wtype):
+    rows, k = 120, 96
+    img, value = _embed_tables(rows, k)[wtype]
+    ids = np.array([7, 0, 119, 7, 63], np.int32)
+    out, valid = oracle_mod.embed(len(ids), rows, k, wtype, img, ids)
+    assert valid.all()
+    assert (out == value[ids]).all()
+
+
+def test_embed_adds_pos_then_bias(oracle_mod):
+    """The page's test picks id 1 of [5, 7] with the second position row of pos and
+    the first k bias values; here with integers, so every sum is exact."""
+    rows, k = 100, 64
+    img, value = _embed_tables(rows, k)[BF16]
+    pos_tab = np.arange(2 * k, dtype=np.float32) * 3.0      # two position rows
+    bias = -np.arange(rows, dtype=np.float32)              # the table's bias (rows values)
+    ids = np.array([5, 7], np.int32)
+    out, valid = oracle_mod.embed(1, rows, k, BF16, img, ids[1:], pos=pos_tab[k:2 * k],
+                                  bias=bias[:k])
+    want = value[7] + 3.0 * np.arange(k, 2 * k) - np.arange(k)
+    assert valid.all() and (out[0] == want).all()
+
+
+def test_embed_leaves_rows_of_bad_ids(oracle_mod):
+    rows, k = 10, 32
+    img, value = _embed_tables(rows, k)[Q4_0]
+    ids = np.array([3, -1, 10, 9], np.int32)
+    init = np.full((4, k), 42.0)
+    out, valid = oracle_mod.embed(4, rows, k, Q4_0, img, ids, init=init)
+    assert valid.tolist() == [True, False, False, True]
+    assert (out[1] == 42.0).all() and (out[2] == 42.0).all()
+    assert (out[0] == value[3]).all() and (out[3] == value[9]).all()
