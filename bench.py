@@ -85,11 +85,14 @@ def make_workloads():
 
 def extra_workloads():
     """Measured and reported beside the metric, not part of it: the quantised
-    large-n tensor-core GEMM (a prompt through GGML weights)."""
+    large-n tensor-core GEMM (a prompt through GGML weights), the LayerNorm fused
+    before the encoder qkv projection, and the token-embedding gather."""
     import synth
     return [synth.workload_quant_prefill(wtype=synth.WTYPE_Q4_0),
             synth.workload_quant_prefill(wtype=synth.WTYPE_Q8_0),
-            synth.workload_ln_qkv()]
+            synth.workload_ln_qkv(),
+            synth.workload_embed(wtype=synth.WTYPE_BF16),
+            synth.workload_embed(wtype=synth.WTYPE_Q4_0)]
 
 
 def algorithmic(w):
@@ -103,6 +106,9 @@ def algorithmic(w):
         touched = len(set(w["ids"].reshape(-1).tolist()))
         b = touched * m * rb + w["n_tok"] * k * 4 + slots * m * 4 + slots * 4
         return b, 2.0 * slots * m * k
+    if w["kind"] == "embed":  # the gathered table rows + pos + bias + out + ids
+        n = w["n"]
+        return n * rb + n * k * 4 + k * 4 + n * k * 4 + n * 4, 0.0
     n = w["n"]
     b = m * rb + n * k * 4 + n * m * 4
     if w["flags"] & synth.FLAG_BIAS:
@@ -331,10 +337,14 @@ class Launches:
         # with a single copy.
         def nbytes(a):
             return 0 if a is None else (np.asarray(a).nbytes + 255) // 256 * 256
+        def out_count(w):
+            if w["kind"] == "moe":
+                return w["n_tok"] * w["topk"] * w["m"]
+            return w["n"] * (w["k"] if w["kind"] == "embed" else w["m"])
+
         in_total = sum(nbytes(w["X"]) + nbytes(w["residual"]) +
-                       (nbytes(w["ids"]) if w["kind"] == "moe" else 0) for w in ws)
-        out_total = sum(((w["n_tok"] * w["topk"] if w["kind"] == "moe" else w["n"]) * w["m"] * 4
-                         + 255) // 256 * 256 for w in ws)
+                       (nbytes(w["ids"]) if w["kind"] in ("moe", "embed") else 0) for w in ws)
+        out_total = sum((out_count(w) * 4 + 255) // 256 * 256 for w in ws)
         self.inputs = torch.empty(in_total, dtype=torch.uint8, device=device)
         self.outputs = torch.empty(out_total, dtype=torch.uint8, device=device)
         cursor = {"in": 0, "out": 0}
@@ -363,12 +373,12 @@ class Launches:
             flat = np.ascontiguousarray(w["W"]).reshape(-1)
             img[:flat.size] = flat
             b["W"] = torch.from_numpy(img).to(device)
-            b["X"] = place(self.inputs, "in", w["X"])
-            nout = (w["n_tok"] * w["topk"] if w["kind"] == "moe" else w["n"]) * m
-            b["Y"] = place(self.outputs, "out", count=nout, dtype=torch.float32)
+            b["X"] = place(self.inputs, "in", w["X"])   # embed: the position rows
+            b["Y"] = place(self.outputs, "out", count=out_count(w), dtype=torch.float32)
             b["bias"] = torch.from_numpy(w["bias"]).to(device) if w["bias"] is not None else None
             b["R"] = place(self.inputs, "in", w["residual"]) if w["residual"] is not None else None
-            b["ids"] = place(self.inputs, "in", w["ids"]) if w["kind"] == "moe" else None
+            b["ids"] = (place(self.inputs, "in", w["ids"]) if w["kind"] in ("moe", "embed")
+                        else None)
             b["ws"] = None
             b["ln_gb"] = torch.from_numpy(w["ln_gb"]).to(device) if "ln_gb" in w else None
             if w["kind"] == "gemm_ln_tc":
@@ -384,6 +394,9 @@ class Launches:
 
     def call(self, i, stream=None):
         w, b, wq = self.ws[i], self.bufs[i], self.wq
+        if w["kind"] == "embed":
+            return wq.wq_embed(w["n"], w["m"], w["k"], w["wtype"], b["W"], b["ids"], b["X"],
+                               b["bias"], b["Y"], stream)
         if w["kind"] == "moe":
             return wq.wq_moe_gemv(w["n_tok"], w["topk"], w["n_experts"], w["m"], w["k"],
                                   w["wtype"], w["flags"], b["X"], b["W"], b["ids"], b["bias"],
@@ -581,8 +594,9 @@ def run_gpu(args):
             t = x0.elapsed_time(x1) * 1e3 / reps
             b, f = algorithmic(w)
             r_us, bound = roofline_us(w, peaks)
-            extra.append({"name": w["name"], "us": round(t, 3), "TFLOP_s": round(f / t / 1e6, 2),
-                          "bound": bound, "roofline_pct": round(r_us / t * 100, 1),
+            extra.append({"name": w["name"], "us": round(t, 3), "GB_s": round(b / t / 1e3, 1),
+                          "TFLOP_s": round(f / t / 1e6, 2), "bound": bound,
+                          "roofline_pct": round(r_us / t * 100, 1),
                           "kernels_per_call": kernels_per_call(w)})
             del lset
 

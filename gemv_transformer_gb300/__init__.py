@@ -22,15 +22,15 @@ WQ_BF16, WQ_Q8_0, WQ_Q4_0 = 0, 1, 2
 WQ_BIAS, WQ_GELU, WQ_RESIDUAL, WQ_TC_BF16 = 1, 2, 4, 256
 WQ_SILU, WQ_RELU, WQ_TANH = 8, 16, 32
 WQ_OK, WQ_ERR_INVALID_ARG, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA = 0, 1, 2, 3
-WQ_ERR_DEVICE_TIMEOUT, WQ_ERR_BAD_EXPERT, WQ_ERR_TOO_LARGE = 4, 5, 6
+WQ_ERR_DEVICE_TIMEOUT, WQ_ERR_BAD_EXPERT, WQ_ERR_TOO_LARGE, WQ_ERR_BAD_INDEX = 4, 5, 6, 7
 WQ_GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20
 WQ_GEMV_MAX_N = 16
 WQ_MOE_MAX_SLOTS = 256
 
 EXPORTS = ("wq_gemm", "wq_gemm_ws", "wq_gemm_workspace_bytes", "wq_gemm_noalloc",
            "wq_gemm_ln_ws", "wq_gemm_ln_workspace_bytes", "wq_gemv",
-           "wq_moe_gemv", "wq_weight_bytes", "wq_dequantize", "wq_get_device_status", "wq_status_string",
-           "wq_set_wait_limit")
+           "wq_moe_gemv", "wq_weight_bytes", "wq_dequantize", "wq_embed", "wq_get_device_status",
+           "wq_status_string", "wq_set_wait_limit")
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,8 @@ def _open(path: str):
     lib.wq_weight_bytes.restype = sz
     lib.wq_dequantize.argtypes = [ci, ci, ci, vp, vp, vp]
     lib.wq_dequantize.restype = ci
+    lib.wq_embed.argtypes = [ci, ci, ci, ci, vp, vp, vp, vp, vp, vp]
+    lib.wq_embed.restype = ci
     lib.wq_get_device_status.argtypes = [vp]
     lib.wq_get_device_status.restype = ci
     lib.wq_status_string.argtypes = [ci]
@@ -155,6 +157,11 @@ def wq_weight_bytes(wtype, m, k) -> int:
 
 def wq_dequantize(wtype, m, k, W, out, stream=None) -> int:
     return load().wq_dequantize(wtype, m, k, _p(W), _p(out), _s(stream))
+
+
+def wq_embed(n_ids, rows, k, wtype, W, ids, pos=None, bias=None, out=None, stream=None) -> int:
+    return load().wq_embed(n_ids, rows, k, wtype, _p(W), _p(ids), _p(pos), _p(bias), _p(out),
+                           _s(stream))
 
 
 def wq_get_device_status(stream=None) -> int:

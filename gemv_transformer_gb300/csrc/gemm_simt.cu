@@ -253,6 +253,31 @@ cudaError_t launch_splitk_wt(const GemmArgs &a, int tiles_m, int tiles_n, int ks
     return cudaLaunchKernelEx(&cfg, gemm_splitk_kernel<WT>, a, spr);
 }
 
+// Eight consecutive weights t0..t0+7 (t0 % 8 == 0) of one W row, exact in f32.
+template <int WT>
+__device__ __forceinline__ void decode8(const uint8_t *row, int t0, float (&w)[8]) {
+    if (WT == kBF16) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(row + (size_t)2 * t0);
+        w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x);
+        w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+        w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z);
+        w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
+    } else if (WT == kQ8_0) {
+        const uint8_t *bp = row + (size_t)34 * (t0 / 32);
+        const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+        for (int e = 0; e < 8; ++e) w[e] = d * (float)(int8_t)bp[2 + (t0 & 31) + e];
+    } else {
+        const uint8_t *bp = row + (size_t)18 * (t0 / 32);
+        const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+        for (int e = 0; e < 8; ++e) {
+            const int t = (t0 & 31) + e;
+            const uint32_t byte = bp[2 + (t & 15)];
+            const int code = (t < 16) ? (int)(byte & 15u) : (int)(byte >> 4);
+            w[e] = d * (float)(code - 8);
+        }
+    }
+}
+
 template <int WT>
 __global__ void dequant_kernel(int m, int k, const uint8_t *W, float *out) {
     pdl_enter();
@@ -263,30 +288,67 @@ __global__ void dequant_kernel(int m, int k, const uint8_t *W, float *out) {
          u += (long long)gridDim.x * blockDim.x) {
         const int j = (int)(u / (k / 8));
         const int t0 = (int)(u % (k / 8)) * 8;
-        const uint8_t *row = W + (size_t)j * rb;
         float w[8];
-        if (WT == kBF16) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(row + (size_t)2 * t0);
-            w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x);
-            w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
-            w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z);
-            w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
-        } else if (WT == kQ8_0) {
-            const uint8_t *bp = row + (size_t)34 * (t0 / 32);
-            const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
-            for (int e = 0; e < 8; ++e) w[e] = d * (float)(int8_t)bp[2 + (t0 & 31) + e];
-        } else {
-            const uint8_t *bp = row + (size_t)18 * (t0 / 32);
-            const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
-            for (int e = 0; e < 8; ++e) {
-                const int t = (t0 & 31) + e;
-                const uint32_t byte = bp[2 + (t & 15)];
-                const int code = (t < 16) ? (int)(byte & 15u) : (int)(byte >> 4);
-                w[e] = d * (float)(code - 8);
-            }
-        }
+        decode8<WT>(W + (size_t)j * rb, t0, w);
         float *o = out + (size_t)j * k + t0;
         for (int e = 0; e < 8; ++e) o[e] = w[e];
+    }
+}
+
+// Embedding row gather (wavo 0.3.0 src/gpu/mod.rs, Recorder::embed):
+// out[t][j] = W[ids[t]][j] + pos[t][j] + bias[j], in that order, f32.  One thread
+// per 8 values (with VEC, pos, bias and out are 16-byte aligned and moved as
+// float4); an id outside [0, rows) leaves its row unwritten and records the
+// bad-index status (once, by the row's first thread).
+template <int WT, bool VEC>
+__global__ void embed_kernel(int n_ids, int rows, int k, const uint8_t *W, const int32_t *ids,
+                             const float *pos, const float *bias, float *out, unsigned *status) {
+    pdl_enter();
+    const long long units = (long long)n_ids * (k / 8);
+    const size_t rb = row_bytes(WT, k);
+    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < units;
+         u += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(u / (k / 8));
+        const int t0 = (int)(u % (k / 8)) * 8;
+        const int id = ids[t];
+        if (id < 0 || id >= rows) {
+            if (t0 == 0) record_status(status, kStBadIndex);
+            continue;
+        }
+        float w[8];
+        decode8<WT>(W + (size_t)id * rb, t0, w);
+        float *o = out + (size_t)t * k + t0;
+        const float *p = pos ? pos + (size_t)t * k + t0 : nullptr;
+        if (VEC) {
+            float pv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (p) {
+                const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+                const float4 c = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+                pv[0] = a.x; pv[1] = a.y; pv[2] = a.z; pv[3] = a.w;
+                pv[4] = c.x; pv[5] = c.y; pv[6] = c.z; pv[7] = c.w;
+            }
+            if (bias) {
+                const float4 a = __ldg(reinterpret_cast<const float4 *>(bias + t0));
+                const float4 c = __ldg(reinterpret_cast<const float4 *>(bias + t0) + 1);
+                bv[0] = a.x; bv[1] = a.y; bv[2] = a.z; bv[3] = a.w;
+                bv[4] = c.x; bv[5] = c.y; bv[6] = c.z; bv[7] = c.w;
+            }
+            float v[8];
+            for (int e = 0; e < 8; ++e) {
+                v[e] = w[e];
+                if (p) v[e] += pv[e];
+                if (bias) v[e] += bv[e];
+            }
+            reinterpret_cast<float4 *>(o)[0] = make_float4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<float4 *>(o)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        } else {
+            for (int e = 0; e < 8; ++e) {
+                float v = w[e];
+                if (p) v += p[e];
+                if (bias) v += bias[t0 + e];
+                o[e] = v;
+            }
+        }
     }
 }
 
@@ -331,6 +393,26 @@ cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out
     case kBF16: return launch_pdl(dequant_kernel<kBF16>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
     case kQ8_0: return launch_pdl(dequant_kernel<kQ8_0>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
     default: return launch_pdl(dequant_kernel<kQ4_0>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
+    }
+}
+
+cudaError_t launch_embed(int n_ids, int rows, int k, int wtype, const uint8_t *W,
+                         const int32_t *ids, const float *pos, const float *bias, float *out,
+                         const DeviceInfo &dev, cudaStream_t stream) {
+    const long long units = (long long)n_ids * (k / 8);
+    long long blocks = (units + 255) / 256;
+    const long long cap = (long long)dev.sm_count * 8;
+    if (blocks > cap) blocks = cap;
+    auto a16 = [](const void *q) { return ((uintptr_t)q & 15u) == 0; };
+    const bool vec = a16(out) && (!pos || a16(pos)) && (!bias || a16(bias));
+    auto go = [&](auto kern) {
+        return launch_pdl(kern, dim3((unsigned)blocks), dim3(256), 0, stream, n_ids, rows, k, W,
+                          ids, pos, bias, out, dev.status);
+    };
+    switch (wtype) {
+    case kBF16: return vec ? go(embed_kernel<kBF16, true>) : go(embed_kernel<kBF16, false>);
+    case kQ8_0: return vec ? go(embed_kernel<kQ8_0, true>) : go(embed_kernel<kQ8_0, false>);
+    default: return vec ? go(embed_kernel<kQ4_0, true>) : go(embed_kernel<kQ4_0, false>);
     }
 }
 

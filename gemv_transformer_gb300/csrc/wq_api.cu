@@ -261,6 +261,16 @@ wq_status wq_dequantize(int wtype, int m, int k, const void *W, float *out, wq_s
         launch_dequant(wtype, m, k, static_cast<const uint8_t *>(W), out, (cudaStream_t)stream));
 }
 
+wq_status wq_embed(int n_ids, int rows, int k, int wtype, const void *W, const int32_t *ids,
+                   const float *pos, const float *bias, float *out, wq_stream_t stream) {
+    if (n_ids <= 0 || !shape_ok(wtype, rows, k) || !W || !ids || !out || !aligned16(W))
+        return WQ_ERR_INVALID_ARG;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return WQ_ERR_CUDA;
+    return cuda_status(launch_embed(n_ids, rows, k, wtype, static_cast<const uint8_t *>(W), ids,
+                                    pos, bias, out, *dev, (cudaStream_t)stream));
+}
+
 wq_status wq_get_device_status(wq_stream_t stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return WQ_ERR_CUDA;
     unsigned v = 0;
@@ -280,6 +290,7 @@ const char *wq_status_string(int status) {
     case WQ_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case WQ_ERR_BAD_EXPERT: return "expert id out of range";
     case WQ_ERR_TOO_LARGE: return "request exceeds the fixed scratch size";
+    case WQ_ERR_BAD_INDEX: return "embedding row id out of range";
     default: return "unknown status";
     }
 }

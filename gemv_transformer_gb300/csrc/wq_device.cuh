@@ -20,7 +20,7 @@ namespace wq {
 enum WType : int { kBF16 = 0, kQ8_0 = 1, kQ4_0 = 2 };
 enum Flag : unsigned { kBias = 1u, kGelu = 2u, kResidual = 4u, kSilu = 8u, kRelu = 16u, kTanh = 32u };
 constexpr unsigned kActs = kGelu | kSilu | kRelu | kTanh;  // at most one per call
-enum DevStatus : unsigned { kStTimeout = 4u, kStBadExpert = 5u };
+enum DevStatus : unsigned { kStTimeout = 4u, kStBadExpert = 5u, kStBadIndex = 7u };
 
 // Bytes of one row of k weights in each format.
 __host__ __device__ __forceinline__ size_t row_bytes(int wt, int k) {

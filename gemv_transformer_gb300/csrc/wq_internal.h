@@ -108,5 +108,8 @@ cudaError_t launch_layer_norm(const float *X, const float *gb, int n, int k, voi
                               bool bf16_out, const DeviceInfo &dev, cudaStream_t stream);
 cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out,
                            cudaStream_t stream);
+cudaError_t launch_embed(int n_ids, int rows, int k, int wtype, const uint8_t *W,
+                         const int32_t *ids, const float *pos, const float *bias, float *out,
+                         const DeviceInfo &dev, cudaStream_t stream);
 
 }  // namespace wq

@@ -19,6 +19,9 @@
  *     W[ids[s], r, k] * x[s, k]" over one bank [E, rows, k], router gather and
  *     expert matvec in one dispatch).
  *   - wq_dequantize: the block formats themselves (same pages).
+ *   - wq_embed: wavo 0.3.0, src/gpu/mod.rs, Recorder::embed ("row ids[i] of the
+ *     table + pos[offset..] + the table's bias, k values") and its test
+ *     gemv_and_embed.
  *   - wq_get_device_status: wavo 0.3.0, Gpu "failure" (the first device error is
  *     reported by the next call) and its completion marks.
  *
@@ -106,7 +109,8 @@ typedef enum {
     WQ_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
     WQ_ERR_DEVICE_TIMEOUT = 4, /* a kernel's bounded wait ran out (device status) */
     WQ_ERR_BAD_EXPERT = 5,     /* an expert id outside [0, n_experts) (device status) */
-    WQ_ERR_TOO_LARGE = 6       /* wq_gemm_noalloc: the call needs more than its fixed scratch */
+    WQ_ERR_TOO_LARGE = 6,      /* wq_gemm_noalloc: the call needs more than its fixed scratch */
+    WQ_ERR_BAD_INDEX = 7       /* wq_embed: a row id outside [0, rows) (device status) */
 } wq_status;
 
 /* Largest n that wq_gemv accepts. */
@@ -245,9 +249,25 @@ WQ_API size_t wq_weight_bytes(int wtype, int m, int k);
  * are exact in f32).  Same W contract as wq_gemm.  Asynchronous on `stream`. */
 WQ_API wq_status wq_dequantize(int wtype, int m, int k, const void *W, float *out, wq_stream_t stream);
 
+/* Embedding row gather: for t < n_ids and j < k,
+ *   out[t][j] = W[ids[t]][j] + pos[t][j] + bias[j]
+ * (f32; the dequantised weight, exact in f32, then + pos, then + bias).
+ * W: a table of `rows` rows of k weights in format wtype, same contract as
+ *    wq_gemm (16-byte aligned; k % 8 == 0 for bf16, k % 32 == 0 for Q8_0/Q4_0).
+ * ids: int32 [n_ids].  An id outside [0, rows) leaves row t of out unwritten and
+ *    records WQ_ERR_BAD_INDEX in the device status.
+ * pos: f32 [n_ids][k] (the page's position rows, one per id) or NULL;
+ * bias: f32 [k] or NULL; out: f32 [n_ids][k].
+ * Errors: WQ_ERR_INVALID_ARG for n_ids <= 0, rows <= 0, a bad k or wtype, null
+ * W, ids or out, W not 16-byte aligned.  Asynchronous on `stream`. */
+WQ_API wq_status wq_embed(int n_ids, int rows, int k, int wtype, const void *W,
+                          const int32_t *ids, const float *pos, const float *bias, float *out,
+                          wq_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the current device's sticky
- * status word: WQ_OK, WQ_ERR_DEVICE_TIMEOUT or WQ_ERR_BAD_EXPERT (the first
- * recorded since the last call); WQ_ERR_CUDA if the synchronisation fails. */
+ * status word: WQ_OK, WQ_ERR_DEVICE_TIMEOUT, WQ_ERR_BAD_EXPERT or
+ * WQ_ERR_BAD_INDEX (the first recorded since the last call); WQ_ERR_CUDA if the
+ * synchronisation fails. */
 WQ_API wq_status wq_get_device_status(wq_stream_t stream);
 
 /* Static English text for a status code. */

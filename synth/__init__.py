@@ -250,3 +250,16 @@ def workload_ln_qkv(seed=7, n=1500, d=1024):
                                       normal_f32(g, (d,), 0.1)]),
                 W=draw_bf16_weights(g, 3 * d, d, 0.03), bias=normal_f32(g, (3 * d,), 0.1),
                 residual=None)
+
+
+def workload_embed(seed=8, wtype=WTYPE_BF16, rows=32000, k=4096, n_ids=512):
+    """The token embedding of a 512-token prompt: rows ids[t] drawn uniformly from
+    a vocabulary table (32,000 x 4,096, the table's format as for the weights
+    above), plus one position row per token (N(0,1)) and the table's bias
+    (N(0, 0.1))."""
+    g = rng(seed * 10 + wtype)
+    tag = {WTYPE_BF16: "bf16", WTYPE_Q8_0: "q8_0", WTYPE_Q4_0: "q4_0"}[wtype]
+    return dict(name=f"embed_{tag}_V{rows}_k{k}_n{n_ids}", kind="embed", wtype=wtype, n=n_ids,
+                m=rows, k=k, flags=FLAG_BIAS, W=draw_weights(g, wtype, rows, k),
+                ids=g.integers(0, rows, size=n_ids).astype(np.int32),
+                X=normal_f32(g, (n_ids, k)), bias=normal_f32(g, (k,), 0.1), residual=None)

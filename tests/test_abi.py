@@ -44,7 +44,7 @@ def test_weight_bytes():
 
 
 def test_status_strings():
-    for code in range(7):
+    for code in range(8):
         assert wq.wq_status_string(code) != "unknown status"
     assert wq.wq_status_string(99) == "unknown status"
 
@@ -77,6 +77,15 @@ A = 0x10000  # a 16-byte aligned fake device address: never dereferenced below
     lambda: wq.wq_moe_gemv(2, 2, 4, 8, 32, wq.WQ_Q4_0, 0, A, A, None, None, None, A, 0),
     lambda: wq.wq_moe_gemv(2, 2, 4, 8, 32, wq.WQ_Q4_0, wq.WQ_TC_BF16, A, A, A, None, None, A, 0),
     lambda: wq.wq_dequantize(wq.WQ_Q8_0, 4, 40, A, A, 0),
+    lambda: wq.wq_embed(0, 8, 32, wq.WQ_Q8_0, A, A, None, None, A, 0),
+    lambda: wq.wq_embed(2, 0, 32, wq.WQ_Q8_0, A, A, None, None, A, 0),
+    lambda: wq.wq_embed(2, 8, 40, wq.WQ_Q4_0, A, A, None, None, A, 0),
+    lambda: wq.wq_embed(2, 8, 12, wq.WQ_BF16, A, A, None, None, A, 0),
+    lambda: wq.wq_embed(2, 8, 32, 3, A, A, None, None, A, 0),
+    lambda: wq.wq_embed(2, 8, 32, wq.WQ_Q8_0, None, A, None, None, A, 0),
+    lambda: wq.wq_embed(2, 8, 32, wq.WQ_Q8_0, A, None, None, None, A, 0),
+    lambda: wq.wq_embed(2, 8, 32, wq.WQ_Q8_0, A, A, None, None, None, 0),
+    lambda: wq.wq_embed(2, 8, 32, wq.WQ_Q8_0, A + 2, A, None, None, A, 0),
     lambda: wq.wq_dequantize(wq.WQ_Q8_0, 4, 32, None, A, 0),
 ])
 def test_invalid_arguments_rejected_on_host(lib, call):
