@@ -67,6 +67,9 @@ def _load():
             lib.oracle_dequant.restype = ci
             lib.oracle_gemm.argtypes = [ci, ci, ci, ci, cu, ci, vp, vp, vp, vp, vp, vp, ci, ci, ci]
             lib.oracle_gemm.restype = ci
+            lib.oracle_gemm_alpha.argtypes = [ci, ci, ci, ci, cu, ci, f64, vp, vp, vp, vp, vp, vp,
+                                              ci, ci, ci]
+            lib.oracle_gemm_alpha.restype = ci
             lib.oracle_moe.argtypes = [ci, ci, ci, ci, ci, ci, cu, vp, vp, vp, vp, vp, vp, vp,
                                        ci, ci, ci]
             lib.oracle_moe.restype = ci
@@ -130,8 +133,11 @@ def dequant(wtype: int, m: int, k: int, W: np.ndarray) -> np.ndarray:
 
 
 def gemm(n, m, k, wtype, flags, X, W, bias=None, residual=None, round_x=False,
-         rows=None, threads=0, bound=True, round_w=False):
+         rows=None, threads=0, bound=True, round_w=False, alpha=1.0):
     """f64 ``(Y [n][m], S [n][m])`` of ``epi(X . W^T)``.
+
+    ``alpha`` scales the contribution before the residual is added (wavo's
+    ``Residual(alpha)``: ``Y = R + alpha * act(X . W^T + bias)``); S scales with it.
 
     ``round_x`` / ``round_w`` feed X / the dequantised W rounded to the nearest
     bf16 (ties to even): the operands of the tensor-core path.
@@ -145,8 +151,8 @@ def gemm(n, m, k, wtype, flags, X, W, bias=None, residual=None, round_x=False,
     S = np.full((n, m), np.nan, dtype=np.float64) if bound else None
     j0, j1 = (0, m) if rows is None else rows
     rnd = int(bool(round_x)) | (int(bool(round_w)) << 1)
-    rc = _load().oracle_gemm(n, m, k, wtype, flags, rnd, _ptr(Xc), _ptr(Wc),
-                             _ptr(bc), _ptr(Rc), _ptr(Y), _ptr(S), j0, j1, int(threads))
+    rc = _load().oracle_gemm_alpha(n, m, k, wtype, flags, rnd, float(alpha), _ptr(Xc), _ptr(Wc),
+                                   _ptr(bc), _ptr(Rc), _ptr(Y), _ptr(S), j0, j1, int(threads))
     if rc != 0:
         raise ValueError("oracle_gemm: bad arguments")
     return Y, S

@@ -148,9 +148,12 @@ int oracle_dequant(int wtype, int m, int k, const uint8_t *W, double *out) {
     return 0;
 }
 
-/* One output element from a dequantised W row. */
-static void dot_epi(int k, unsigned flags, int round_x, const float *x, const double *w,
-                    const float *bias_j, const float *res_ij, double *y, double *s) {
+/* One output element from a dequantised W row.  alpha scales the contribution
+ * before the residual is added: wavo 0.3.0 src/gpu/mod.rs, Epilogue::Residual(a),
+ * "c += a(aW^T + b)" (1 for every other epilogue); the bound scales with |alpha|. */
+static void dot_epi(int k, unsigned flags, int round_x, double alpha, const float *x,
+                    const double *w, const float *bias_j, const float *res_ij, double *y,
+                    double *s) {
     double acc = 0.0, bound = 0.0;
     for (int t = 0; t < k; ++t) {
         double xv = round_x ? oracle_round_bf16((double)x[t]) : (double)x[t];
@@ -164,9 +167,10 @@ static void dot_epi(int k, unsigned flags, int round_x, const float *x, const do
     else if (flags & O_SILU) v = v / (1.0 + exp(-v));
     else if (flags & O_RELU) v = v > 0.0 ? v : 0.0;
     else if (flags & O_TANH) v = tanh(v);
+    v *= alpha;
     if (flags & O_RESIDUAL) v += (double)*res_ij;
     *y = v;
-    if (s) *s = bound;
+    if (s) *s = fabs(alpha) * bound;
 }
 
 static int set_threads(int threads) {
@@ -187,9 +191,9 @@ static int set_threads(int threads) {
  * the tensor-core path.  threads <= 0: all.
  * Returns 0, or -1 on a bad argument.
  */
-int oracle_gemm(int n, int m, int k, int wtype, unsigned flags, int round,
-                const float *X, const uint8_t *W, const float *bias, const float *R,
-                double *Y, double *S, int j0, int j1, int threads) {
+int oracle_gemm_alpha(int n, int m, int k, int wtype, unsigned flags, int round, double alpha,
+                      const float *X, const uint8_t *W, const float *bias, const float *R,
+                      double *Y, double *S, int j0, int j1, int threads) {
     if (n < 0 || !shape_ok(wtype, m, k) || j0 < 0 || j1 > m || j0 > j1) return -1;
     if (__builtin_popcount(flags & O_ACTS) > 1) return -1;
     if (((flags & O_BIAS) && !bias) || ((flags & O_RESIDUAL) && !R)) return -1;
@@ -211,14 +215,22 @@ int oracle_gemm(int n, int m, int k, int wtype, unsigned flags, int round,
                     for (int t = 0; t < k; ++t) w[t] = oracle_round_bf16(w[t]);
                 for (int i = 0; i < n; ++i) {
                     size_t o = (size_t)i * m + j;
-                    dot_epi(k, flags, round_x, X + (size_t)i * k, w, bias ? bias + j : NULL,
-                            R ? R + o : NULL, Y + o, S ? S + o : NULL);
+                    dot_epi(k, flags, round_x, alpha, X + (size_t)i * k, w,
+                            bias ? bias + j : NULL, R ? R + o : NULL, Y + o, S ? S + o : NULL);
                 }
             }
             free(w);
         }
     }
     return bad ? -1 : 0;
+}
+
+/* The same with alpha = 1 (every epilogue but wavo's Residual(a)). */
+int oracle_gemm(int n, int m, int k, int wtype, unsigned flags, int round,
+                const float *X, const uint8_t *W, const float *bias, const float *R,
+                double *Y, double *S, int j0, int j1, int threads) {
+    return oracle_gemm_alpha(n, m, k, wtype, flags, round, 1.0, X, W, bias, R, Y, S, j0, j1,
+                             threads);
 }
 
 /*
@@ -253,7 +265,7 @@ int oracle_moe(int n_tok, int topk, int n_experts, int m, int k, int wtype, unsi
                     int t = q / topk;
                     dequant_row(wtype, Wbank + rb * ((size_t)e * m + j), k, w);
                     size_t o = (size_t)q * m + j;
-                    dot_epi(k, flags, 0, X + (size_t)t * k, w,
+                    dot_epi(k, flags, 0, 1.0, X + (size_t)t * k, w,
                             bias ? bias + (size_t)e * m + j : NULL, R ? R + o : NULL, Y + o,
                             S ? S + o : NULL);
                 }

@@ -250,6 +250,32 @@ def test_epilogue_order(oracle_mod):
     assert np.allclose(Y, want, rtol=1e-15)
 
 
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("alpha", [1.0, 0.5, -2.0, 0.0])
+def test_residual_alpha_closed_form(oracle_mod, wtype, alpha):
+    """wavo's Residual(a): c += a(aW^T + b).  With W = I every product is one x, so
+    Y = R + alpha (x + b) exactly for small integers and halves; the bound scales."""
+    n, k = 3, 64
+    g = np.random.default_rng(4)
+    X = g.integers(-20, 21, size=(n, k)).astype(np.float32)
+    b = g.integers(-5, 6, size=k).astype(np.float32)
+    R = g.integers(-9, 10, size=(n, k)).astype(np.float32)
+    Y, S = oracle_mod.gemm(n, k, k, wtype, BIAS | RESIDUAL, X, _identity_image(wtype, k), bias=b,
+                           residual=R, alpha=alpha)
+    assert (Y == R + alpha * (X.astype(np.float64) + b)).all()
+    assert (S == abs(alpha) * np.abs(X).astype(np.float64)).all()
+
+
+def test_residual_alpha_scales_the_activation(oracle_mod):
+    """The scale applies to the activation's output, before the residual."""
+    k = 32
+    X = np.ones((1, k), np.float32)
+    Y, _ = oracle_mod.gemm(1, k, k, Q4_0, BIAS | GELU | RESIDUAL, X, _identity_image(Q4_0, k),
+                           bias=np.ones(k, np.float32), residual=np.ones((1, k), np.float32),
+                           alpha=-0.25)
+    assert np.allclose(Y, 1.0 - 0.25 * 1.9544997361036416, rtol=1e-15)  # 1 - gelu(2) / 4
+
+
 @pytest.mark.parametrize("wtype", [Q8_0, Q4_0])
 def test_zero_weights_residual(oracle_mod, wtype):
     n, m, k = 3, 7, 64
