@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const GemmArgs a) {
             const int j = j0 + tx * 4 + v;
             if (j >= a.m) continue;
             const size_t o = (size_t)i * a.m + j;
-            a.Y[o] = epilogue(acc[u][v], a.flags, a.bias + j, a.R + o);
+            a.Y[o] = epilogue(acc[u][v], a.flags, a.bias + j, a.R + o, a.alpha);
         }
     }
 }
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(256) gemm_splitk_kernel(const GemmArgs a, int 
         const int i = i0 + idx / SK, j = j0 + idx % SK;
         if (i < a.n && j < a.m) {
             const size_t o = (size_t)i * a.m + j;
-            a.Y[o] = epilogue(sum, a.flags, a.bias + j, a.R + o);
+            a.Y[o] = epilogue(sum, a.flags, a.bias + j, a.R + o, a.alpha);
         }
     }
     cluster.sync();  // every rank keeps its shared memory until all slices are read

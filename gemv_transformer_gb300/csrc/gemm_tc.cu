@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(Roles<ATMA>::kThreads, 1)
                     for (int c = 0; c < 32; ++c) {
                         float t = v[c];
                         if (a.flags & kBias) t += (jb + c < a.m) ? __ldg(a.bias + jb + c) : 0.f;
-                        v[c] = activate(t, a.flags);
+                        v[c] = a.alpha * activate(t, a.flags);
                     }
                 }
                 // Row `lane` of the 32x32 block into shared memory...

@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float bc = __shfl_sync(0xFFFFFFFFu, bl[u], c);
                     float x = v[c];
                     if (a.flags & kBias) x += bc;
-                    v[c] = activate(x, a.flags);
+                    v[c] = a.alpha * activate(x, a.flags);
                 }
                 if (a.flags & kResidual) {
                     bool w = mbar_wait(&rbar[ew], rphase, limit);

@@ -733,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v += packed ? rp[i] + rp[P + i] : rp[i];
                         }
                         const int yrow = MOE ? s_sorted[seg0 + p0 + i] : p0 + i;
-                        a.Y[(size_t)yrow * m + row] = epilogue_vals(v, a.flags, s_bias[r], s_res[idx]);
+                        a.Y[(size_t)yrow * m + row] = epilogue_vals(v, a.flags, s_bias[r], s_res[idx], a.alpha);
                     }
                 }
                 consumers_sync();

@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) stream_kernel(const StreamArgs
                 const int yrow = MOE ? s_sorted[seg0 + r] : r;
                 const size_t o = (size_t)yrow * m + j;
                 const float *bj = a.bias + (MOE ? (size_t)e * m + j : (size_t)j);
-                a.Y[o] = epilogue(tot[r], a.flags, bj, a.R + o);
+                a.Y[o] = epilogue(tot[r], a.flags, bj, a.R + o, a.alpha);
             }
         }
         __syncwarp();

@@ -6,6 +6,7 @@
 // (wavo 0.3.0 src/gpu/mod.rs keeps the first device error and reports it on the
 // next call).  Nothing here computes; every step of the contraction runs in the
 // kernels.
+#include <cmath>
 #include <mutex>
 
 #include "../../include/wq.h"
@@ -94,7 +95,7 @@ size_t wq_weight_bytes(int wtype, int m, int k) {
 
 static wq_status gemv_impl(int n, int m, int k, int wtype, unsigned flags, const float *X,
                            const void *W, const float *bias, const float *residual, float *Y,
-                           wq_stream_t stream) {
+                           wq_stream_t stream, float alpha = 1.0f) {
     const DeviceInfo *dev = device_info();
     if (!dev) return WQ_ERR_CUDA;
     StreamArgs a{};
@@ -109,6 +110,7 @@ static wq_status gemv_impl(int n, int m, int k, int wtype, unsigned flags, const
     a.flags = flags & WQ_EPILOGUE_FLAGS;
     a.status = dev->status;
     a.wait_limit = wait_limit();
+    a.alpha = alpha;
     if (mma_gemv_supported(wtype, k))
         return cuda_status(launch_mma_gemv(a, wtype, *dev, (cudaStream_t)stream));
     return cuda_status(launch_stream_gemv(a, wtype, *dev, (cudaStream_t)stream));
@@ -122,12 +124,12 @@ wq_status wq_gemv(int n, int m, int k, int wtype, unsigned flags, const float *X
     return gemv_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream);
 }
 
-wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X, const void *W,
-                  const float *bias, const float *residual, float *Y, wq_stream_t stream) {
-    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
-    if (s != WQ_OK) return s;
+// wq_gemm after its argument checks.
+static wq_status gemm_impl(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                           const void *W, const float *bias, const float *residual, float *Y,
+                           wq_stream_t stream, float alpha) {
     if (n <= WQ_GEMV_MAX_N)
-        return gemv_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream);
+        return gemv_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, alpha);
     // Tensor cores with quantised W need the bf16 copy of W: wq_gemm_ws.
     if ((flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
     const DeviceInfo *dev = device_info();
@@ -144,8 +146,16 @@ wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X
     a.flags = flags & WQ_EPILOGUE_FLAGS;
     a.status = dev->status;
     a.wait_limit = wait_limit();
+    a.alpha = alpha;
     if (flags & WQ_TC_BF16) return cuda_status(launch_gemm_tc(a, *dev, (cudaStream_t)stream));
     return cuda_status(launch_gemm_simt(a, wtype, *dev, (cudaStream_t)stream));
+}
+
+wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X, const void *W,
+                  const float *bias, const float *residual, float *Y, wq_stream_t stream) {
+    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
+    if (s != WQ_OK) return s;
+    return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, 1.0f);
 }
 
 size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned flags) {
@@ -155,14 +165,14 @@ size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned flags) {
     return wtype == kBF16 ? x : x + gemm_tc_w_workspace_bytes(m, k);
 }
 
-wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float *X,
-                     const void *W, const float *bias, const float *residual, float *Y,
-                     void *workspace, size_t workspace_bytes, wq_stream_t stream) {
-    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
-    if (s != WQ_OK) return s;
+// wq_gemm_ws after the common argument checks.
+static wq_status gemm_ws_impl(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                              const void *W, const float *bias, const float *residual, float *Y,
+                              void *workspace, size_t workspace_bytes, wq_stream_t stream,
+                              float alpha) {
     const size_t need = wq_gemm_workspace_bytes(n, m, k, wtype, flags);
     if (need == 0)
-        return wq_gemm(n, m, k, wtype, flags, X, W, bias, residual, Y, stream);
+        return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, alpha);
     if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < need)
         return WQ_ERR_INVALID_ARG;
     const DeviceInfo *dev = device_info();
@@ -179,7 +189,29 @@ wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float
     a.flags = flags & WQ_EPILOGUE_FLAGS;
     a.status = dev->status;
     a.wait_limit = wait_limit();
+    a.alpha = alpha;
     return cuda_status(launch_gemm_tc_ws(a, wtype, workspace, *dev, (cudaStream_t)stream));
+}
+
+wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float *X,
+                     const void *W, const float *bias, const float *residual, float *Y,
+                     void *workspace, size_t workspace_bytes, wq_stream_t stream) {
+    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
+    if (s != WQ_OK) return s;
+    return gemm_ws_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, workspace,
+                        workspace_bytes, stream, 1.0f);
+}
+
+wq_status wq_gemm_alpha(int n, int m, int k, int wtype, unsigned flags, float alpha,
+                        const float *X, const void *W, const float *bias, const float *residual,
+                        float *Y, void *workspace, size_t workspace_bytes, wq_stream_t stream) {
+    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
+    if (s != WQ_OK) return s;
+    if (!std::isfinite(alpha)) return WQ_ERR_INVALID_ARG;
+    if (!workspace)
+        return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, alpha);
+    return gemm_ws_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, workspace,
+                        workspace_bytes, stream, alpha);
 }
 
 size_t wq_gemm_ln_workspace_bytes(int n, int m, int k, int wtype, unsigned flags) {

@@ -84,12 +84,14 @@ __device__ __forceinline__ float activate(float v, unsigned flags) {
     return tanhf(v);
 }
 
-// acc -> Y value.  `res` is read only with kResidual.
+// acc -> Y value.  `res` is read only with kResidual.  alpha scales the
+// contribution before the residual is added (wavo's Epilogue::Residual(a),
+// "c += a(aW^T + b)"; 1 otherwise, which leaves every value unchanged).
 __device__ __forceinline__ float epilogue(float acc, unsigned flags, const float *bias_j,
-                                          const float *res_ij) {
+                                          const float *res_ij, float alpha) {
     float v = acc;
     if (flags & kBias) v += __ldg(bias_j);
-    v = activate(v, flags);
+    v = alpha * activate(v, flags);
     if (flags & kResidual) v += *res_ij;  // may alias Y: plain load
     return v;
 }
@@ -97,10 +99,10 @@ __device__ __forceinline__ float epilogue(float acc, unsigned flags, const float
 // The same, with the bias and residual values already loaded (e.g. staged in
 // shared memory); each is used only when its flag is set.
 __device__ __forceinline__ float epilogue_vals(float acc, unsigned flags, float bias_j,
-                                               float res_ij) {
+                                               float res_ij, float alpha) {
     float v = acc;
     if (flags & kBias) v += bias_j;
-    v = activate(v, flags);
+    v = alpha * activate(v, flags);
     if (flags & kResidual) v += res_ij;
     return v;
 }

@@ -25,6 +25,7 @@ struct StreamArgs {
     int topk, n_experts;   // MoE only
     unsigned *status;      // device status word
     unsigned long long wait_limit;
+    float alpha = 1.0f;    // scale of the contribution before the residual
 };
 
 struct GemmArgs {
@@ -37,6 +38,7 @@ struct GemmArgs {
     unsigned flags;
     unsigned *status;
     unsigned long long wait_limit;
+    float alpha = 1.0f;    // scale of the contribution before the residual
 };
 
 struct DeviceInfo {

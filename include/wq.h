@@ -18,6 +18,8 @@
  *   - wq_moe_gemv: hanzo-ml 0.11.13, moe_matvec_gpu ("y[s, r] = sum_k
  *     W[ids[s], r, k] * x[s, k]" over one bank [E, rows, k], router gather and
  *     expert matvec in one dispatch).
+ *   - wq_gemm_alpha: wavo 0.3.0, src/gpu/mod.rs, Epilogue::Residual(a)
+ *     ("c += a(aW^T + b)") on the routes of wq_gemm / wq_gemm_ws.
  *   - wq_dequantize: the block formats themselves (same pages).
  *   - wq_embed: wavo 0.3.0, src/gpu/mod.rs, Recorder::embed ("row ids[i] of the
  *     table + pos[offset..] + the table's bias, k values") and its test
@@ -248,6 +250,20 @@ WQ_API size_t wq_weight_bytes(int wtype, int m, int k);
 /* out[m][k] (f32, device) = the dequantised weights, bit-exact (d*q and d*(q-8)
  * are exact in f32).  Same W contract as wq_gemm.  Asynchronous on `stream`. */
 WQ_API wq_status wq_dequantize(int wtype, int m, int k, const void *W, float *out, wq_stream_t stream);
+
+/* wq_gemm / wq_gemm_ws with the epilogue's contribution scaled by alpha before
+ * the residual is added: wavo 0.3.0 src/gpu/mod.rs, Epilogue::Residual(a),
+ * "c += a(aW^T + b)":
+ *   Y[i][j] = (WQ_RESIDUAL ? residual[i][j] : 0) + alpha * act(X.W^T + bias),
+ * the product and sum in f32.  workspace NULL: the routes of wq_gemm; otherwise
+ * those of wq_gemm_ws, with the same workspace rules.  alpha = 1 gives results
+ * bit-identical to wq_gemm / wq_gemm_ws.
+ * Errors: as wq_gemm / wq_gemm_ws, plus WQ_ERR_INVALID_ARG for a NaN or infinite
+ * alpha. */
+WQ_API wq_status wq_gemm_alpha(int n, int m, int k, int wtype, unsigned flags, float alpha,
+                               const float *X, const void *W, const float *bias,
+                               const float *residual, float *Y, void *workspace,
+                               size_t workspace_bytes, wq_stream_t stream);
 
 /* Embedding row gather: for t < n_ids and j < k,
  *   out[t][j] = W[ids[t]][j] + pos[t][j] + bias[j]

@@ -77,6 +77,11 @@ A = 0x10000  # a 16-byte aligned fake device address: never dereferenced below
     lambda: wq.wq_moe_gemv(2, 2, 4, 8, 32, wq.WQ_Q4_0, 0, A, A, None, None, None, A, 0),
     lambda: wq.wq_moe_gemv(2, 2, 4, 8, 32, wq.WQ_Q4_0, wq.WQ_TC_BF16, A, A, A, None, None, A, 0),
     lambda: wq.wq_dequantize(wq.WQ_Q8_0, 4, 40, A, A, 0),
+    lambda: wq.wq_gemm_alpha(1, 8, 32, wq.WQ_Q8_0, 0, float("nan"), A, A, None, None, A, None, 0, 0),
+    lambda: wq.wq_gemm_alpha(1, 8, 32, wq.WQ_Q8_0, 0, float("inf"), A, A, None, None, A, None, 0, 0),
+    lambda: wq.wq_gemm_alpha(1, 8, 40, wq.WQ_Q8_0, 0, 0.5, A, A, None, None, A, None, 0, 0),
+    lambda: wq.wq_gemm_alpha(1, 8, 32, wq.WQ_Q8_0, wq.WQ_RESIDUAL, 0.5, A, A, None, None, A, None,
+                             0, 0),
     lambda: wq.wq_embed(0, 8, 32, wq.WQ_Q8_0, A, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 0, 32, wq.WQ_Q8_0, A, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 8, 40, wq.WQ_Q4_0, A, A, None, None, A, 0),
