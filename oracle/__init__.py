@@ -30,7 +30,7 @@ _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-BF16, Q8_0, Q4_0 = 0, 1, 2
+BF16, Q8_0, Q4_0, F16, F32 = 0, 1, 2, 3, 4
 BIAS, GELU, RESIDUAL = 1, 2, 4
 
 

@@ -40,11 +40,12 @@
 #include <stddef.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
 
-enum { O_BF16 = 0, O_Q8_0 = 1, O_Q4_0 = 2 };
+enum { O_BF16 = 0, O_Q8_0 = 1, O_Q4_0 = 2, O_F16 = 3, O_F32 = 4 };
 enum { O_BIAS = 1u, O_GELU = 2u, O_RESIDUAL = 4u, O_SILU = 8u, O_RELU = 16u, O_TANH = 32u };
 #define O_ACTS (O_GELU | O_SILU | O_RELU | O_TANH)
 
@@ -101,12 +102,31 @@ static size_t row_bytes(int wtype, int k) {
     case O_BF16: return (size_t)2 * k;
     case O_Q8_0: return (size_t)34 * (k / 32);
     case O_Q4_0: return (size_t)18 * (k / 32);
+    case O_F16: return (size_t)2 * k;
+    case O_F32: return (size_t)4 * k;
     }
     return 0;
 }
 
-/* Dequantise one W row of k weights into f64. */
+/* Dequantise one W row of k weights into f64.  F16 / F32: wavo 0.3.0
+ * src/gpu/mod.rs, Linear "GEMM pipeline index: 0: F32, 1: F16" -- plain IEEE
+ * binary16 / binary32 elements, little-endian, row after row. */
 static void dequant_row(int wtype, const uint8_t *row, int k, double *w) {
+    if (wtype == O_F16) {
+        for (int t = 0; t < k; ++t)
+            w[t] = oracle_half_to_f64((uint16_t)(row[2 * t] | (row[2 * t + 1] << 8)));
+        return;
+    }
+    if (wtype == O_F32) {
+        for (int t = 0; t < k; ++t) {
+            uint32_t bits = (uint32_t)row[4 * t] | ((uint32_t)row[4 * t + 1] << 8) |
+                            ((uint32_t)row[4 * t + 2] << 16) | ((uint32_t)row[4 * t + 3] << 24);
+            float f;
+            memcpy(&f, &bits, sizeof f);
+            w[t] = (double)f;
+        }
+        return;
+    }
     if (wtype == O_BF16) {
         for (int c = 0; c < k / 2; ++c) {
             uint32_t word = (uint32_t)row[4 * c] | ((uint32_t)row[4 * c + 1] << 8) |
@@ -137,6 +157,7 @@ static int shape_ok(int wtype, int m, int k) {
     if (m < 0 || k <= 0) return 0;
     if (wtype == O_BF16) return k % 2 == 0;
     if (wtype == O_Q8_0 || wtype == O_Q4_0) return k % 32 == 0;
+    if (wtype == O_F16 || wtype == O_F32) return 1;
     return 0;
 }
 

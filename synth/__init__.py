@@ -32,6 +32,8 @@ import numpy as np
 WTYPE_BF16 = 0
 WTYPE_Q8_0 = 1
 WTYPE_Q4_0 = 2
+WTYPE_F16 = 3
+WTYPE_F32 = 4
 
 QK = 32  # weights per quantisation block along k
 Q8_0_BLOCK_BYTES = 34
@@ -116,6 +118,10 @@ def weight_bytes(wtype: int, m: int, k: int) -> int:
         return Q8_0_BLOCK_BYTES * m * (k // QK)
     if wtype == WTYPE_Q4_0:
         return Q4_0_BLOCK_BYTES * m * (k // QK)
+    if wtype == WTYPE_F16:
+        return 2 * m * k
+    if wtype == WTYPE_F32:
+        return 4 * m * k
     raise ValueError(wtype)
 
 
@@ -143,6 +149,16 @@ def draw_q4_0_weights(g, m, k, d_lo=1e-3, d_hi=1e-2):
     return out.reshape(m, nb * Q4_0_BLOCK_BYTES)
 
 
+def draw_f16_weights(g, m, k, std):
+    """W = f16(N(0, std)) (numpy's round-to-nearest-even), the byte image [m][2k]."""
+    return f16_bits(normal_f32(g, (m, k), std)).view(np.uint8).reshape(m, 2 * k)
+
+
+def draw_f32_weights(g, m, k, std):
+    """W = N(0, std) in f32, the byte image [m][4k]."""
+    return normal_f32(g, (m, k), std).view(np.uint8).reshape(m, 4 * k)
+
+
 def draw_weights(g, wtype, m, k, std=0.05):
     if wtype == WTYPE_BF16:
         return draw_bf16_weights(g, m, k, std)
@@ -150,6 +166,10 @@ def draw_weights(g, wtype, m, k, std=0.05):
         return draw_q8_0_weights(g, m, k)
     if wtype == WTYPE_Q4_0:
         return draw_q4_0_weights(g, m, k)
+    if wtype == WTYPE_F16:
+        return draw_f16_weights(g, m, k, std)
+    if wtype == WTYPE_F32:
+        return draw_f32_weights(g, m, k, std)
     raise ValueError(wtype)
 
 

@@ -527,3 +527,37 @@ def test_embed_leaves_rows_of_bad_ids(oracle_mod):
     assert valid.tolist() == [True, False, False, True]
     assert (out[1] == 42.0).all() and (out[2] == 42.0).all()
     assert (out[0] == value[3]).all() and (out[3] == value[9]).all()
+
+
+# ----------------------------------------------- F16 / F32 weights (wavo ty 1 / 0) --
+
+@pytest.mark.parametrize("wtype", [synth.WTYPE_F16, synth.WTYPE_F32])
+def test_plain_float_weights_dequantise_like_numpy(oracle_mod, wtype):
+    """wavo's F16 and F32 weight types are IEEE elements row after row: the oracle's
+    decode equals numpy's own conversions, specials included."""
+    g = synth.rng(31)
+    m, k = 9, 40
+    img = synth.draw_weights(g, wtype, m, k, std=3.0)
+    specials = np.array([0.0, -0.0, np.inf, -np.inf, 65504.0, 2.0 ** -24, -(2.0 ** -14)])
+    if wtype == synth.WTYPE_F16:
+        img[0, :2 * len(specials)] = specials.astype(np.float16).view(np.uint8)
+        want = img.view(np.float16).astype(np.float64)
+    else:
+        img[0, :4 * len(specials)] = specials.astype(np.float32).view(np.uint8)
+        want = img.view(np.float32).astype(np.float64)
+    got = oracle_mod.dequant(wtype, m, k, img)
+    assert np.array_equal(got, want.reshape(m, k))
+
+
+@pytest.mark.parametrize("wtype", [synth.WTYPE_F16, synth.WTYPE_F32])
+def test_plain_float_weights_exact_integer_gemm(oracle_mod, wtype):
+    """Small integers are exact in f16 and f32: the oracle's GEMM equals integer
+    brute force."""
+    g = synth.rng(32)
+    n, m, k = 3, 5, 24
+    Wv = g.integers(-9, 10, size=(m, k))
+    X = g.integers(-9, 10, size=(n, k)).astype(np.float32)
+    img = (Wv.astype(np.float16) if wtype == synth.WTYPE_F16 else Wv.astype(np.float32))
+    img = img.view(np.uint8).reshape(m, -1)
+    Y, _ = oracle_mod.gemm(n, m, k, wtype, 0, X, img)
+    assert (Y == X.astype(np.int64) @ Wv.T).all()
