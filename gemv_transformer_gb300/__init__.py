@@ -18,7 +18,7 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libwq.so")
 
-WQ_BF16, WQ_Q8_0, WQ_Q4_0 = 0, 1, 2
+WQ_BF16, WQ_Q8_0, WQ_Q4_0, WQ_F16, WQ_F32 = 0, 1, 2, 3, 4
 WQ_BIAS, WQ_GELU, WQ_RESIDUAL, WQ_TC_BF16 = 1, 2, 4, 256
 WQ_SILU, WQ_RELU, WQ_TANH = 8, 16, 32
 WQ_OK, WQ_ERR_INVALID_ARG, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA = 0, 1, 2, 3

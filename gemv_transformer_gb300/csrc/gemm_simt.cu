@@ -23,6 +23,43 @@
 namespace wq {
 namespace {
 
+// Eight consecutive weights t0..t0+7 (t0 % 8 == 0) of one W row, exact in f32.
+template <int WT>
+__device__ __forceinline__ void decode8(const uint8_t *row, int t0, float (&w)[8]) {
+    if (WT == kF16) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(row + (size_t)2 * t0);
+        w[0] = half_bits_to_f32(v.x); w[1] = half_bits_to_f32(v.x >> 16);
+        w[2] = half_bits_to_f32(v.y); w[3] = half_bits_to_f32(v.y >> 16);
+        w[4] = half_bits_to_f32(v.z); w[5] = half_bits_to_f32(v.z >> 16);
+        w[6] = half_bits_to_f32(v.w); w[7] = half_bits_to_f32(v.w >> 16);
+    } else if (WT == kF32) {
+        const float4 v0 = *reinterpret_cast<const float4 *>(row + (size_t)4 * t0);
+        const float4 v1 = *reinterpret_cast<const float4 *>(row + (size_t)4 * t0 + 16);
+        w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+        w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+    } else if (WT == kBF16) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(row + (size_t)2 * t0);
+        w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x);
+        w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+        w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z);
+        w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
+    } else if (WT == kQ8_0) {
+        const uint8_t *bp = row + (size_t)34 * (t0 / 32);
+        const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+        for (int e = 0; e < 8; ++e) w[e] = d * (float)(int8_t)bp[2 + (t0 & 31) + e];
+    } else {
+        const uint8_t *bp = row + (size_t)18 * (t0 / 32);
+        const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+        for (int e = 0; e < 8; ++e) {
+            const int t = (t0 & 31) + e;
+            const uint32_t byte = bp[2 + (t & 15)];
+            const int code = (t < 16) ? (int)(byte & 15u) : (int)(byte >> 4);
+            w[e] = d * (float)(code - 8);
+        }
+    }
+}
+
+
 constexpr int TI = 64, TJ = 64, TK = 32;
 
 template <int WT>
@@ -35,15 +72,9 @@ __device__ __forceinline__ void load_w_tile(const GemmArgs &a, int j0, int kk, i
     for (int e = 0; e < 8; ++e) w[e] = 0.f;
     if (j < a.m) {
         const uint8_t *row = a.W + (size_t)j * row_bytes(WT, a.k);
-        if (WT == kBF16) {
+        if (WT == kBF16 || WT == kF16 || WT == kF32) {
             const int t0 = kk + 8 * q;
-            if (t0 < a.k) {  // k % 8 == 0: all eight or none
-                const uint4 v = *reinterpret_cast<const uint4 *>(row + (size_t)2 * t0);
-                w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x);
-                w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
-                w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z);
-                w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
-            }
+            if (t0 < a.k) decode8<WT>(row, t0, w);  // k % 8 == 0: all eight or none
         } else if (WT == kQ8_0) {
             const uint8_t *bp = row + (size_t)34 * (kk / 32);
             const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
@@ -140,6 +171,13 @@ __device__ __forceinline__ void load_w4(const GemmArgs &a, int j, int kk, int q,
         const uint2 v = *reinterpret_cast<const uint2 *>(row + (size_t)2 * (kk + 4 * q));
         w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x);
         w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+    } else if (WT == kF16) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(row + (size_t)2 * (kk + 4 * q));
+        w[0] = half_bits_to_f32(v.x); w[1] = half_bits_to_f32(v.x >> 16);
+        w[2] = half_bits_to_f32(v.y); w[3] = half_bits_to_f32(v.y >> 16);
+    } else if (WT == kF32) {
+        const float4 v = *reinterpret_cast<const float4 *>(row + (size_t)4 * (kk + 4 * q));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
     } else if (WT == kQ8_0) {
         const uint8_t *bp = row + (size_t)34 * (kk / 32);
         const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
@@ -253,31 +291,6 @@ cudaError_t launch_splitk_wt(const GemmArgs &a, int tiles_m, int tiles_n, int ks
     return cudaLaunchKernelEx(&cfg, gemm_splitk_kernel<WT>, a, spr);
 }
 
-// Eight consecutive weights t0..t0+7 (t0 % 8 == 0) of one W row, exact in f32.
-template <int WT>
-__device__ __forceinline__ void decode8(const uint8_t *row, int t0, float (&w)[8]) {
-    if (WT == kBF16) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(row + (size_t)2 * t0);
-        w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x);
-        w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
-        w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z);
-        w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
-    } else if (WT == kQ8_0) {
-        const uint8_t *bp = row + (size_t)34 * (t0 / 32);
-        const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
-        for (int e = 0; e < 8; ++e) w[e] = d * (float)(int8_t)bp[2 + (t0 & 31) + e];
-    } else {
-        const uint8_t *bp = row + (size_t)18 * (t0 / 32);
-        const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
-        for (int e = 0; e < 8; ++e) {
-            const int t = (t0 & 31) + e;
-            const uint32_t byte = bp[2 + (t & 15)];
-            const int code = (t < 16) ? (int)(byte & 15u) : (int)(byte >> 4);
-            w[e] = d * (float)(code - 8);
-        }
-    }
-}
-
 template <int WT>
 __global__ void dequant_kernel(int m, int k, const uint8_t *W, float *out) {
     pdl_enter();
@@ -370,6 +383,8 @@ cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev
         if (tn <= 65535) {
             switch (wtype) {
             case kBF16: return launch_splitk_wt<kBF16>(a, (int)tm, (int)tn, (int)ks, spr, stream);
+            case kF16: return launch_splitk_wt<kF16>(a, (int)tm, (int)tn, (int)ks, spr, stream);
+            case kF32: return launch_splitk_wt<kF32>(a, (int)tm, (int)tn, (int)ks, spr, stream);
             case kQ8_0: return launch_splitk_wt<kQ8_0>(a, (int)tm, (int)tn, (int)ks, spr, stream);
             default: return launch_splitk_wt<kQ4_0>(a, (int)tm, (int)tn, (int)ks, spr, stream);
             }
@@ -378,6 +393,8 @@ cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     switch (wtype) {
     case kBF16: return launch_pdl(gemm_simt_kernel<kBF16>, grid, dim3(256), 0, stream, a);
+    case kF16: return launch_pdl(gemm_simt_kernel<kF16>, grid, dim3(256), 0, stream, a);
+    case kF32: return launch_pdl(gemm_simt_kernel<kF32>, grid, dim3(256), 0, stream, a);
     case kQ8_0: return launch_pdl(gemm_simt_kernel<kQ8_0>, grid, dim3(256), 0, stream, a);
     default: return launch_pdl(gemm_simt_kernel<kQ4_0>, grid, dim3(256), 0, stream, a);
     }
@@ -391,6 +408,8 @@ cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out
     if (blocks < 1) blocks = 1;
     switch (wtype) {
     case kBF16: return launch_pdl(dequant_kernel<kBF16>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
+    case kF16: return launch_pdl(dequant_kernel<kF16>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
+    case kF32: return launch_pdl(dequant_kernel<kF32>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
     case kQ8_0: return launch_pdl(dequant_kernel<kQ8_0>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
     default: return launch_pdl(dequant_kernel<kQ4_0>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
     }
@@ -411,6 +430,8 @@ cudaError_t launch_embed(int n_ids, int rows, int k, int wtype, const uint8_t *W
     };
     switch (wtype) {
     case kBF16: return vec ? go(embed_kernel<kBF16, true>) : go(embed_kernel<kBF16, false>);
+    case kF16: return vec ? go(embed_kernel<kF16, true>) : go(embed_kernel<kF16, false>);
+    case kF32: return vec ? go(embed_kernel<kF32, true>) : go(embed_kernel<kF32, false>);
     case kQ8_0: return vec ? go(embed_kernel<kQ8_0, true>) : go(embed_kernel<kQ8_0, false>);
     default: return vec ? go(embed_kernel<kQ4_0, true>) : go(embed_kernel<kQ4_0, false>);
     }

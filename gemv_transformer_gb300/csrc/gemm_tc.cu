@@ -399,6 +399,35 @@ __global__ void w_to_bf16_kernel(const uint8_t *__restrict__ W, int m, int k,
     }
 }
 
+// F16 / F32 W -> bf16 [m][k], each element rounded to the nearest bf16 (ties to
+// even).  One thread per 8 weights (k % 8 == 0, rows 16-byte aligned).
+template <int WT>
+__global__ void wf_to_bf16_kernel(const uint8_t *__restrict__ W, int m, int k,
+                                  uint4 *__restrict__ wb) {
+    pdl_enter();
+    const long long units = (long long)m * (k / 8);
+    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < units;
+         u += (long long)gridDim.x * blockDim.x) {
+        float w[8];
+        if (WT == kF16) {
+            const uint4 v = reinterpret_cast<const uint4 *>(W)[u];  // 8 halves
+            const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                w[2 * e] = half_bits_to_f32(h[e]);
+                w[2 * e + 1] = half_bits_to_f32(h[e] >> 16);
+            }
+        } else {
+            const float4 a = reinterpret_cast<const float4 *>(W)[2 * u];
+            const float4 b = reinterpret_cast<const float4 *>(W)[2 * u + 1];
+            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+            w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        }
+        wb[u] = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                           pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+    }
+}
+
 size_t gemm_tc_w_workspace_bytes(int m, int k) {
     return ((size_t)m * k * 2 + 255) & ~(size_t)255;
 }
@@ -409,15 +438,29 @@ cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
     if (wtype != kBF16) {
         // The weights first: bf16 after X in the workspace, then the bf16 GEMM.
         uint8_t *wb = static_cast<uint8_t *>(workspace) + gemm_tc_workspace_bytes(a.n, a.k);
-        const long long blocks = (long long)a.m * (a.k / 32);
-        long long grid = (blocks + 255) / 256;
+        const bool plain = wtype == kF16 || wtype == kF32;
+        const long long units = (long long)a.m * (a.k / (plain ? 8 : 32));
+        long long grid = (units + 255) / 256;
         if (grid > (long long)dev.sm_count * 8) grid = (long long)dev.sm_count * 8;
-        cudaError_t err =
-            wtype == kQ8_0
-                ? launch_pdl(w_to_bf16_kernel<kQ8_0>, dim3((unsigned)grid), dim3(256), 0, stream,
-                             a.W, a.m, a.k, reinterpret_cast<uint4 *>(wb))
-                : launch_pdl(w_to_bf16_kernel<kQ4_0>, dim3((unsigned)grid), dim3(256), 0, stream,
-                             a.W, a.m, a.k, reinterpret_cast<uint4 *>(wb));
+        uint4 *wo = reinterpret_cast<uint4 *>(wb);
+        cudaError_t err;
+        switch (wtype) {
+        case kQ8_0:
+            err = launch_pdl(w_to_bf16_kernel<kQ8_0>, dim3((unsigned)grid), dim3(256), 0, stream,
+                             a.W, a.m, a.k, wo);
+            break;
+        case kF16:
+            err = launch_pdl(wf_to_bf16_kernel<kF16>, dim3((unsigned)grid), dim3(256), 0, stream,
+                             a.W, a.m, a.k, wo);
+            break;
+        case kF32:
+            err = launch_pdl(wf_to_bf16_kernel<kF32>, dim3((unsigned)grid), dim3(256), 0, stream,
+                             a.W, a.m, a.k, wo);
+            break;
+        default:
+            err = launch_pdl(w_to_bf16_kernel<kQ4_0>, dim3((unsigned)grid), dim3(256), 0, stream,
+                             a.W, a.m, a.k, wo);
+        }
         if (err != cudaSuccess) return err;
         g.W = wb;
     }

@@ -47,6 +47,14 @@ template <>
 struct Piece<kBF16> {
     static constexpr int elems = 1024;
 };
+template <>
+struct Piece<kF16> {
+    static constexpr int elems = 1024;
+};
+template <>
+struct Piece<kF32> {
+    static constexpr int elems = 512;
+};
 
 constexpr size_t kSmemStages = (size_t)kWarps * kStages * kStageBytes;
 constexpr size_t kSmemBars = (size_t)kWarps * kStages * sizeof(uint64_t);
@@ -258,12 +266,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1) stream_kernel(const StreamArgs
                         }
                     }
                 }
-            } else {  // bf16 pairs
-                const int units = elems >> 2;  // 4 weights (two words) per lane step
+            } else {  // bf16 pairs, f16 or f32 elements
+                const int units = elems >> 2;  // 4 weights per lane step
                 for (int u = lane; u < units; u += 32) {
-                    const uint2 wv = *reinterpret_cast<const uint2 *>(pc + (size_t)u * 8);
-                    const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x);
-                    const float w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
+                    float w0, w1, w2, w3;
+                    if (WT == kF32) {
+                        const float4 wv = *reinterpret_cast<const float4 *>(pc + (size_t)u * 16);
+                        w0 = wv.x; w1 = wv.y; w2 = wv.z; w3 = wv.w;
+                    } else if (WT == kF16) {
+                        const uint2 wv = *reinterpret_cast<const uint2 *>(pc + (size_t)u * 8);
+                        w0 = half_bits_to_f32(wv.x); w1 = half_bits_to_f32(wv.x >> 16);
+                        w2 = half_bits_to_f32(wv.y); w3 = half_bits_to_f32(wv.y >> 16);
+                    } else {
+                        const uint2 wv = *reinterpret_cast<const uint2 *>(pc + (size_t)u * 8);
+                        w0 = bf16_lo(wv.x); w1 = bf16_hi(wv.x);
+                        w2 = bf16_lo(wv.y); w3 = bf16_hi(wv.y);
+                    }
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
                         if (t < ng) {
@@ -329,6 +347,8 @@ cudaError_t launch_stream_gemv(const StreamArgs &a, int wtype, const DeviceInfo 
     const int grid = (int)(need < dev.sm_count ? need : dev.sm_count);
     switch (wtype) {
     case kBF16: return launch_gemv_wt<kBF16>(a, grid, dev, stream);
+    case kF16: return launch_gemv_wt<kF16>(a, grid, dev, stream);
+    case kF32: return launch_gemv_wt<kF32>(a, grid, dev, stream);
     case kQ8_0: return launch_gemv_wt<kQ8_0>(a, grid, dev, stream);
     default: return launch_gemv_wt<kQ4_0>(a, grid, dev, stream);
     }
@@ -341,6 +361,8 @@ cudaError_t launch_stream_moe(const StreamArgs &a, int wtype, const DeviceInfo &
     const int grid = (int)(need < dev.sm_count ? need : dev.sm_count);
     switch (wtype) {
     case kBF16: return launch_one<kBF16, true, 4>(a, grid, dev, stream);
+    case kF16: return launch_one<kF16, true, 4>(a, grid, dev, stream);
+    case kF32: return launch_one<kF32, true, 4>(a, grid, dev, stream);
     case kQ8_0: return launch_one<kQ8_0, true, 4>(a, grid, dev, stream);
     default: return launch_one<kQ4_0, true, 4>(a, grid, dev, stream);
     }

@@ -34,6 +34,7 @@ bool shape_ok(int wtype, int m, int k) {
     if (m <= 0 || k <= 0) return false;
     if (wtype == kBF16) return k % 8 == 0;
     if (wtype == kQ8_0 || wtype == kQ4_0) return k % 32 == 0;
+    if (wtype == kF16 || wtype == kF32) return k % 8 == 0;
     return false;
 }
 

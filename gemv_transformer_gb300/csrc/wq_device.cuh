@@ -8,6 +8,8 @@
 //   Q4_0         hanzo-ml 0.11.13, matvec_q4_0_gpu: 18-byte blocks, f16 d then 16
 //                bytes; element t < 16 = low nibble of byte t, t >= 16 = high
 //                nibble of byte t-16; w = d*(q-8).
+//   F16 / F32    wavo 0.3.0 src/gpu/mod.rs, Linear ("0: F32, 1: F16"): IEEE
+//                binary16 / binary32 elements, row after row.
 // Epilogue       cortiq-engine ae_put: +bias, erf-GELU, +old Y, in that order.
 #pragma once
 
@@ -17,14 +19,19 @@
 
 namespace wq {
 
-enum WType : int { kBF16 = 0, kQ8_0 = 1, kQ4_0 = 2 };
+enum WType : int { kBF16 = 0, kQ8_0 = 1, kQ4_0 = 2, kF16 = 3, kF32 = 4 };
 enum Flag : unsigned { kBias = 1u, kGelu = 2u, kResidual = 4u, kSilu = 8u, kRelu = 16u, kTanh = 32u };
 constexpr unsigned kActs = kGelu | kSilu | kRelu | kTanh;  // at most one per call
 enum DevStatus : unsigned { kStTimeout = 4u, kStBadExpert = 5u, kStBadIndex = 7u };
 
 // Bytes of one row of k weights in each format.
 __host__ __device__ __forceinline__ size_t row_bytes(int wt, int k) {
-    return wt == kBF16 ? (size_t)2 * k : (wt == kQ8_0 ? (size_t)34 * (k / 32) : (size_t)18 * (k / 32));
+    switch (wt) {
+    case kBF16: case kF16: return (size_t)2 * k;
+    case kF32: return (size_t)4 * k;
+    case kQ8_0: return (size_t)34 * (k / 32);
+    default: return (size_t)18 * (k / 32);
+    }
 }
 
 // First error wins; later ones are dropped.

@@ -76,9 +76,12 @@ typedef enum {
                     i.e. row-major little-endian bf16 [m][k]; k % 8 == 0 */
     WQ_Q8_0 = 1, /* 34-byte blocks of 32 weights along k: f16 d (LE), int8 q[32];
                     w = d*q; k % 32 == 0 */
-    WQ_Q4_0 = 2  /* 18-byte blocks of 32 weights: f16 d (LE), 16 bytes; element t<16
+    WQ_Q4_0 = 2, /* 18-byte blocks of 32 weights: f16 d (LE), 16 bytes; element t<16
                     = low nibble of byte t, t>=16 = high nibble of byte t-16;
                     w = d*(q-8); k % 32 == 0 */
+    WQ_F16 = 3,  /* wavo 0.3.0 src/gpu/mod.rs Linear type 1: IEEE binary16 [m][k],
+                    little-endian; k % 8 == 0 */
+    WQ_F32 = 4   /* wavo Linear type 0: IEEE binary32 [m][k]; k % 8 == 0 */
 } wq_wtype;
 
 /* Epilogue flags, the bit values and order of cortiq-engine's ae_put:
@@ -126,10 +129,12 @@ typedef enum {
  * wq_gemv); otherwise WQ_TC_BF16 with WQ_BF16 weights runs the tcgen05 kernel,
  * and everything else the f32-FMA tiled kernel.
  * Errors: WQ_ERR_INVALID_ARG for n, m, k <= 0; k % 32 != 0 (Q8_0/Q4_0) or
- * k % 8 != 0 (bf16); null X, W or Y; null bias/residual when its flag is set;
- * X or W not 16-byte aligned; unknown flag bits or wtype.  WQ_ERR_UNSUPPORTED for
- * WQ_TC_BF16 with a quantised wtype and n > WQ_GEMV_MAX_N (that needs the bf16
- * copy of W in a workspace: wq_gemm_ws).  WQ_ERR_CUDA if the launch fails.
+ * k % 8 != 0 (bf16, f16, f32); null X, W or Y; null bias/residual when its flag
+ * is set; X or W not 16-byte aligned; unknown flag bits or wtype.
+ * WQ_ERR_UNSUPPORTED for WQ_TC_BF16 with a wtype other than WQ_BF16 and
+ * n > WQ_GEMV_MAX_N (that needs the bf16 copy of W in a workspace: wq_gemm_ws;
+ * f16/f32 elements, like d*q, are rounded to the nearest bf16 there).
+ * WQ_ERR_CUDA if the launch fails.
  */
 WQ_API wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X, const void *W,
                   const float *bias, const float *residual, float *Y, wq_stream_t stream);

@@ -41,6 +41,10 @@ def test_weight_bytes():
     assert wq.wq_weight_bytes(wq.WQ_Q4_0, 1, 40) == 0       # k % 32
     assert wq.wq_weight_bytes(wq.WQ_BF16, 1, 12) == 0       # k % 8
     assert wq.wq_weight_bytes(7, 1, 32) == 0
+    assert wq.wq_weight_bytes(wq.WQ_F16, 3, 40) == 240
+    assert wq.wq_weight_bytes(wq.WQ_F32, 3, 40) == 480
+    assert wq.wq_weight_bytes(wq.WQ_F16, 3, 36) == 0       # k % 8
+    assert wq.wq_weight_bytes(wq.WQ_F32, 1, 12) == 0
 
 
 def test_status_strings():
@@ -58,7 +62,9 @@ A = 0x10000  # a 16-byte aligned fake device address: never dereferenced below
     lambda: wq.wq_gemm(1, 8, 40, wq.WQ_Q8_0, 0, A, A, None, None, A, 0),
     lambda: wq.wq_gemm(1, 8, 36, wq.WQ_Q4_0, 0, A, A, None, None, A, 0),
     lambda: wq.wq_gemm(1, 8, 12, wq.WQ_BF16, 0, A, A, None, None, A, 0),
-    lambda: wq.wq_gemm(1, 8, 32, 3, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 12, wq.WQ_F16, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 20, wq.WQ_F32, 0, A, A, None, None, A, 0),
+    lambda: wq.wq_gemm(1, 8, 32, 7, 0, A, A, None, None, A, 0),      # unknown wtype
     lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, 64, A, A, None, None, A, 0),      # unknown flag
     lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, wq.WQ_GELU | wq.WQ_SILU, A, A, None, None, A, 0),
     lambda: wq.wq_gemm(1, 8, 32, wq.WQ_Q8_0, wq.WQ_RELU | wq.WQ_TANH, A, A, None, None, A, 0),
@@ -86,7 +92,7 @@ A = 0x10000  # a 16-byte aligned fake device address: never dereferenced below
     lambda: wq.wq_embed(2, 0, 32, wq.WQ_Q8_0, A, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 8, 40, wq.WQ_Q4_0, A, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 8, 12, wq.WQ_BF16, A, A, None, None, A, 0),
-    lambda: wq.wq_embed(2, 8, 32, 3, A, A, None, None, A, 0),
+    lambda: wq.wq_embed(2, 8, 32, 7, A, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 8, 32, wq.WQ_Q8_0, None, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 8, 32, wq.WQ_Q8_0, A, None, None, None, A, 0),
     lambda: wq.wq_embed(2, 8, 32, wq.WQ_Q8_0, A, A, None, None, None, 0),
@@ -95,6 +101,12 @@ A = 0x10000  # a 16-byte aligned fake device address: never dereferenced below
 ])
 def test_invalid_arguments_rejected_on_host(lib, call):
     assert call() == wq.WQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("wtype", [wq.WQ_Q8_0, wq.WQ_Q4_0, wq.WQ_F16, wq.WQ_F32])
+def test_tensor_core_gemm_of_other_formats_needs_a_workspace(lib, wtype):
+    assert wq.wq_gemm(20, 8, 32, wtype, wq.WQ_TC_BF16, A, A, None, None, A, 0) == \
+        wq.WQ_ERR_UNSUPPORTED
 
 
 def test_workspace_sizes_and_errors(lib):
