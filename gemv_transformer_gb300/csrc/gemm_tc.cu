@@ -320,20 +320,37 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
 }
 
 // X f32 -> bf16, round to nearest even (the rounding the fused path applies).
-// Four 16-byte loads in flight per thread per step (the copy is latency-bound
-// with one).
-__global__ void x_to_bf16_kernel(const float4 *__restrict__ x, uint2 *__restrict__ xb, size_t n4) {
+// The copy is bound by bytes in flight: each thread first requests kXU 16-byte
+// pieces with cp.async into shared memory (no registers held while they are in
+// flight, so four CTAs of 48 KB keep ~190 KB per SM outstanding), then converts
+// its own pieces and stores them.
+constexpr int kXU = 12;
+constexpr int kXThreads = 256;
+constexpr int kXSmem = kXThreads * kXU * 16;
+__global__ void __launch_bounds__(kXThreads) x_to_bf16_kernel(const float4 *__restrict__ x,
+                                                              uint2 *__restrict__ xb, size_t n4) {
     pdl_enter();
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += 4 * stride) {
-        float4 v[4];
+    extern __shared__ float4 xs[];
+    const size_t per_cta = (size_t)kXThreads * kXU;
+    for (size_t base = (size_t)blockIdx.x * per_cta; base < n4; base += (size_t)gridDim.x * per_cta) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (i + u * stride < n4) v[u] = __ldg(x + i + u * stride);
+        for (int u = 0; u < kXU; ++u) {
+            const size_t i = base + (size_t)u * kXThreads + threadIdx.x;
+            if (i < n4)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                 smem_addr(&xs[u * kXThreads + threadIdx.x])),
+                             "l"(x + i)
+                             : "memory");
+        }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (i + u * stride < n4)
-                xb[i + u * stride] = make_uint2(pack_bf16x2(v[u].x, v[u].y), pack_bf16x2(v[u].z, v[u].w));
+        for (int u = 0; u < kXU; ++u) {
+            const size_t i = base + (size_t)u * kXThreads + threadIdx.x;
+            if (i < n4) {
+                const float4 v = xs[u * kXThreads + threadIdx.x];
+                xb[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+            }
+        }
     }
 }
 
@@ -466,12 +483,16 @@ cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
     }
     if (!x_ready) {  // else the workspace already holds bf16 X (e.g. a fused LayerNorm)
         const size_t n4 = (size_t)a.n * a.k / 4;
-        long long blocks = (long long)((n4 + 1023) / 1024);
-        const long long cap = (long long)dev.sm_count * 8;
+        const size_t per_cta = (size_t)kXThreads * kXU;
+        long long blocks = (long long)((n4 + per_cta - 1) / per_cta);
+        const long long cap = (long long)dev.sm_count * 4;  // resident at once
         if (blocks > cap) blocks = cap;
-        cudaError_t err = launch_pdl(x_to_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0,
-                                     stream, reinterpret_cast<const float4 *>(a.X),
-                                     reinterpret_cast<uint2 *>(workspace), n4);
+        static std::atomic<unsigned long long> smem_set{0};
+        cudaError_t err = ensure_smem(x_to_bf16_kernel, kXSmem, dev, smem_set);
+        if (err != cudaSuccess) return err;
+        err = launch_pdl(x_to_bf16_kernel, dim3((unsigned)blocks), dim3(kXThreads), kXSmem, stream,
+                         reinterpret_cast<const float4 *>(a.X),
+                         reinterpret_cast<uint2 *>(workspace), n4);
         if (err != cudaSuccess) return err;
     }
     if (gemm_tcp_supported(g)) return launch_gemm_tcp(g, workspace, dev, stream);
