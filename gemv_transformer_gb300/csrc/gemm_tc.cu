@@ -416,6 +416,50 @@ __global__ void w_to_bf16_kernel(const uint8_t *__restrict__ W, int m, int k,
     }
 }
 
+// Quantised W -> bf16 [m][k] when a row is a whole number of 16-byte words
+// (k % 256 == 0): a CTA takes a row at a time, loads its blocks with coalesced
+// 16-byte loads into shared memory, and each thread then decodes 8-weight pieces
+// c = threadIdx.x + 256 u (block c / 4, quarter c % 4) and stores them, so that a
+// warp's store covers 512 contiguous bytes.  Same values as w_to_bf16_kernel.
+template <int WT>
+__global__ void __launch_bounds__(256) w_rows_to_bf16_kernel(const uint8_t *__restrict__ W,
+                                                             int m, int k,
+                                                             uint4 *__restrict__ wb) {
+    pdl_enter();
+    extern __shared__ uint4 rowbuf[];
+    const size_t rb = row_bytes(WT, k);
+    const int words = (int)(rb / 16);
+    const int pieces = k / 8;
+    const uint8_t *sb = reinterpret_cast<const uint8_t *>(rowbuf);
+    for (int j = blockIdx.x; j < m; j += gridDim.x) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(W + (size_t)j * rb);
+        for (int w = threadIdx.x; w < words; w += blockDim.x) rowbuf[w] = __ldg(src + w);
+        __syncthreads();
+        for (int c = threadIdx.x; c < pieces; c += blockDim.x) {
+            const int b = c >> 2, qt = c & 3;
+            const uint8_t *bp = sb + (size_t)b * (WT == kQ8_0 ? 34 : 18);
+            const float d = half_bits_to_f32((uint32_t)bp[0] | ((uint32_t)bp[1] << 8));
+            float w[8];
+            if (WT == kQ8_0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = d * (float)(int8_t)bp[2 + 8 * qt + e];
+            } else {  // quarter qt: low (qt < 2) or high nibbles of code bytes 8 (qt & 1) ..
+                const uint8_t *cb = bp + 2 + 8 * (qt & 1);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t byte = cb[e];
+                    const int code = qt < 2 ? (int)(byte & 15u) : (int)(byte >> 4);
+                    w[e] = d * (float)(code - 8);
+                }
+            }
+            wb[(size_t)j * pieces + c] =
+                make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                           pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+        }
+        __syncthreads();  // the row buffer is refilled next
+    }
+}
+
 // F16 / F32 W -> bf16 [m][k], each element rounded to the nearest bf16 (ties to
 // even).  One thread per 8 weights (k % 8 == 0, rows 16-byte aligned).
 template <int WT>
@@ -461,7 +505,22 @@ cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
         if (grid > (long long)dev.sm_count * 8) grid = (long long)dev.sm_count * 8;
         uint4 *wo = reinterpret_cast<uint4 *>(wb);
         cudaError_t err;
-        switch (wtype) {
+        const bool rows16 = !plain && a.k % 256 == 0 && ((uintptr_t)a.W & 15u) == 0;
+        if (rows16) {  // whole rows through shared memory: coalesced loads and stores
+            // The row buffer's size follows k: above the default 48 KB the limit is
+            // raised for this call (never lowered, so other sizes stay launchable).
+            const int rbytes = (int)row_bytes(wtype, a.k);
+            long long g = a.m < dev.sm_count * 8 ? a.m : (long long)dev.sm_count * 8;
+            auto kern = wtype == kQ8_0 ? w_rows_to_bf16_kernel<kQ8_0> : w_rows_to_bf16_kernel<kQ4_0>;
+            err = rbytes > 48 * 1024
+                      ? cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             rbytes)
+                      : cudaSuccess;
+            if (err == cudaSuccess)
+                err = launch_pdl(kern, dim3((unsigned)g), dim3(256), rbytes, stream, a.W, a.m, a.k,
+                                 wo);
+            if (err != cudaSuccess) return err;
+        } else switch (wtype) {
         case kQ8_0:
             err = launch_pdl(w_to_bf16_kernel<kQ8_0>, dim3((unsigned)grid), dim3(256), 0, stream,
                              a.W, a.m, a.k, wo);
