@@ -86,13 +86,16 @@ def make_workloads():
 def extra_workloads():
     """Measured and reported beside the metric, not part of it: the quantised
     large-n tensor-core GEMM (a prompt through GGML weights), the LayerNorm fused
-    before the encoder qkv projection, and the token-embedding gather."""
+    before the encoder qkv projection, the token-embedding gather, and a q
+    projection without and with a second output band (dual outputs)."""
     import synth
     return [synth.workload_quant_prefill(wtype=synth.WTYPE_Q4_0),
             synth.workload_quant_prefill(wtype=synth.WTYPE_Q8_0),
             synth.workload_ln_qkv(),
             synth.workload_embed(wtype=synth.WTYPE_BF16),
-            synth.workload_embed(wtype=synth.WTYPE_Q4_0)]
+            synth.workload_embed(wtype=synth.WTYPE_Q4_0),
+            synth.workload_dual_q(dual=False),
+            synth.workload_dual_q(dual=True)]
 
 
 def algorithmic(w):
@@ -109,8 +112,8 @@ def algorithmic(w):
     if w["kind"] == "embed":  # the gathered table rows + pos + bias + out + ids
         n = w["n"]
         return n * rb + n * k * 4 + k * 4 + n * k * 4 + n * 4, 0.0
-    n = w["n"]
-    b = m * rb + n * k * 4 + n * m * 4
+    n, dual = w["n"], w.get("dual", 0)
+    b = m * rb + n * k * 4 + n * (m + dual) * 4 + dual * 4
     if w["flags"] & synth.FLAG_BIAS:
         b += m * 4
     if w["flags"] & synth.FLAG_RESIDUAL:
@@ -123,7 +126,7 @@ def kernels_per_call(w):
     quantised W) to bf16 first; every other call is one launch."""
     if w["kind"] == "gemm_ln_tc":
         return 2  # LayerNorm into the workspace, then the GEMM
-    if w["kind"] != "gemm_tc":
+    if w["kind"] not in ("gemm_tc", "gemm_dual_tc"):
         return 1
     return 2 if w["wtype"] == 0 else 3  # quantised W is dequantised to bf16 first
 
@@ -340,7 +343,7 @@ class Launches:
         def out_count(w):
             if w["kind"] == "moe":
                 return w["n_tok"] * w["topk"] * w["m"]
-            return w["n"] * (w["k"] if w["kind"] == "embed" else w["m"])
+            return w["n"] * (w["k"] if w["kind"] == "embed" else w["m"] + w.get("dual", 0))
 
         in_total = sum(nbytes(w["X"]) + nbytes(w["residual"]) +
                        (nbytes(w["ids"]) if w["kind"] in ("moe", "embed") else 0) for w in ws)
@@ -381,11 +384,12 @@ class Launches:
                         else None)
             b["ws"] = None
             b["ln_gb"] = torch.from_numpy(w["ln_gb"]).to(device) if "ln_gb" in w else None
+            b["bias2"] = torch.from_numpy(w["bias2"]).to(device) if "bias2" in w else None
             if w["kind"] == "gemm_ln_tc":
                 need = wq.wq_gemm_ln_workspace_bytes(w["n"], m, k, w["wtype"],
                                                      w["flags"] | wq.WQ_TC_BF16)
                 b["ws"] = torch.empty(need, dtype=torch.uint8, device=device)
-            if w["kind"] == "gemm_tc":
+            if w["kind"] in ("gemm_tc", "gemm_dual_tc"):
                 need = wq.wq_gemm_workspace_bytes(w["n"], m, k, w["wtype"],
                                                   w["flags"] | wq.WQ_TC_BF16)
                 b["ws"] = torch.empty(need, dtype=torch.uint8, device=device)
@@ -410,6 +414,11 @@ class Launches:
             flags = w["flags"] | wq.WQ_TC_BF16
             return wq.wq_gemm_ws(w["n"], w["m"], w["k"], w["wtype"], flags, b["X"], b["W"],
                                  b["bias"], b["R"], b["Y"], b["ws"], b["ws"].numel(), stream)
+        if w["kind"] == "gemm_dual_tc":
+            flags = w["flags"] | wq.WQ_TC_BF16
+            return wq.wq_gemm_dual(w["n"], w["m"], w["k"], w["dual"], w["wtype"], flags, 1.0,
+                                   b["X"], b["W"], b["bias"], b["bias2"], b["R"], b["Y"], b["ws"],
+                                   b["ws"].numel(), stream)
         fn = wq.wq_gemv if w["kind"] == "gemv" else wq.wq_gemm
         return fn(w["n"], w["m"], w["k"], w["wtype"], w["flags"], b["X"], b["W"], b["bias"],
                   b["R"], b["Y"], stream)

@@ -27,7 +27,8 @@ WQ_GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20
 WQ_GEMV_MAX_N = 16
 WQ_MOE_MAX_SLOTS = 256
 
-EXPORTS = ("wq_gemm", "wq_gemm_ws", "wq_gemm_alpha", "wq_gemm_workspace_bytes", "wq_gemm_noalloc",
+EXPORTS = ("wq_gemm", "wq_gemm_ws", "wq_gemm_alpha", "wq_gemm_dual", "wq_gemm_workspace_bytes",
+           "wq_gemm_noalloc",
            "wq_gemm_ln_ws", "wq_gemm_ln_workspace_bytes", "wq_gemv",
            "wq_moe_gemv", "wq_weight_bytes", "wq_dequantize", "wq_embed", "wq_get_device_status",
            "wq_status_string", "wq_set_wait_limit")
@@ -74,6 +75,9 @@ def _open(path: str):
     lib.wq_gemm_alpha.argtypes = [ci, ci, ci, ci, ctypes.c_uint, ctypes.c_float, vp, vp, vp, vp,
                                   vp, vp, sz, vp]
     lib.wq_gemm_alpha.restype = ci
+    lib.wq_gemm_dual.argtypes = [ci, ci, ci, ci, ci, ctypes.c_uint, ctypes.c_float, vp, vp, vp, vp,
+                                 vp, vp, vp, sz, vp]
+    lib.wq_gemm_dual.restype = ci
     lib.wq_embed.argtypes = [ci, ci, ci, ci, vp, vp, vp, vp, vp, vp]
     lib.wq_embed.restype = ci
     lib.wq_get_device_status.argtypes = [vp]
@@ -167,6 +171,13 @@ def wq_gemm_alpha(n, m, k, wtype, flags, alpha, X, W, bias=None, residual=None, 
     return load().wq_gemm_alpha(n, m, k, wtype, flags, float(alpha), _p(X), _p(W), _p(bias),
                                 _p(residual), _p(Y), _p(workspace), int(workspace_bytes),
                                 _s(stream))
+
+
+def wq_gemm_dual(n, m, k, dual, wtype, flags, alpha, X, W, bias=None, bias2=None, residual=None,
+                 Y=None, workspace=None, workspace_bytes=0, stream=None) -> int:
+    return load().wq_gemm_dual(n, m, k, dual, wtype, flags, float(alpha), _p(X), _p(W), _p(bias),
+                               _p(bias2), _p(residual), _p(Y), _p(workspace), int(workspace_bytes),
+                               _s(stream))
 
 
 def wq_embed(n_ids, rows, k, wtype, W, ids, pos=None, bias=None, out=None, stream=None) -> int:

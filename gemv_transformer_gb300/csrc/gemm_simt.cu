@@ -96,7 +96,9 @@ __device__ __forceinline__ void load_w_tile(const GemmArgs &a, int j0, int kk, i
     for (int e = 0; e < 8; ++e) ws[8 * q + e][r] = w[e];
 }
 
-template <int WT>
+// DUAL: also the second output band (columns m.. of Y); a separate instantiation,
+// so that kernels without it carry none of its code.
+template <int WT, bool DUAL>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const GemmArgs a) {
     pdl_enter();
     __shared__ float xs[TK][TI + 4];
@@ -151,8 +153,9 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const GemmArgs a) {
         for (int v = 0; v < 4; ++v) {
             const int j = j0 + tx * 4 + v;
             if (j >= a.m) continue;
-            const size_t o = (size_t)i * a.m + j;
+            const size_t o = (size_t)i * a.ldy + j;
             a.Y[o] = epilogue(acc[u][v], a.flags, a.bias + j, a.R + o, a.alpha);
+            if (DUAL && j < a.dual) a.Y[o + a.m] = acc[u][v] + a.bias2[j];  // the raw second band
         }
     }
 }
@@ -196,7 +199,7 @@ __device__ __forceinline__ void load_w4(const GemmArgs &a, int j, int kk, int q,
     }
 }
 
-template <int WT>
+template <int WT, bool DUAL>
 __global__ void __launch_bounds__(256) gemm_splitk_kernel(const GemmArgs a, int steps_per_rank) {
     pdl_enter();
     namespace cg = cooperative_groups;
@@ -264,8 +267,9 @@ __global__ void __launch_bounds__(256) gemm_splitk_kernel(const GemmArgs a, int 
             if (r < KS) sum += p[r];
         const int i = i0 + idx / SK, j = j0 + idx % SK;
         if (i < a.n && j < a.m) {
-            const size_t o = (size_t)i * a.m + j;
+            const size_t o = (size_t)i * a.ldy + j;
             a.Y[o] = epilogue(sum, a.flags, a.bias + j, a.R + o, a.alpha);
+            if (DUAL && j < a.dual) a.Y[o + a.m] = sum + a.bias2[j];  // the raw second band
         }
     }
     cluster.sync();  // every rank keeps its shared memory until all slices are read
@@ -288,7 +292,8 @@ cudaError_t launch_splitk_wt(const GemmArgs &a, int tiles_m, int tiles_n, int ks
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_splitk_kernel<WT>, a, spr);
+    if (a.dual > 0) return cudaLaunchKernelEx(&cfg, gemm_splitk_kernel<WT, true>, a, spr);
+    return cudaLaunchKernelEx(&cfg, gemm_splitk_kernel<WT, false>, a, spr);
 }
 
 template <int WT>
@@ -391,12 +396,21 @@ cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev
         }
     }
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+    if (a.dual > 0) {
+        switch (wtype) {
+        case kBF16: return launch_pdl(gemm_simt_kernel<kBF16, true>, grid, dim3(256), 0, stream, a);
+        case kF16: return launch_pdl(gemm_simt_kernel<kF16, true>, grid, dim3(256), 0, stream, a);
+        case kF32: return launch_pdl(gemm_simt_kernel<kF32, true>, grid, dim3(256), 0, stream, a);
+        case kQ8_0: return launch_pdl(gemm_simt_kernel<kQ8_0, true>, grid, dim3(256), 0, stream, a);
+        default: return launch_pdl(gemm_simt_kernel<kQ4_0, true>, grid, dim3(256), 0, stream, a);
+        }
+    }
     switch (wtype) {
-    case kBF16: return launch_pdl(gemm_simt_kernel<kBF16>, grid, dim3(256), 0, stream, a);
-    case kF16: return launch_pdl(gemm_simt_kernel<kF16>, grid, dim3(256), 0, stream, a);
-    case kF32: return launch_pdl(gemm_simt_kernel<kF32>, grid, dim3(256), 0, stream, a);
-    case kQ8_0: return launch_pdl(gemm_simt_kernel<kQ8_0>, grid, dim3(256), 0, stream, a);
-    default: return launch_pdl(gemm_simt_kernel<kQ4_0>, grid, dim3(256), 0, stream, a);
+    case kBF16: return launch_pdl(gemm_simt_kernel<kBF16, false>, grid, dim3(256), 0, stream, a);
+    case kF16: return launch_pdl(gemm_simt_kernel<kF16, false>, grid, dim3(256), 0, stream, a);
+    case kF32: return launch_pdl(gemm_simt_kernel<kF32, false>, grid, dim3(256), 0, stream, a);
+    case kQ8_0: return launch_pdl(gemm_simt_kernel<kQ8_0, false>, grid, dim3(256), 0, stream, a);
+    default: return launch_pdl(gemm_simt_kernel<kQ4_0, false>, grid, dim3(256), 0, stream, a);
     }
 }
 

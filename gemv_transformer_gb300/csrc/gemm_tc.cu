@@ -219,46 +219,60 @@ __global__ void __launch_bounds__(Roles<ATMA>::kThreads, 1)
             constexpr int kStage = 36;               // staging row stride (floats)
             // The operand stages are idle now: every MMA has completed.
             float *stg = reinterpret_cast<float *>(smem) + cw * 32 * kStage;
-            const bool vec = (a.m & 3) == 0;
+            // 16-byte stores where every row of Y (and of the residual, and the second
+            // band at column m) starts 16-byte aligned.
+            const bool vec = ((a.ldy | a.m) & 3) == 0 && ((uintptr_t)a.Y & 15u) == 0 &&
+                             (!(a.flags & kResidual) || ((uintptr_t)a.R & 15u) == 0);
             for (int c0 = cg * CW; c0 < (cg + 1) * CW; c0 += 32) {
-                float v[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
                 const int jb = j0 + c0;
-                if (a.flags & (kBias | kActs)) {
+                // Band 0: epi(sums) into columns < m; band 1 (blocks left of dual): the
+                // same sums + bias2, no activation, alpha or residual, at column m + j.
+                for (int band = 0; band < (jb < a.dual ? 2 : 1); ++band) {
+                    float v[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+                    if (band == 1) {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        float t = v[c];
-                        if (a.flags & kBias) t += (jb + c < a.m) ? __ldg(a.bias + jb + c) : 0.f;
-                        v[c] = a.alpha * activate(t, a.flags);
-                    }
-                }
-                // Row `lane` of the 32x32 block into shared memory...
+                        for (int c = 0; c < 32; ++c)
+                            v[c] += (jb + c < a.dual) ? __ldg(a.bias2 + jb + c) : 0.f;
+                    } else if (a.flags & (kBias | kActs)) {
 #pragma unroll
-                for (int c = 0; c < 32; c += 4)
-                    *reinterpret_cast<float4 *>(&stg[lane * kStage + c]) =
-                        make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
-                __syncwarp();
-                // ...then four rows of 128 bytes per warp instruction to global.
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int rr = it * 4 + (lane >> 3), cc = (lane & 7) * 4;
-                    const int row = i0 + q * 32 + rr, col = jb + cc;
-                    if (row >= a.n || col >= a.m) continue;
-                    float4 o = *reinterpret_cast<const float4 *>(&stg[rr * kStage + cc]);
-                    const size_t off = (size_t)row * a.m + col;
-                    if (vec && col + 4 <= a.m) {
-                        if (a.flags & kResidual) {
-                            const float4 r4 = *reinterpret_cast<const float4 *>(a.R + off);
-                            o.x += r4.x; o.y += r4.y; o.z += r4.z; o.w += r4.w;
+                        for (int c = 0; c < 32; ++c) {
+                            float t = v[c];
+                            if (a.flags & kBias) t += (jb + c < a.m) ? __ldg(a.bias + jb + c) : 0.f;
+                            v[c] = a.alpha * activate(t, a.flags);
                         }
-                        *reinterpret_cast<float4 *>(a.Y + off) = o;
-                    } else {
-                        const float ov[4] = {o.x, o.y, o.z, o.w};
-                        for (int e = 0; e < 4 && col + e < a.m; ++e)
-                            a.Y[off + e] = ov[e] + ((a.flags & kResidual) ? a.R[off + e] : 0.f);
                     }
+                    // Row `lane` of the 32x32 block into shared memory...
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4 *>(&stg[lane * kStage + c]) =
+                            make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+                    __syncwarp();
+                    // ...then four rows of 128 bytes per warp instruction to global.
+                    const int lim = band ? a.dual : a.m;
+                    const bool res = !band && (a.flags & kResidual);
+                    float *yb = a.Y + (band ? a.m : 0);
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = it * 4 + (lane >> 3), cc = (lane & 7) * 4;
+                        const int row = i0 + q * 32 + rr, col = jb + cc;
+                        if (row >= a.n || col >= lim) continue;
+                        float4 o = *reinterpret_cast<const float4 *>(&stg[rr * kStage + cc]);
+                        const size_t off = (size_t)row * a.ldy + col;
+                        if (vec && col + 4 <= lim) {
+                            if (res) {
+                                const float4 r4 = *reinterpret_cast<const float4 *>(a.R + off);
+                                o.x += r4.x; o.y += r4.y; o.z += r4.z; o.w += r4.w;
+                            }
+                            *reinterpret_cast<float4 *>(yb + off) = o;
+                        } else {
+                            const float ov[4] = {o.x, o.y, o.z, o.w};
+                            for (int e = 0; e < 4 && col + e < lim; ++e)
+                                yb[off + e] = ov[e] + (res ? a.R[off + e] : 0.f);
+                        }
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
     }

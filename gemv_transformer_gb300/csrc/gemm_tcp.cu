@@ -94,17 +94,21 @@ __host__ __device__ constexpr int help_split(int KB, int h) {
     return KB - ((3 * KB) / (4 * (h + 1)) > 1 ? (3 * KB) / (4 * (h + 1)) : 1);
 }
 
-template <int BN, int KS, int SCH>
+// DUAL: the epilogue also writes the second output band (columns m.. of Y); a
+// separate instantiation, so that kernels without it carry none of its code.
+template <int BN, int KS, int SCH, bool DUAL = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcp_kernel(const __grid_constant__ CUtensorMap wmap,
                     const __grid_constant__ CUtensorMap xmap,
                     const __grid_constant__ CUtensorMap ymap,
-                    const __grid_constant__ CUtensorMap rmap, const GemmArgs a) {
+                    const __grid_constant__ CUtensorMap rmap,
+                    const __grid_constant__ CUtensorMap y2map, const GemmArgs a) {
     // Barriers, tensor memory and descriptors are set up before waiting for the
     // previous grid (they touch nothing it writes); global memory after.
     pdl_launch();
     using L = PLayout<BN, KS, SCH>;
     constexpr bool PAIR = SCH == kPair, HELP = SCH == kHelp;
+    static_assert(!(DUAL && HELP), "the helper schedule has no second band");
     constexpr int S = L::kStages;
     constexpr int TM = PAIR ? 2 * BM : BM;  // tile rows
     extern __shared__ uint8_t smem_raw[];
@@ -163,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&wmap);
         prefetch_tmap(&ymap);
         if (a.flags & kResidual) prefetch_tmap(&rmap);
+        if (DUAL) prefetch_tmap(&y2map);
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -514,6 +519,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_commit();
                 }
                 stored = true;
+                if (DUAL && jb < a.dual) {
+                    // The second band: the same sums + bias2, no activation, alpha or
+                    // residual, at column m + jb (the map clips columns past dual).
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) +
+                                  (uint32_t)(b * BN + (cg + 4 * u) * 32),
+                              v);
+                    if (HELP) {
+                        const uint8_t *pp = sA + ew * kStgBytes + lane * 128;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 pv =
+                                *reinterpret_cast<const float4 *>(pp + ((j ^ (lane & 7)) << 4));
+                            v[4 * j] += pv.x;
+                            v[4 * j + 1] += pv.y;
+                            v[4 * j + 2] += pv.z;
+                            v[4 * j + 3] += pv.w;
+                        }
+                    }
+                    const float b2 = jb + lane < a.dual ? __ldg(a.bias2 + jb + lane) : 0.f;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[c] += __shfl_sync(0xFFFFFFFFu, b2, c);
+                    if (lane == 0) bulk_wait_read0();  // the block above has left stg
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&y2map, jb, r0, stg);
+                        bulk_commit();
+                    }
+                }
             }
             // This accumulator may be refilled.
             tc_fence_before();
@@ -562,11 +601,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool encode_2d(CUtensorMap &map, CUtensorMapDataType dt, int esize, const void *base, int cols,
-               int rows, int box_cols, int box_rows) {
+               int rows, int box_cols, int box_rows, int ld = 0) {
     auto encode = encode_fn();
     if (!encode) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld > 0 ? ld : cols) * esize};
     const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return encode(&map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
@@ -609,24 +648,31 @@ int max_clusters(Kernel kern, int smem, int csize, const DeviceInfo &dev) {
     return clusters;
 }
 
-template <int BN, int KS, int SCH>
+template <int BN, int KS, int SCH, bool DUAL = false>
 cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
                       cudaStream_t stream, int clusters = 0) {
     using L = PLayout<BN, KS, SCH>;
     constexpr int TM = SCH == kPair ? 2 * BM : BM;
     static std::atomic<unsigned long long> smem_set{0};
-    CUtensorMap wmap, xmap, ymap, rmap;
+    CUtensorMap wmap, xmap, ymap, rmap, y2map;
     if (!encode_2d(wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.W, a.k, a.m, BK, L::kBRows) ||
         !encode_2d(xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xb, a.k, a.n, BK, BM) ||
-        !encode_2d(ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.Y, a.m, a.n, 32, 32))
+        !encode_2d(ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.Y, a.m, a.n, 32, 32, a.ldy))
         return cudaErrorInvalidValue;
     if (a.flags & kResidual) {
-        if (!encode_2d(rmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.m, a.n, 32, 32))
+        if (!encode_2d(rmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.m, a.n, 32, 32, a.ldy))
             return cudaErrorInvalidValue;
     } else {
         rmap = ymap;  // unused
     }
-    auto kern = gemm_tcp_kernel<BN, KS, SCH>;
+    if (DUAL) {  // the second band: columns m .. m + dual of each row of Y
+        if (!encode_2d(y2map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.Y + a.m, a.dual, a.n, 32, 32,
+                       a.ldy))
+            return cudaErrorInvalidValue;
+    } else {
+        y2map = ymap;  // unused
+    }
+    auto kern = gemm_tcp_kernel<BN, KS, SCH, DUAL>;
     static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
     cudaError_t err = ensure_smem(kern, (int)L::kBytes, dev, smem_set);
     if (err != cudaSuccess) return err;
@@ -634,7 +680,7 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
     if (SCH == kData) {
         const int grid = (int)(tiles < dev.sm_count ? tiles : dev.sm_count);
         return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kBytes, stream, wmap, xmap, ymap,
-                          rmap, a);
+                          rmap, y2map, a);
     }
     // Pair mode: up to `clusters` pairs walk the tiles.  Helper mode: `clusters`
     // is h, one cluster of h + 1 CTAs per h tiles.
@@ -655,14 +701,15 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, wmap, xmap, ymap, rmap, a);
+    return cudaLaunchKernelEx(&cfg, kern, wmap, xmap, ymap, rmap, y2map, a);
 }
 
 }  // namespace
 
 bool gemm_tcp_supported(const GemmArgs &a) {
-    // TMA stores need 16-byte aligned rows of Y (and of the residual).
-    if (a.m % 4 != 0 || ((uintptr_t)a.Y & 15u)) return false;
+    // TMA stores need 16-byte aligned rows of Y (and of the residual, and of the
+    // second band at column m).
+    if (a.m % 4 != 0 || a.ldy % 4 != 0 || ((uintptr_t)a.Y & 15u)) return false;
     if ((a.flags & kResidual) && ((uintptr_t)a.R & 15u)) return false;
     return encode_fn() != nullptr;
 }
@@ -716,12 +763,14 @@ cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo 
         }
     }
     const long long kb128 = (a.k + 2 * BK - 1) / (2 * BK);  // 128-k stages
-    // The helper schedule parks partial sums in Y: only when Y is not the residual.
-    const size_t ybytes = (size_t)a.n * a.m * sizeof(float);
+    // The helper schedule parks partial sums in Y: only when Y is not the residual,
+    // and only without a second band.
+    const size_t ybytes = (size_t)a.n * a.ldy * sizeof(float);
     const uintptr_t y0 = (uintptr_t)a.Y, r0 = (uintptr_t)a.R;
     const bool y_free = !(a.flags & kResidual) || r0 + ybytes <= y0 || y0 + ybytes <= r0;
     int owners = 0;
-    for (int hh = 2; hh <= 3 && y_free && kb128 >= hh + 1 && tiles128 >= hh; ++hh) {
+    for (int hh = 2; hh <= 3 && y_free && a.dual == 0 && kb128 >= hh + 1 && tiles128 >= hh;
+         ++hh) {
         // Only when every cluster is resident at once (one round).
         const int fit = max_clusters(gemm_tcp_kernel<128, 2, kHelp>, (int)LH::kBytes, hh + 1, dev);
         const long long need = (tiles128 + hh - 1) / hh;
@@ -732,6 +781,14 @@ cudaError_t launch_gemm_tcp(const GemmArgs &a, const void *xb, const DeviceInfo 
             best = th;
             pick = 3;
             owners = hh;
+        }
+    }
+    if (a.dual > 0) {
+        switch (pick) {
+            case 1: return launch_bn<256, 1, kData, true>(a, xb, dev, stream);
+            case 2: return launch_bn<256, 1, kPair, true>(a, xb, dev, stream, pairs);
+            case 4: return launch_bn<192, 1, kPair, true>(a, xb, dev, stream, pairs);
+            default: return launch_bn<128, 2, kData, true>(a, xb, dev, stream);
         }
     }
     switch (pick) {

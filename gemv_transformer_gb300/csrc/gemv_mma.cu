@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (row < m) {
                             if (a.flags & kResidual) {
                                 const int yrow = MOE ? s_sorted[seg0 + p0 + i] : p0 + i;
-                                cp_async4(&s_res[idx], a.R + (size_t)yrow * m + row);
+                                cp_async4(&s_res[idx], a.R + (size_t)yrow * (MOE ? m : a.ldy) + row);
                             }
                             if (i == 0 && (a.flags & kBias))
                                 cp_async4(&s_bias[r], a.bias + (MOE ? (size_t)e * m + row : (size_t)row));
@@ -733,7 +733,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v += packed ? rp[i] + rp[P + i] : rp[i];
                         }
                         const int yrow = MOE ? s_sorted[seg0 + p0 + i] : p0 + i;
-                        a.Y[(size_t)yrow * m + row] = epilogue_vals(v, a.flags, s_bias[r], s_res[idx], a.alpha);
+                        // MoE has no second band: its rows are m wide.
+                        float *yp = a.Y + (size_t)yrow * (MOE ? m : a.ldy) + row;
+                        *yp = epilogue_vals(v, a.flags, s_bias[r], s_res[idx], a.alpha);
+                        if (!MOE && row < a.dual) yp[m] = v + a.bias2[row];  // the raw second band
                     }
                 }
                 consumers_sync();

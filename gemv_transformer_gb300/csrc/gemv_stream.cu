@@ -312,9 +312,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) stream_kernel(const StreamArgs
         if (p == P - 1) {  // row done: epilogue and store
             for (int r = lane; r < ns; r += 32) {
                 const int yrow = MOE ? s_sorted[seg0 + r] : r;
-                const size_t o = (size_t)yrow * m + j;
+                const size_t o = (size_t)yrow * a.ldy + j;
                 const float *bj = a.bias + (MOE ? (size_t)e * m + j : (size_t)j);
                 a.Y[o] = epilogue(tot[r], a.flags, bj, a.R + o, a.alpha);
+                if (j < a.dual) a.Y[o + m] = tot[r] + a.bias2[j];  // the raw second band
             }
         }
         __syncwarp();

@@ -51,6 +51,20 @@ wq_status check_common(int n, int m, int k, int wtype, unsigned flags, const flo
     if (!aligned16(X) || !aligned16(W)) return WQ_ERR_INVALID_ARG;
     return WQ_OK;
 }
+
+// The epilogue's parts beyond the flags (wavo 0.3.0 src/gpu/mod.rs): the scale of
+// Epilogue::Residual(a), and the `dual` outputs of Gpu::linear, written a second
+// time after the m others with their own bias and no epilogue.
+struct Extra {
+    float alpha = 1.0f;
+    int dual = 0;
+    const float *bias2 = nullptr;
+};
+
+template <typename Args>
+void fill_args(Args &a, int n, int m, int k, unsigned flags, const float *X, const void *W,
+               const float *bias, const float *residual, float *Y, const DeviceInfo &dev,
+               const Extra &ex);
 }  // namespace
 
 wq_status check_gemm_args(int n, int m, int k, int wtype, unsigned flags, const float *X,
@@ -82,6 +96,29 @@ unsigned long long wait_limit() {
     return g_wait_limit;
 }
 
+namespace {
+template <typename Args>
+void fill_args(Args &a, int n, int m, int k, unsigned flags, const float *X, const void *W,
+               const float *bias, const float *residual, float *Y, const DeviceInfo &dev,
+               const Extra &ex) {
+    a.X = X;
+    a.W = static_cast<const uint8_t *>(W);
+    a.bias = bias;
+    a.R = residual;
+    a.Y = Y;
+    a.n = n;
+    a.m = m;
+    a.k = k;
+    a.flags = flags & WQ_EPILOGUE_FLAGS;
+    a.status = dev.status;
+    a.wait_limit = wait_limit();
+    a.alpha = ex.alpha;
+    a.ldy = m + ex.dual;
+    a.dual = ex.dual;
+    a.bias2 = ex.bias2;
+}
+}  // namespace
+
 }  // namespace wq
 
 using namespace wq;
@@ -96,22 +133,11 @@ size_t wq_weight_bytes(int wtype, int m, int k) {
 
 static wq_status gemv_impl(int n, int m, int k, int wtype, unsigned flags, const float *X,
                            const void *W, const float *bias, const float *residual, float *Y,
-                           wq_stream_t stream, float alpha = 1.0f) {
+                           wq_stream_t stream, const Extra &ex = Extra()) {
     const DeviceInfo *dev = device_info();
     if (!dev) return WQ_ERR_CUDA;
     StreamArgs a{};
-    a.X = X;
-    a.W = static_cast<const uint8_t *>(W);
-    a.bias = bias;
-    a.R = residual;
-    a.Y = Y;
-    a.n = n;
-    a.m = m;
-    a.k = k;
-    a.flags = flags & WQ_EPILOGUE_FLAGS;
-    a.status = dev->status;
-    a.wait_limit = wait_limit();
-    a.alpha = alpha;
+    fill_args(a, n, m, k, flags, X, W, bias, residual, Y, *dev, ex);
     if (mma_gemv_supported(wtype, k))
         return cuda_status(launch_mma_gemv(a, wtype, *dev, (cudaStream_t)stream));
     return cuda_status(launch_stream_gemv(a, wtype, *dev, (cudaStream_t)stream));
@@ -128,26 +154,15 @@ wq_status wq_gemv(int n, int m, int k, int wtype, unsigned flags, const float *X
 // wq_gemm after its argument checks.
 static wq_status gemm_impl(int n, int m, int k, int wtype, unsigned flags, const float *X,
                            const void *W, const float *bias, const float *residual, float *Y,
-                           wq_stream_t stream, float alpha) {
+                           wq_stream_t stream, const Extra &ex) {
     if (n <= WQ_GEMV_MAX_N)
-        return gemv_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, alpha);
+        return gemv_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, ex);
     // Tensor cores with quantised W need the bf16 copy of W: wq_gemm_ws.
     if ((flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
     const DeviceInfo *dev = device_info();
     if (!dev) return WQ_ERR_CUDA;
     GemmArgs a{};
-    a.X = X;
-    a.W = static_cast<const uint8_t *>(W);
-    a.bias = bias;
-    a.R = residual;
-    a.Y = Y;
-    a.n = n;
-    a.m = m;
-    a.k = k;
-    a.flags = flags & WQ_EPILOGUE_FLAGS;
-    a.status = dev->status;
-    a.wait_limit = wait_limit();
-    a.alpha = alpha;
+    fill_args(a, n, m, k, flags, X, W, bias, residual, Y, *dev, ex);
     if (flags & WQ_TC_BF16) return cuda_status(launch_gemm_tc(a, *dev, (cudaStream_t)stream));
     return cuda_status(launch_gemm_simt(a, wtype, *dev, (cudaStream_t)stream));
 }
@@ -156,7 +171,7 @@ wq_status wq_gemm(int n, int m, int k, int wtype, unsigned flags, const float *X
                   const float *bias, const float *residual, float *Y, wq_stream_t stream) {
     wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
     if (s != WQ_OK) return s;
-    return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, 1.0f);
+    return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, Extra());
 }
 
 size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned flags) {
@@ -170,27 +185,16 @@ size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned flags) {
 static wq_status gemm_ws_impl(int n, int m, int k, int wtype, unsigned flags, const float *X,
                               const void *W, const float *bias, const float *residual, float *Y,
                               void *workspace, size_t workspace_bytes, wq_stream_t stream,
-                              float alpha) {
+                              const Extra &ex) {
     const size_t need = wq_gemm_workspace_bytes(n, m, k, wtype, flags);
     if (need == 0)
-        return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, alpha);
+        return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, ex);
     if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < need)
         return WQ_ERR_INVALID_ARG;
     const DeviceInfo *dev = device_info();
     if (!dev) return WQ_ERR_CUDA;
     GemmArgs a{};
-    a.X = X;
-    a.W = static_cast<const uint8_t *>(W);
-    a.bias = bias;
-    a.R = residual;
-    a.Y = Y;
-    a.n = n;
-    a.m = m;
-    a.k = k;
-    a.flags = flags & WQ_EPILOGUE_FLAGS;
-    a.status = dev->status;
-    a.wait_limit = wait_limit();
-    a.alpha = alpha;
+    fill_args(a, n, m, k, flags, X, W, bias, residual, Y, *dev, ex);
     return cuda_status(launch_gemm_tc_ws(a, wtype, workspace, *dev, (cudaStream_t)stream));
 }
 
@@ -200,19 +204,29 @@ wq_status wq_gemm_ws(int n, int m, int k, int wtype, unsigned flags, const float
     wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
     if (s != WQ_OK) return s;
     return gemm_ws_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, workspace,
-                        workspace_bytes, stream, 1.0f);
+                        workspace_bytes, stream, Extra());
+}
+
+wq_status wq_gemm_dual(int n, int m, int k, int dual, int wtype, unsigned flags, float alpha,
+                       const float *X, const void *W, const float *bias, const float *bias2,
+                       const float *residual, float *Y, void *workspace, size_t workspace_bytes,
+                       wq_stream_t stream) {
+    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
+    if (s != WQ_OK) return s;
+    if (!std::isfinite(alpha)) return WQ_ERR_INVALID_ARG;
+    if (dual < 0 || dual > m || (dual > 0 && !bias2)) return WQ_ERR_INVALID_ARG;
+    const Extra ex{alpha, dual, dual > 0 ? bias2 : nullptr};
+    if (!workspace)
+        return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, ex);
+    return gemm_ws_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, workspace,
+                        workspace_bytes, stream, ex);
 }
 
 wq_status wq_gemm_alpha(int n, int m, int k, int wtype, unsigned flags, float alpha,
                         const float *X, const void *W, const float *bias, const float *residual,
                         float *Y, void *workspace, size_t workspace_bytes, wq_stream_t stream) {
-    wq_status s = check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
-    if (s != WQ_OK) return s;
-    if (!std::isfinite(alpha)) return WQ_ERR_INVALID_ARG;
-    if (!workspace)
-        return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, alpha);
-    return gemm_ws_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, workspace,
-                        workspace_bytes, stream, alpha);
+    return wq_gemm_dual(n, m, k, 0, wtype, flags, alpha, X, W, bias, nullptr, residual, Y,
+                        workspace, workspace_bytes, stream);
 }
 
 size_t wq_gemm_ln_workspace_bytes(int n, int m, int k, int wtype, unsigned flags) {
@@ -243,17 +257,8 @@ wq_status wq_gemm_ln_ws(int n, int m, int k, int wtype, unsigned flags, const fl
         return wq_gemm(n, m, k, wtype, flags & ~(unsigned)WQ_TC_BF16,
                        static_cast<const float *>(workspace), W, bias, residual, Y, stream);
     GemmArgs a{};
-    a.X = X;  // not read: the GEMM takes the bf16 rows from the workspace
-    a.W = static_cast<const uint8_t *>(W);
-    a.bias = bias;
-    a.R = residual;
-    a.Y = Y;
-    a.n = n;
-    a.m = m;
-    a.k = k;
-    a.flags = flags & WQ_EPILOGUE_FLAGS;
-    a.status = dev->status;
-    a.wait_limit = wait_limit();
+    // X is not read: the GEMM takes the bf16 rows from the workspace.
+    fill_args(a, n, m, k, flags, X, W, bias, residual, Y, *dev, Extra());
     return cuda_status(launch_gemm_tc_ws(a, wtype, workspace, *dev, (cudaStream_t)stream, true));
 }
 
@@ -269,20 +274,10 @@ wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtyp
     const DeviceInfo *dev = device_info();
     if (!dev) return WQ_ERR_CUDA;
     StreamArgs a{};
-    a.X = X;
-    a.W = static_cast<const uint8_t *>(Wbank);
-    a.bias = bias;
-    a.R = residual;
-    a.Y = Y;
+    fill_args(a, n_tok, m, k, flags, X, Wbank, bias, residual, Y, *dev, Extra());
     a.ids = ids;
-    a.n = n_tok;
-    a.m = m;
-    a.k = k;
-    a.flags = flags & WQ_EPILOGUE_FLAGS;
     a.topk = topk;
     a.n_experts = n_experts;
-    a.status = dev->status;
-    a.wait_limit = wait_limit();
     if (mma_gemv_supported(wtype, k))
         return cuda_status(launch_mma_moe(a, wtype, *dev, (cudaStream_t)stream));
     return cuda_status(launch_stream_moe(a, wtype, *dev, (cudaStream_t)stream));

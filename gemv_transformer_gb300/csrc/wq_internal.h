@@ -26,6 +26,9 @@ struct StreamArgs {
     unsigned *status;      // device status word
     unsigned long long wait_limit;
     float alpha = 1.0f;    // scale of the contribution before the residual
+    int ldy = 0;           // row stride of Y and R: m + dual (MoE: m)
+    int dual = 0;          // GEMV: columns j < dual also stored as acc + bias2[j] at m + j
+    const float *bias2 = nullptr;  // [dual]
 };
 
 struct GemmArgs {
@@ -39,6 +42,9 @@ struct GemmArgs {
     unsigned *status;
     unsigned long long wait_limit;
     float alpha = 1.0f;    // scale of the contribution before the residual
+    int ldy = 0;           // row stride of Y and R: m + dual
+    int dual = 0;          // columns j < dual also stored as acc + bias2[j] at m + j
+    const float *bias2 = nullptr;  // [dual]
 };
 
 struct DeviceInfo {

@@ -9,20 +9,22 @@
  *
  * Sources of each operation (page title, item):
  *   - wq_gemm: cortiq-engine 0.8.49, src/gpu_wgpu/nemotron_audio.rs,
- *     AudioEncoder::gemm and its kernel ae_gemm ("Y[n.m] (=|+=) X[n.k] . W[m.k]^T
- *     (+bias) (gelu); W bf16 pairs"), epilogue ae_put, masked store ae_store;
+ *     AudioEncoder::gemm and its kernel ae_gemm (Y[n][m] set or accumulated from
+ *     X[n][k] . W[m][k]^T, optional bias and GELU, W as bf16 pairs), epilogue
+ *     ae_put, masked store ae_store;
  *     wavo 0.3.0, src/gpu/mod.rs, Pass::gemm (Q8_0 weights).
  *   - wq_gemv: hanzo-ml 0.11.13, src/wgpu_backend.rs, matvec_q8_0_gpu /
- *     matvec_q4_0_gpu ("y[nout] = Wq * x[k]", raw GGML blocks read in place);
+ *     matvec_q4_0_gpu (y[nout] = Wq x[k] with the raw GGML blocks read in place);
  *     wavo 0.3.0, Pass::gemv (one activation row).
- *   - wq_moe_gemv: hanzo-ml 0.11.13, moe_matvec_gpu ("y[s, r] = sum_k
- *     W[ids[s], r, k] * x[s, k]" over one bank [E, rows, k], router gather and
+ *   - wq_moe_gemv: hanzo-ml 0.11.13, moe_matvec_gpu (y[s][r] = sum over k of
+ *     W[ids[s]][r][k] x[s][k] over one bank [E][rows][k], router gather and
  *     expert matvec in one dispatch).
  *   - wq_gemm_alpha: wavo 0.3.0, src/gpu/mod.rs, Epilogue::Residual(a)
- *     ("c += a(aW^T + b)") on the routes of wq_gemm / wq_gemm_ws.
+ *     (c += alpha (a W^T + b)) on the routes of wq_gemm / wq_gemm_ws.
+ *   - wq_gemm_dual: wavo 0.3.0, src/gpu/mod.rs, Gpu::linear (dual outputs).
  *   - wq_dequantize: the block formats themselves (same pages).
- *   - wq_embed: wavo 0.3.0, src/gpu/mod.rs, Recorder::embed ("row ids[i] of the
- *     table + pos[offset..] + the table's bias, k values") and its test
+ *   - wq_embed: wavo 0.3.0, src/gpu/mod.rs, Recorder::embed (table row ids[i]
+ *     plus a position row plus the table's bias, k values each) and its test
  *     gemv_and_embed.
  *   - wq_get_device_status: wavo 0.3.0, Gpu "failure" (the first device error is
  *     reported by the next call) and its completion marks.
@@ -257,8 +259,8 @@ WQ_API size_t wq_weight_bytes(int wtype, int m, int k);
 WQ_API wq_status wq_dequantize(int wtype, int m, int k, const void *W, float *out, wq_stream_t stream);
 
 /* wq_gemm / wq_gemm_ws with the epilogue's contribution scaled by alpha before
- * the residual is added: wavo 0.3.0 src/gpu/mod.rs, Epilogue::Residual(a),
- * "c += a(aW^T + b)":
+ * the residual is added: wavo 0.3.0 src/gpu/mod.rs, Epilogue::Residual(a), which
+ * accumulates alpha times the biased product into c:
  *   Y[i][j] = (WQ_RESIDUAL ? residual[i][j] : 0) + alpha * act(X.W^T + bias),
  * the product and sum in f32.  workspace NULL: the routes of wq_gemm; otherwise
  * those of wq_gemm_ws, with the same workspace rules.  alpha = 1 gives results
@@ -269,6 +271,27 @@ WQ_API wq_status wq_gemm_alpha(int n, int m, int k, int wtype, unsigned flags, f
                                const float *X, const void *W, const float *bias,
                                const float *residual, float *Y, void *workspace,
                                size_t workspace_bytes, wq_stream_t stream);
+
+/*
+ * wq_gemm_alpha with `dual` outputs: wavo 0.3.0 src/gpu/mod.rs, Gpu::linear (a
+ * bias with `dual` more values than rows has the first `dual` outputs written a
+ * second time after the others, with those biases: one q projection with two
+ * position biases) and its gemm test (the extra columns carry no epilogue):
+ *   Y[i][j]     = (WQ_RESIDUAL ? residual[i][j] : 0) + alpha * act(X.W^T + bias)[i][j],  j < m
+ *   Y[i][m + j] = (X.W^T)[i][j] + bias2[j],                                           j < dual
+ * Y and residual: f32 [n][m + dual], row stride m + dual (residual may equal Y;
+ * its columns m.. are not read).  bias2: f32 [dual] on the device, required when
+ * dual > 0.  0 <= dual <= m; dual = 0 is wq_gemm_alpha.  Both bands come from one
+ * accumulation: W is read once, and Y[i][m + j] - bias2[j] is bit-identical to the
+ * sum that feeds column j.  workspace NULL: the routes of wq_gemm; otherwise those
+ * of wq_gemm_ws, with the same workspace rules.
+ * Errors: as wq_gemm_alpha, plus WQ_ERR_INVALID_ARG for dual < 0, dual > m, or a
+ * null bias2 with dual > 0.
+ */
+WQ_API wq_status wq_gemm_dual(int n, int m, int k, int dual, int wtype, unsigned flags,
+                              float alpha, const float *X, const void *W, const float *bias,
+                              const float *bias2, const float *residual, float *Y,
+                              void *workspace, size_t workspace_bytes, wq_stream_t stream);
 
 /* Embedding row gather: for t < n_ids and j < k,
  *   out[t][j] = W[ids[t]][j] + pos[t][j] + bias[j]

@@ -70,6 +70,9 @@ def _load():
             lib.oracle_gemm_alpha.argtypes = [ci, ci, ci, ci, cu, ci, f64, vp, vp, vp, vp, vp, vp,
                                               ci, ci, ci]
             lib.oracle_gemm_alpha.restype = ci
+            lib.oracle_gemm_dual.argtypes = [ci, ci, ci, ci, ci, cu, ci, f64, vp, vp, vp, vp, vp,
+                                             vp, vp, ci, ci, ci]
+            lib.oracle_gemm_dual.restype = ci
             lib.oracle_moe.argtypes = [ci, ci, ci, ci, ci, ci, cu, vp, vp, vp, vp, vp, vp, vp,
                                        ci, ci, ci]
             lib.oracle_moe.restype = ci
@@ -133,26 +136,32 @@ def dequant(wtype: int, m: int, k: int, W: np.ndarray) -> np.ndarray:
 
 
 def gemm(n, m, k, wtype, flags, X, W, bias=None, residual=None, round_x=False,
-         rows=None, threads=0, bound=True, round_w=False, alpha=1.0):
-    """f64 ``(Y [n][m], S [n][m])`` of ``epi(X . W^T)``.
+         rows=None, threads=0, bound=True, round_w=False, alpha=1.0, dual=0, bias2=None):
+    """f64 ``(Y, S)`` of ``epi(X . W^T)``, each ``[n][m + dual]``.
 
     ``alpha`` scales the contribution before the residual is added (wavo's
     ``Residual(alpha)``: ``Y = R + alpha * act(X . W^T + bias)``); S scales with it.
 
+    ``dual`` (wavo's dual outputs): columns ``m + j`` for ``j < dual`` hold the
+    plain sum of output ``j`` plus ``bias2[j]``, with no activation, alpha or
+    residual; ``residual`` then has rows of ``m + dual`` values too.
+
     ``round_x`` / ``round_w`` feed X / the dequantised W rounded to the nearest
     bf16 (ties to even): the operands of the tensor-core path.
 
-    ``rows=(j0, j1)`` restricts the computed output columns (W rows) to
-    ``[j0, j1)``; the rest of Y and S stays NaN.
+    ``rows=(j0, j1)`` restricts the computed outputs to those of W rows
+    ``[j0, j1)`` (with their dual columns); the rest of Y and S stays NaN.
     """
     Xc, Wc = _c(X, np.float32), _c(W, np.uint8)
-    bc, Rc = _c(bias, np.float32), _c(residual, np.float32)
-    Y = np.full((n, m), np.nan, dtype=np.float64)
-    S = np.full((n, m), np.nan, dtype=np.float64) if bound else None
+    bc, Rc, b2c = _c(bias, np.float32), _c(residual, np.float32), _c(bias2, np.float32)
+    ld = m + dual
+    Y = np.full((n, ld), np.nan, dtype=np.float64)
+    S = np.full((n, ld), np.nan, dtype=np.float64) if bound else None
     j0, j1 = (0, m) if rows is None else rows
     rnd = int(bool(round_x)) | (int(bool(round_w)) << 1)
-    rc = _load().oracle_gemm_alpha(n, m, k, wtype, flags, rnd, float(alpha), _ptr(Xc), _ptr(Wc),
-                                   _ptr(bc), _ptr(Rc), _ptr(Y), _ptr(S), j0, j1, int(threads))
+    rc = _load().oracle_gemm_dual(n, m, k, int(dual), wtype, flags, rnd, float(alpha), _ptr(Xc),
+                                  _ptr(Wc), _ptr(bc), _ptr(b2c), _ptr(Rc), _ptr(Y), _ptr(S), j0,
+                                  j1, int(threads))
     if rc != 0:
         raise ValueError("oracle_gemm: bad arguments")
     return Y, S

@@ -29,6 +29,10 @@
  *     reference epilogue(): Silu v/(1+exp(-v)), Relu max(v, 0), Tanh tanh(v); here
  *     flags 8, 16, 32, in the activation's place (after bias, before residual);
  *     at most one activation per call.
+ *   - dual outputs: wavo 0.3.0 src/gpu/mod.rs, Gpu::linear (a bias with `dual`
+ *     more values than rows) and its gemm test: the first `dual` outputs are
+ *     written again after the others, as the plain sum plus the extra bias values,
+ *     with no epilogue.
  *   - MoE: hanzo-ml 0.11.13, moe_matvec_gpu: y[s, r] = sum_k W[ids[s], r, k] x[s, k]
  *     over one bank [E][rows][k]; here x is per token and slot (t, s) reads
  *     token t's row, output [t][s][m].
@@ -204,21 +208,30 @@ static int set_threads(int threads) {
 }
 
 /*
- * Y[i][j] (f64, [n][m]) for all i < n and output rows j in [j0, j1).
- * X f32 [n][k]; W byte image [m][row_bytes]; bias f32 [m] (flag 1);
- * R f32 [n][m] (flag 4, the old Y); S (optional) gets the bound.
+ * Y[i][j] (f64) for all i < n and output rows j in [j0, j1) of W, with wavo's
+ * dual outputs (wavo 0.3.0 src/gpu/mod.rs, Gpu::linear and its gemm test): a bias
+ * with `dual` more values has the first `dual` outputs written once more after
+ * the m others, as the plain sum plus those values, with no epilogue:
+ *   Y[i][j]     = epi(sum_k X[i][k] W[j][k]),         j < m
+ *   Y[i][m + j] = sum_k X[i][k] W[j][k] + bias2[j],   j < dual.
+ * Y, S and R have rows of m + dual values.  X f32 [n][k]; W byte image
+ * [m][row_bytes]; bias f32 [m] (flag 1); R f32 (flag 4, the old Y; its columns
+ * m.. are not read); bias2 f32 [dual]; S (optional) gets the bound of each output.
  * round: bit 0 feeds bf16-rounded X, bit 1 bf16-rounded W (each dequantised value
  * d*q, exact in f64, rounded to the nearest bf16, ties to even): the operands of
  * the tensor-core path.  threads <= 0: all.
  * Returns 0, or -1 on a bad argument.
  */
-int oracle_gemm_alpha(int n, int m, int k, int wtype, unsigned flags, int round, double alpha,
-                      const float *X, const uint8_t *W, const float *bias, const float *R,
-                      double *Y, double *S, int j0, int j1, int threads) {
+int oracle_gemm_dual(int n, int m, int k, int dual, int wtype, unsigned flags, int round,
+                     double alpha, const float *X, const uint8_t *W, const float *bias,
+                     const float *bias2, const float *R, double *Y, double *S, int j0, int j1,
+                     int threads) {
     if (n < 0 || !shape_ok(wtype, m, k) || j0 < 0 || j1 > m || j0 > j1) return -1;
+    if (dual < 0 || dual > m || (dual > 0 && !bias2)) return -1;
     if (__builtin_popcount(flags & O_ACTS) > 1) return -1;
     if (((flags & O_BIAS) && !bias) || ((flags & O_RESIDUAL) && !R)) return -1;
     size_t rb = row_bytes(wtype, k);
+    size_t ld = (size_t)m + (size_t)dual;
     int nt = set_threads(threads);
     int bad = 0;
     const int round_x = round & 1, round_w = (round >> 1) & 1;
@@ -235,15 +248,26 @@ int oracle_gemm_alpha(int n, int m, int k, int wtype, unsigned flags, int round,
                 if (round_w)
                     for (int t = 0; t < k; ++t) w[t] = oracle_round_bf16(w[t]);
                 for (int i = 0; i < n; ++i) {
-                    size_t o = (size_t)i * m + j;
+                    size_t o = (size_t)i * ld + j;
                     dot_epi(k, flags, round_x, alpha, X + (size_t)i * k, w,
                             bias ? bias + j : NULL, R ? R + o : NULL, Y + o, S ? S + o : NULL);
+                    if (j < dual) /* the second output: bias only, alpha 1 */
+                        dot_epi(k, O_BIAS, round_x, 1.0, X + (size_t)i * k, w, bias2 + j, NULL,
+                                Y + o + m, S ? S + o + m : NULL);
                 }
             }
             free(w);
         }
     }
     return bad ? -1 : 0;
+}
+
+/* Without dual outputs: Y, S and R are [n][m]. */
+int oracle_gemm_alpha(int n, int m, int k, int wtype, unsigned flags, int round, double alpha,
+                      const float *X, const uint8_t *W, const float *bias, const float *R,
+                      double *Y, double *S, int j0, int j1, int threads) {
+    return oracle_gemm_dual(n, m, k, 0, wtype, flags, round, alpha, X, W, bias, NULL, R, Y, S,
+                            j0, j1, threads);
 }
 
 /* The same with alpha = 1 (every epilogue but wavo's Residual(a)). */

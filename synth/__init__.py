@@ -272,6 +272,20 @@ def workload_ln_qkv(seed=7, n=1500, d=1024):
                 residual=None)
 
 
+def workload_dual_q(seed=9, n=1500, d=1024, dual=True):
+    """A q projection whose bias carries a second set of d values (wavo's dual
+    outputs: one q with two position biases): 1500 rows of X ~ N(0,1) through a
+    bf16 d x d weight (N(0, 0.03)) on the tensor cores, bias and second bias
+    N(0, 0.1); Y has 2d columns.  With dual=False the same call without the
+    second band."""
+    g = rng(seed)
+    tag = "dual" if dual else "plain"
+    return dict(name=f"{tag}_bf16_tc_q_n{n}_m{d}_k{d}", kind="gemm_dual_tc", wtype=WTYPE_BF16,
+                n=n, m=d, k=d, dual=d if dual else 0, flags=FLAG_BIAS, X=normal_f32(g, (n, d)),
+                W=draw_bf16_weights(g, d, d, 0.03), bias=normal_f32(g, (d,), 0.1),
+                bias2=normal_f32(g, (d,), 0.1), residual=None)
+
+
 def workload_embed(seed=8, wtype=WTYPE_BF16, rows=32000, k=4096, n_ids=512):
     """The token embedding of a 512-token prompt: rows ids[t] drawn uniformly from
     a vocabulary table (32,000 x 4,096, the table's format as for the weights

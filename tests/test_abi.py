@@ -88,6 +88,15 @@ A = 0x10000  # a 16-byte aligned fake device address: never dereferenced below
     lambda: wq.wq_gemm_alpha(1, 8, 40, wq.WQ_Q8_0, 0, 0.5, A, A, None, None, A, None, 0, 0),
     lambda: wq.wq_gemm_alpha(1, 8, 32, wq.WQ_Q8_0, wq.WQ_RESIDUAL, 0.5, A, A, None, None, A, None,
                              0, 0),
+    lambda: wq.wq_gemm_dual(1, 8, 32, 9, wq.WQ_Q8_0, 0, 1.0, A, A, None, A, None, A, None, 0, 0),
+    lambda: wq.wq_gemm_dual(1, 8, 32, -1, wq.WQ_Q8_0, 0, 1.0, A, A, None, A, None, A, None, 0, 0),
+    lambda: wq.wq_gemm_dual(1, 8, 32, 4, wq.WQ_Q8_0, 0, 1.0, A, A, None, None, None, A, None, 0,
+                            0),
+    lambda: wq.wq_gemm_dual(1, 8, 32, 4, wq.WQ_Q8_0, 0, float("nan"), A, A, None, A, None, A, None,
+                            0, 0),
+    lambda: wq.wq_gemm_dual(1, 8, 32, 4, wq.WQ_Q8_0, wq.WQ_BIAS, 1.0, A, A, None, A, None, A, None,
+                            0, 0),
+    lambda: wq.wq_gemm_dual(1, 8, 32, 4, wq.WQ_Q8_0, 0, 1.0, A, A, None, A, None, None, None, 0, 0),
     lambda: wq.wq_embed(0, 8, 32, wq.WQ_Q8_0, A, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 0, 32, wq.WQ_Q8_0, A, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 8, 40, wq.WQ_Q4_0, A, A, None, None, A, 0),

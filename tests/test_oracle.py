@@ -276,6 +276,72 @@ def test_residual_alpha_scales_the_activation(oracle_mod):
     assert np.allclose(Y, 1.0 - 0.25 * 1.9544997361036416, rtol=1e-15)  # 1 - gelu(2) / 4
 
 
+# ------------------------------------------- wavo's dual outputs (Gpu::linear) --
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+def test_dual_outputs_identity_closed_form(oracle_mod, wtype):
+    """A bias with `dual` extra values: with W = I the first m columns are
+    R + alpha * relu(x + b), and columns m + j (j < dual) are x_j + b2_j, with no
+    activation, scale or residual (the residual's own columns m.. are not read)."""
+    n, k, dual = 3, 64, 24
+    g = np.random.default_rng(7)
+    X = g.integers(-6, 7, size=(n, k)).astype(np.float32)
+    b = g.integers(-3, 4, size=k).astype(np.float32)
+    b2 = g.integers(-9, 10, size=dual).astype(np.float32)
+    R = g.integers(-5, 6, size=(n, k + dual)).astype(np.float32)
+    R[:, k:] = np.nan
+    relu = 16
+    Y, S = oracle_mod.gemm(n, k, k, wtype, BIAS | relu | RESIDUAL, X, _identity_image(wtype, k),
+                           bias=b, residual=R, alpha=-0.5, dual=dual, bias2=b2)
+    Xd = X.astype(np.float64)
+    assert Y.shape == (n, k + dual)
+    assert (Y[:, :k] == R[:, :k] - 0.5 * np.maximum(Xd + b, 0.0)).all()
+    assert (Y[:, k:] == Xd[:, :dual] + b2).all()
+    assert (S[:, :k] == 0.5 * np.abs(Xd)).all()
+    assert (S[:, k:] == np.abs(Xd[:, :dual])).all()
+
+
+@pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
+@pytest.mark.parametrize("dual", [1, 5, 7])
+def test_dual_outputs_exact_integer_brute_force(oracle_mod, wtype, dual):
+    """Exact rational arithmetic: columns m + j hold output j's plain sum + b2_j
+    whatever the first band's epilogue (GELU here)."""
+    n, m, k = 3, 7, 64
+    g = np.random.default_rng(300 + 10 * wtype + dual)
+    X, img, Wf = _exact_case(g, wtype, n, m, k)
+    b = g.integers(-4, 5, size=m).astype(np.float32)
+    b2 = g.integers(-4, 5, size=dual).astype(np.float32)
+    Y, S = oracle_mod.gemm(n, m, k, wtype, BIAS | GELU, X, img, bias=b, dual=dual, bias2=b2)
+    for i in range(n):
+        for j in range(dual):
+            acc = sum(Fraction(float(X[i, t])) * Wf[j][t] for t in range(k))
+            s = sum(abs(Fraction(float(X[i, t])) * Wf[j][t]) for t in range(k))
+            assert Y[i, m + j] == float(acc + Fraction(float(b2[j]))), (i, j)
+            assert S[i, m + j] == float(s)
+            v = float(acc + Fraction(float(b[j])))
+            assert Y[i, j] == oracle_mod.gelu(v)
+
+
+def test_dual_outputs_rows_and_arguments(oracle_mod):
+    """rows=(j0, j1) computes both bands of those outputs only; dual = 0 is the
+    plain call; dual outside [0, m] or a missing bias2 is refused."""
+    n, m, k = 2, 40, 32
+    g = np.random.default_rng(12)
+    X, img, _ = _exact_case(g, Q8_0, n, m, k)
+    b2 = np.arange(m, dtype=np.float32)
+    Y, _ = oracle_mod.gemm(n, m, k, Q8_0, 0, X, img, dual=m, bias2=b2, rows=(3, 9))
+    done = np.zeros(2 * m, bool)
+    done[3:9] = True
+    done[m + 3:m + 9] = True
+    assert np.isfinite(Y[:, done]).all() and np.isnan(Y[:, ~done]).all()
+    Y0, _ = oracle_mod.gemm(n, m, k, Q8_0, 0, X, img, dual=0)
+    Yp, _ = oracle_mod.gemm(n, m, k, Q8_0, 0, X, img)
+    assert (Y0 == Yp).all()
+    for dual, bias2 in ((m + 1, np.zeros(m + 1, np.float32)), (-1, b2), (3, None)):
+        with pytest.raises(ValueError):
+            oracle_mod.gemm(n, m, k, Q8_0, 0, X, img, dual=dual, bias2=bias2)
+
+
 @pytest.mark.parametrize("wtype", [Q8_0, Q4_0])
 def test_zero_weights_residual(oracle_mod, wtype):
     n, m, k = 3, 7, 64
