@@ -8,7 +8,7 @@
 //   Q4_0         hanzo-ml 0.11.13, matvec_q4_0_gpu: 18-byte blocks, f16 d then 16
 //                bytes; element t < 16 = low nibble of byte t, t >= 16 = high
 //                nibble of byte t-16; w = d*(q-8).
-//   F16 / F32    wavo 0.3.0 src/gpu/mod.rs, Linear ("0: F32, 1: F16"): IEEE
+//   F16 / F32    wavo 0.3.0 src/gpu/mod.rs, Linear (pipeline index 0 / 1): IEEE
 //                binary16 / binary32 elements, row after row.
 // Epilogue       cortiq-engine ae_put: +bias, erf-GELU, +old Y, in that order.
 #pragma once

@@ -113,7 +113,7 @@ static size_t row_bytes(int wtype, int k) {
 }
 
 /* Dequantise one W row of k weights into f64.  F16 / F32: wavo 0.3.0
- * src/gpu/mod.rs, Linear "GEMM pipeline index: 0: F32, 1: F16" -- plain IEEE
+ * src/gpu/mod.rs, Linear (pipeline index 0 for F32, 1 for F16 weights) -- plain IEEE
  * binary16 / binary32 elements, little-endian, row after row. */
 static void dequant_row(int wtype, const uint8_t *row, int k, double *w) {
     if (wtype == O_F16) {

@@ -1,4 +1,4 @@
-"""GPU parity of wq_gemm_alpha: wavo's Epilogue::Residual(a), "c += a(aW^T + b)",
+"""GPU parity of wq_gemm_alpha: wavo's Epilogue::Residual(a), c += alpha (a W^T + b),
 Y = R + alpha * act(X.W^T + bias), on every route (GEMV, f32-FMA GEMM, tensor-core
 GEMM with and without a workspace), against the oracle with the same alpha; alpha =
 1 must reproduce wq_gemm / wq_gemm_ws bit for bit."""

@@ -1,5 +1,5 @@
 """GPU parity for wavo's F16 and F32 weight types (wavo 0.3.0 src/gpu/mod.rs,
-Linear "GEMM pipeline index: 0: F32, 1: F16") on every route that takes them: the
+Linear, pipeline index 0 for F32 and 1 for F16) on every route that takes them: the
 weight-streaming GEMV and MoE, the f32-FMA GEMM (tiled and cluster split-k),
 dequantize, the embedding gather and the tensor-core workspace GEMM (elements
 rounded to bf16 there, like d*q).  The f32 routes are held to 1e-5 sum|x||w|."""

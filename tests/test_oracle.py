@@ -253,7 +253,7 @@ def test_epilogue_order(oracle_mod):
 @pytest.mark.parametrize("wtype", [BF16, Q8_0, Q4_0])
 @pytest.mark.parametrize("alpha", [1.0, 0.5, -2.0, 0.0])
 def test_residual_alpha_closed_form(oracle_mod, wtype, alpha):
-    """wavo's Residual(a): c += a(aW^T + b).  With W = I every product is one x, so
+    """wavo's Residual(a): c += alpha (a W^T + b).  With W = I every product is one x, so
     Y = R + alpha (x + b) exactly for small integers and halves; the bound scales."""
     n, k = 3, 64
     g = np.random.default_rng(4)
