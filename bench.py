@@ -86,8 +86,9 @@ def make_workloads():
 def extra_workloads():
     """Measured and reported beside the metric, not part of it: the quantised
     large-n tensor-core GEMM (a prompt through GGML weights), the LayerNorm fused
-    before the encoder qkv projection, the token-embedding gather, and a q
-    projection without and with a second output band (dual outputs)."""
+    before the encoder qkv projection, the token-embedding gather, a q projection
+    without and with a second output band (dual outputs), and one-token GEMVs
+    through bf16 / F16 / F32 weights (the weight-streaming kernel)."""
     import synth
     return [synth.workload_quant_prefill(wtype=synth.WTYPE_Q4_0),
             synth.workload_quant_prefill(wtype=synth.WTYPE_Q8_0),
@@ -95,7 +96,10 @@ def extra_workloads():
             synth.workload_embed(wtype=synth.WTYPE_BF16),
             synth.workload_embed(wtype=synth.WTYPE_Q4_0),
             synth.workload_dual_q(dual=False),
-            synth.workload_dual_q(dual=True)]
+            synth.workload_dual_q(dual=True),
+            synth.workload_float_gemv(wtype=synth.WTYPE_BF16),
+            synth.workload_float_gemv(wtype=synth.WTYPE_F16),
+            synth.workload_float_gemv(wtype=synth.WTYPE_F32)]
 
 
 def algorithmic(w):

@@ -12,11 +12,11 @@
  *   - bf16 pairs: cortiq-engine 0.8.49 src/gpu_wgpu/nemotron_audio.rs, kernel
  *     ae_gemm: word c of a W row holds element 2c in its low half and element
  *     2c+1 in its high half; each half is the top 16 bits of an f32.
- *   - Q8_0: hanzo-ml 0.11.13 src/wgpu_backend.rs, matvec_q8_0_gpu ("34-byte
- *     BlockQ8_0"); wavo 0.3.0 src/gpu/mod.rs, upload_linear (scale = bytes 0..1,
+ *   - Q8_0: hanzo-ml 0.11.13 src/wgpu_backend.rs, matvec_q8_0_gpu (34-byte
+ *     blocks); wavo 0.3.0 src/gpu/mod.rs, upload_linear (scale = bytes 0..1,
  *     data = bytes 2..) and its test quantiser (scale written little-endian):
  *     32 weights per block, value d*q with q a signed byte.
- *   - Q4_0: hanzo-ml 0.11.13, matvec_q4_0_gpu ("raw Q4_0 block bytes", k a
+ *   - Q4_0: hanzo-ml 0.11.13, matvec_q4_0_gpu (the blocks read as stored, k a
  *     multiple of 32).  The nibble order is not on the pages; this oracle takes
  *     the Q4_0 workload's definition: 18-byte block = f16 d + 16 bytes, element
  *     t < 16 is the low nibble of byte t, t >= 16 the high nibble of byte t-16,

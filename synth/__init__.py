@@ -13,11 +13,11 @@ Storage formats, as the pages define them:
   ``ae_gemm``): W is an array of u32 words; word c of row j holds element 2c in
   its low 16 bits and element 2c+1 in its high 16 bits.  On a little-endian
   machine that is byte-identical to row-major bf16 ``[m][k]``.
-* Q8_0 (hanzo-ml 0.11.13, src/wgpu_backend.rs, ``matvec_q8_0_gpu``: "34-byte
-  BlockQ8_0"; wavo 0.3.0, src/gpu/mod.rs, ``upload_linear`` and the test
+* Q8_0 (hanzo-ml 0.11.13, src/wgpu_backend.rs, ``matvec_q8_0_gpu``, 34-byte
+  blocks; wavo 0.3.0, src/gpu/mod.rs, ``upload_linear`` and the test
   quantiser, which writes the f16 scale with ``to_le_bytes``): per 32 weights
   along k, a little-endian f16 scale ``d`` then 32 int8 ``qs``; value d*q.
-* Q4_0 (hanzo-ml 0.11.13, ``matvec_q4_0_gpu``, "raw Q4_0 block bytes"; the
+* Q4_0 (hanzo-ml 0.11.13, ``matvec_q4_0_gpu``, which reads the blocks as stored; the
   nibble order is not on the pages, it is the one the Q4_0 workload fixes): per
   32 weights, a little-endian f16 scale then 16 bytes; element j < 16 is the
   low nibble of byte j, element j >= 16 the high nibble of byte j-16; value
@@ -210,6 +210,16 @@ def workload_q8_0_gemv(seed=2, n=1, m=4096, k=4096):
     return dict(name=f"q8_0_gemv_n{n}_m{m}_k{k}", kind="gemv", wtype=WTYPE_Q8_0, n=n, m=m, k=k,
                 flags=0, W=draw_q8_0_weights(g, m, k), X=normal_f32(g, (n, k)),
                 bias=None, residual=None)
+
+
+def workload_float_gemv(seed=10, wtype=WTYPE_BF16, n=1, m=4096, k=4096):
+    """A one-token GEMV through unquantised weights (bf16 pairs, or wavo's F16 / F32
+    elements), N(0, 0.03), with a bias: the weight-streaming kernel's workload."""
+    g = rng(seed * 10 + wtype)
+    tag = {WTYPE_BF16: "bf16", WTYPE_F16: "f16", WTYPE_F32: "f32"}[wtype]
+    return dict(name=f"{tag}_gemv_n{n}_m{m}_k{k}", kind="gemv", wtype=wtype, n=n, m=m, k=k,
+                flags=FLAG_BIAS, W=draw_weights(g, wtype, m, k, 0.03), X=normal_f32(g, (n, k)),
+                bias=normal_f32(g, (m,), 0.1), residual=None)
 
 
 def workload_q4_0_gemv(seed=3, n=1, m=14336, k=4096):
