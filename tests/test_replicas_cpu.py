@@ -2,6 +2,7 @@
 run, "replicas only": no collective on the data path).  Checks the rendezvous, the
 barrier and the max-over-ranks reduction of the step time, and that only rank 0
 runs the CPU reference arm."""
+import functools
 import os
 import socket
 
@@ -61,3 +62,42 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
 def test_kernels_per_call(name, kernels):
     w = {x["name"]: x for x in bench.make_workloads()}[name]
     assert bench.kernels_per_call(w) == kernels
+
+
+@functools.lru_cache(maxsize=1)
+def _extras():
+    return {x["name"]: x for x in bench.extra_workloads()}
+
+
+def _extra(name):
+    return _extras()[name]
+
+
+def test_algorithmic_bytes_of_the_dual_output_band():
+    """The second band adds n x dual f32 outputs and dual bias values, and no flops."""
+    plain = _extra("plain_bf16_tc_q_n1500_m1024_k1024")
+    dual = _extra("dual_bf16_tc_q_n1500_m1024_k1024")
+    bp, fp = bench.algorithmic(plain)
+    bd, fd = bench.algorithmic(dual)
+    assert fd == fp == 2.0 * 1500 * 1024 * 1024
+    assert bd - bp == 1500 * 1024 * 4 + 1024 * 4
+    assert bench.kernels_per_call(dual) == 2
+
+
+@pytest.mark.parametrize("tag,wbytes", [("bf16", 2), ("f16", 2), ("f32", 4)])
+def test_algorithmic_bytes_of_the_float_gemvs(tag, wbytes):
+    w = _extra(f"{tag}_gemv_n1_m4096_k4096")
+    b, f = bench.algorithmic(w)
+    # weights once, X, Y, bias
+    assert b == 4096 * 4096 * wbytes + 4096 * 4 + 4096 * 4 + 4096 * 4
+    assert f == 2.0 * 4096 * 4096
+    assert bench.kernels_per_call(w) == 1
+
+
+def test_traffic_record_is_dropped_when_its_source_changes(monkeypatch):
+    name = "moe_q4_0_E64_m1408_k2048_t16x6"
+    rec = dict(bench.TRAFFIC[name])
+    assert bench.traffic_for(name) == rec["bytes"]  # recorded on the source as committed
+    monkeypatch.setitem(bench.TRAFFIC, name, dict(rec, sha256="0" * 64))
+    assert bench.traffic_for(name) is None
+    assert bench.traffic_for("no_such_workload") is None
