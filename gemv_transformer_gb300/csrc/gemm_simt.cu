@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(256) gemm_splitk_kernel(const GemmArgs a, int 
         {   // X tile: row r, elements 4q..4q+3 (k % 4 == 0: a float4 is all in or all out)
             const int r = tid >> 3, q = tid & 7, i = i0 + r, t = kk + 4 * q;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i < a.n && t < a.k) v = __ldg(reinterpret_cast<const float4 *>(a.X + (size_t)i * a.k + t));
+            if (i < a.n && t < a.k)
+                v = __ldg(reinterpret_cast<const float4 *>(a.X + (size_t)i * a.k + t));
             xs[4 * q + 0][r] = v.x; xs[4 * q + 1][r] = v.y;
             xs[4 * q + 2][r] = v.z; xs[4 * q + 3][r] = v.w;
         }
@@ -338,7 +339,8 @@ __global__ void embed_kernel(int n_ids, int rows, int k, const uint8_t *W, const
         float *o = out + (size_t)t * k + t0;
         const float *p = pos ? pos + (size_t)t * k + t0 : nullptr;
         if (VEC) {
-            float pv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float pv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (p) {
                 const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
                 const float4 c = __ldg(reinterpret_cast<const float4 *>(p) + 1);
@@ -370,6 +372,17 @@ __global__ void embed_kernel(int n_ids, int rows, int k, const uint8_t *W, const
     }
 }
 
+template <bool DUAL>
+cudaError_t launch_simt(const GemmArgs &a, int wtype, dim3 grid, cudaStream_t stream) {
+    switch (wtype) {
+    case kBF16: return launch_pdl(gemm_simt_kernel<kBF16, DUAL>, grid, dim3(256), 0, stream, a);
+    case kF16: return launch_pdl(gemm_simt_kernel<kF16, DUAL>, grid, dim3(256), 0, stream, a);
+    case kF32: return launch_pdl(gemm_simt_kernel<kF32, DUAL>, grid, dim3(256), 0, stream, a);
+    case kQ8_0: return launch_pdl(gemm_simt_kernel<kQ8_0, DUAL>, grid, dim3(256), 0, stream, a);
+    default: return launch_pdl(gemm_simt_kernel<kQ4_0, DUAL>, grid, dim3(256), 0, stream, a);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev,
@@ -396,22 +409,8 @@ cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev
         }
     }
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-    if (a.dual > 0) {
-        switch (wtype) {
-        case kBF16: return launch_pdl(gemm_simt_kernel<kBF16, true>, grid, dim3(256), 0, stream, a);
-        case kF16: return launch_pdl(gemm_simt_kernel<kF16, true>, grid, dim3(256), 0, stream, a);
-        case kF32: return launch_pdl(gemm_simt_kernel<kF32, true>, grid, dim3(256), 0, stream, a);
-        case kQ8_0: return launch_pdl(gemm_simt_kernel<kQ8_0, true>, grid, dim3(256), 0, stream, a);
-        default: return launch_pdl(gemm_simt_kernel<kQ4_0, true>, grid, dim3(256), 0, stream, a);
-        }
-    }
-    switch (wtype) {
-    case kBF16: return launch_pdl(gemm_simt_kernel<kBF16, false>, grid, dim3(256), 0, stream, a);
-    case kF16: return launch_pdl(gemm_simt_kernel<kF16, false>, grid, dim3(256), 0, stream, a);
-    case kF32: return launch_pdl(gemm_simt_kernel<kF32, false>, grid, dim3(256), 0, stream, a);
-    case kQ8_0: return launch_pdl(gemm_simt_kernel<kQ8_0, false>, grid, dim3(256), 0, stream, a);
-    default: return launch_pdl(gemm_simt_kernel<kQ4_0, false>, grid, dim3(256), 0, stream, a);
-    }
+    return a.dual > 0 ? launch_simt<true>(a, wtype, grid, stream)
+                      : launch_simt<false>(a, wtype, grid, stream);
 }
 
 cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out,
@@ -420,12 +419,15 @@ cudaError_t launch_dequant(int wtype, int m, int k, const uint8_t *W, float *out
     long long blocks = (units + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
+    auto go = [&](auto kern) {
+        return launch_pdl(kern, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
+    };
     switch (wtype) {
-    case kBF16: return launch_pdl(dequant_kernel<kBF16>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
-    case kF16: return launch_pdl(dequant_kernel<kF16>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
-    case kF32: return launch_pdl(dequant_kernel<kF32>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
-    case kQ8_0: return launch_pdl(dequant_kernel<kQ8_0>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
-    default: return launch_pdl(dequant_kernel<kQ4_0>, dim3((unsigned)blocks), dim3(256), 0, stream, m, k, W, out);
+    case kBF16: return go(dequant_kernel<kBF16>);
+    case kF16: return go(dequant_kernel<kF16>);
+    case kF32: return go(dequant_kernel<kF32>);
+    case kQ8_0: return go(dequant_kernel<kQ8_0>);
+    default: return go(dequant_kernel<kQ4_0>);
     }
 }
 

@@ -60,11 +60,6 @@ struct Extra {
     int dual = 0;
     const float *bias2 = nullptr;
 };
-
-template <typename Args>
-void fill_args(Args &a, int n, int m, int k, unsigned flags, const float *X, const void *W,
-               const float *bias, const float *residual, float *Y, const DeviceInfo &dev,
-               const Extra &ex);
 }  // namespace
 
 wq_status check_gemm_args(int n, int m, int k, int wtype, unsigned flags, const float *X,
@@ -97,6 +92,8 @@ unsigned long long wait_limit() {
 }
 
 namespace {
+// The fields every contraction call shares; Y and the residual have rows of
+// m + dual values.
 template <typename Args>
 void fill_args(Args &a, int n, int m, int k, unsigned flags, const float *X, const void *W,
                const float *bias, const float *residual, float *Y, const DeviceInfo &dev,
