@@ -212,6 +212,7 @@ wq_status wq_gemm_dual(int n, int m, int k, int dual, int wtype, unsigned flags,
     if (s != WQ_OK) return s;
     if (!std::isfinite(alpha)) return WQ_ERR_INVALID_ARG;
     if (dual < 0 || dual > m || (dual > 0 && !bias2)) return WQ_ERR_INVALID_ARG;
+    if ((long long)m + dual > 0x7FFFFFFFll) return WQ_ERR_INVALID_ARG;  // the row stride is an int
     const Extra ex{alpha, dual, dual > 0 ? bias2 : nullptr};
     if (!workspace)
         return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, ex);

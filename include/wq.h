@@ -285,8 +285,8 @@ WQ_API wq_status wq_gemm_alpha(int n, int m, int k, int wtype, unsigned flags, f
  * accumulation: W is read once, and Y[i][m + j] - bias2[j] is bit-identical to the
  * sum that feeds column j.  workspace NULL: the routes of wq_gemm; otherwise those
  * of wq_gemm_ws, with the same workspace rules.
- * Errors: as wq_gemm_alpha, plus WQ_ERR_INVALID_ARG for dual < 0, dual > m, or a
- * null bias2 with dual > 0.
+ * Errors: as wq_gemm_alpha, plus WQ_ERR_INVALID_ARG for dual < 0, dual > m, a null
+ * bias2 with dual > 0, or m + dual above 2^31 - 1.
  */
 WQ_API wq_status wq_gemm_dual(int n, int m, int k, int dual, int wtype, unsigned flags,
                               float alpha, const float *X, const void *W, const float *bias,

@@ -97,6 +97,8 @@ A = 0x10000  # a 16-byte aligned fake device address: never dereferenced below
     lambda: wq.wq_gemm_dual(1, 8, 32, 4, wq.WQ_Q8_0, wq.WQ_BIAS, 1.0, A, A, None, A, None, A, None,
                             0, 0),
     lambda: wq.wq_gemm_dual(1, 8, 32, 4, wq.WQ_Q8_0, 0, 1.0, A, A, None, A, None, None, None, 0, 0),
+    lambda: wq.wq_gemm_dual(1, 0x7FFFFFE0, 32, 0x40, wq.WQ_Q8_0, 0, 1.0, A, A, None, A, None, A,
+                            None, 0, 0),
     lambda: wq.wq_embed(0, 8, 32, wq.WQ_Q8_0, A, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 0, 32, wq.WQ_Q8_0, A, A, None, None, A, 0),
     lambda: wq.wq_embed(2, 8, 40, wq.WQ_Q4_0, A, A, None, None, A, 0),
