@@ -1,8 +1,9 @@
 // wq_api.cu -- the extern "C" entry points of libwq (declared in include/wq.h).
 //
-// Host-side only: argument checks (the page's own checks are hanzo-ml 0.11.13
-// matvec_q*_gpu "k must be a multiple of 32", "x count < k", moe_matvec_gpu
-// "ids count < nrows"), routing to a kernel, and the sticky device status word
+// Host-side only: argument checks (hanzo-ml 0.11.13 src/wgpu_backend.rs refuses,
+// in matvec_q*_gpu, a k that 32 does not divide and an x shorter than k, and in
+// moe_matvec_gpu, fewer ids than rows), routing to a kernel, and the sticky device
+// status word
 // (wavo 0.3.0 src/gpu/mod.rs keeps the first device error and reports it on the
 // next call).  Nothing here computes; every step of the contraction runs in the
 // kernels.
@@ -22,8 +23,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWaitPolls = 1ull << 22;
 std::mutex g_mu;
-DeviceInfo g_dev[kMaxDevices];
-bool g_dev_ok[kMaxDevices];
+int g_sm_count[kMaxDevices];  // per ordinal, 0 until first asked
 unsigned long long g_wait_limit = kDefaultWaitPolls;
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -68,22 +68,27 @@ wq_status check_gemm_args(int n, int m, int k, int wtype, unsigned flags, const 
     return check_common(n, m, k, wtype, flags, X, W, bias, residual, Y);
 }
 
-const DeviceInfo *device_info() {
+bool device_info(DeviceInfo &out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_dev_ok[dev]) {
-        DeviceInfo d{};
-        d.ordinal = dev;
-        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return nullptr;
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-        d.status = static_cast<unsigned *>(p);
-        g_dev[dev] = d;
-        g_dev_ok[dev] = true;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    // The status word's address is looked up on every call (a host-side lookup
+    // that allocates nothing), not cached: after a cudaDeviceReset the module is
+    // loaded again in a new context and the word may sit elsewhere.
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return false;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_sm_count[dev] &&
+            cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess) {
+            g_sm_count[dev] = 0;
+            return false;
+        }
+        out.sm_count = g_sm_count[dev];
     }
-    return &g_dev[dev];
+    out.ordinal = dev;
+    out.status = static_cast<unsigned *>(p);
+    return true;
 }
 
 unsigned long long wait_limit() {
@@ -131,8 +136,9 @@ size_t wq_weight_bytes(int wtype, int m, int k) {
 static wq_status gemv_impl(int n, int m, int k, int wtype, unsigned flags, const float *X,
                            const void *W, const float *bias, const float *residual, float *Y,
                            wq_stream_t stream, const Extra &ex = Extra()) {
-    const DeviceInfo *dev = device_info();
-    if (!dev) return WQ_ERR_CUDA;
+    DeviceInfo dv;
+    if (!device_info(dv)) return WQ_ERR_CUDA;
+    const DeviceInfo *dev = &dv;
     StreamArgs a{};
     fill_args(a, n, m, k, flags, X, W, bias, residual, Y, *dev, ex);
     if (mma_gemv_supported(wtype, k))
@@ -156,8 +162,9 @@ static wq_status gemm_impl(int n, int m, int k, int wtype, unsigned flags, const
         return gemv_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, ex);
     // Tensor cores with quantised W need the bf16 copy of W: wq_gemm_ws.
     if ((flags & WQ_TC_BF16) && wtype != kBF16) return WQ_ERR_UNSUPPORTED;
-    const DeviceInfo *dev = device_info();
-    if (!dev) return WQ_ERR_CUDA;
+    DeviceInfo dv;
+    if (!device_info(dv)) return WQ_ERR_CUDA;
+    const DeviceInfo *dev = &dv;
     GemmArgs a{};
     fill_args(a, n, m, k, flags, X, W, bias, residual, Y, *dev, ex);
     if (flags & WQ_TC_BF16) return cuda_status(launch_gemm_tc(a, *dev, (cudaStream_t)stream));
@@ -188,8 +195,9 @@ static wq_status gemm_ws_impl(int n, int m, int k, int wtype, unsigned flags, co
         return gemm_impl(n, m, k, wtype, flags, X, W, bias, residual, Y, stream, ex);
     if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < need)
         return WQ_ERR_INVALID_ARG;
-    const DeviceInfo *dev = device_info();
-    if (!dev) return WQ_ERR_CUDA;
+    DeviceInfo dv;
+    if (!device_info(dv)) return WQ_ERR_CUDA;
+    const DeviceInfo *dev = &dv;
     GemmArgs a{};
     fill_args(a, n, m, k, flags, X, W, bias, residual, Y, *dev, ex);
     return cuda_status(launch_gemm_tc_ws(a, wtype, workspace, *dev, (cudaStream_t)stream));
@@ -246,8 +254,9 @@ wq_status wq_gemm_ln_ws(int n, int m, int k, int wtype, unsigned flags, const fl
         return WQ_ERR_INVALID_ARG;
     if ((const void *)residual == workspace || (const void *)Y == workspace)
         return WQ_ERR_INVALID_ARG;
-    const DeviceInfo *dev = device_info();
-    if (!dev) return WQ_ERR_CUDA;
+    DeviceInfo dv;
+    if (!device_info(dv)) return WQ_ERR_CUDA;
+    const DeviceInfo *dev = &dv;
     const bool tc = wq_gemm_workspace_bytes(n, m, k, wtype, flags) != 0;
     cudaError_t err = launch_layer_norm(X, ln_gb, n, k, workspace, tc, *dev, (cudaStream_t)stream);
     if (err != cudaSuccess) return WQ_ERR_CUDA;
@@ -269,8 +278,9 @@ wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtyp
     if (flags & WQ_TC_BF16) return WQ_ERR_INVALID_ARG;
     if ((long long)m * n_experts > 0x7FFFFFFFll) return WQ_ERR_INVALID_ARG;
     if ((long long)n_tok * topk > WQ_MOE_MAX_SLOTS) return WQ_ERR_UNSUPPORTED;
-    const DeviceInfo *dev = device_info();
-    if (!dev) return WQ_ERR_CUDA;
+    DeviceInfo dv;
+    if (!device_info(dv)) return WQ_ERR_CUDA;
+    const DeviceInfo *dev = &dv;
     StreamArgs a{};
     fill_args(a, n_tok, m, k, flags, X, Wbank, bias, residual, Y, *dev, Extra());
     a.ids = ids;
@@ -291,8 +301,9 @@ wq_status wq_embed(int n_ids, int rows, int k, int wtype, const void *W, const i
                    const float *pos, const float *bias, float *out, wq_stream_t stream) {
     if (n_ids <= 0 || !shape_ok(wtype, rows, k) || !W || !ids || !out || !aligned16(W))
         return WQ_ERR_INVALID_ARG;
-    const DeviceInfo *dev = device_info();
-    if (!dev) return WQ_ERR_CUDA;
+    DeviceInfo dv;
+    if (!device_info(dv)) return WQ_ERR_CUDA;
+    const DeviceInfo *dev = &dv;
     return cuda_status(launch_embed(n_ids, rows, k, wtype, static_cast<const uint8_t *>(W), ids,
                                     pos, bias, out, *dev, (cudaStream_t)stream));
 }

@@ -92,8 +92,9 @@ __device__ __forceinline__ float activate(float v, unsigned flags) {
 }
 
 // acc -> Y value.  `res` is read only with kResidual.  alpha scales the
-// contribution before the residual is added (wavo's Epilogue::Residual(a),
-// "c += a(aW^T + b)"; 1 otherwise, which leaves every value unchanged).
+// contribution before the residual is added (wavo 0.3.0 src/gpu/mod.rs,
+// Epilogue::Residual(a): the biased product times a is added to the old output;
+// 1 otherwise, which leaves every value unchanged).
 __device__ __forceinline__ float epilogue(float acc, unsigned flags, const float *bias_j,
                                           const float *res_ij, float alpha) {
     float v = acc;

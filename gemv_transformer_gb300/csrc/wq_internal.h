@@ -89,8 +89,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Cached per-device facts (current device).  Returns nullptr on a CUDA error.
-const DeviceInfo *device_info();
+// Facts about the current device (SM count cached per ordinal; the status word's
+// address looked up each time).  Returns false on a CUDA error.
+bool device_info(DeviceInfo &out);
 unsigned long long wait_limit();
 
 cudaError_t launch_stream_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,

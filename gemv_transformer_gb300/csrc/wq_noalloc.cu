@@ -9,37 +9,30 @@
 // allocator at all).  Nothing here allocates: no cudaMalloc/cudaFree, no
 // allocating library routine.  The array below is part of the library's device
 // image; the CUDA runtime reserves it when it loads this module on a device.
-#include <mutex>
-
 #include "../../include/wq.h"
 #include "wq_device.cuh"
 #include "wq_internal.h"
 
 namespace wq {
 
-// The rounded X (bf16 [n][k], row-major).  Every byte a call reads is written by
-// the same call first (the rounding pass covers all n*k elements and the GEMM's
-// tensor map stops at row n; rows past it are zero-filled by the TMA unit, not
-// read), so nothing here has to start at zero.  One copy per device.
-__device__ __align__(256) unsigned char g_noalloc_scratch[WQ_GEMM_NOALLOC_SCRATCH_BYTES];
+// The rounded X (bf16 [n][k], row-major), followed for Q8_0/Q4_0/F16/F32 weights
+// by the rounded W (bf16 [m][k]).  Every byte a call reads is written by the same
+// call first (the rounding passes cover all n*k and m*k elements and the GEMM's
+// tensor maps stop at rows n and m; rows past them are zero-filled by the TMA
+// unit, not read), so nothing here has to start at zero.  One copy per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[WQ_GEMM_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_na_mu;
-void *g_na_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per ordinal
-
-// Looks the array's address up once per device, with that device current (the
-// caller's).  Returns nullptr if the lookup fails.
-void *scratch_ptr(int ordinal) {
-    if (ordinal < 0 || ordinal >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_na_mu);
-    if (!g_na_ptr[ordinal]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress((void **)&p, g_noalloc_scratch) != cudaSuccess || !p)
-            return nullptr;
-        g_na_ptr[ordinal] = p;
-    }
-    return g_na_ptr[ordinal];
+// The array's device address on the current device.  Host code cannot use the
+// symbol itself (it names a host-side stand-in), so the address is looked up;
+// this is a host-side table lookup that allocates nothing.  It is repeated on
+// every call rather than cached, so that a context created after a
+// cudaDeviceReset (which loads the module again, possibly elsewhere) is never
+// given a stale address.  Returns nullptr if the lookup fails.
+void *scratch_ptr() {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    return p;
 }
 }  // namespace
 }  // namespace wq
@@ -55,9 +48,7 @@ extern "C" wq_status wq_gemm_noalloc(int n, int m, int k, int wtype, unsigned fl
     if (need == 0)  // this route takes no scratch: plain wq_gemm
         return wq_gemm(n, m, k, wtype, flags, X, W, bias, residual, Y, stream);
     if (need > (size_t)WQ_GEMM_NOALLOC_SCRATCH_BYTES) return WQ_ERR_TOO_LARGE;
-    int ordinal = -1;
-    if (cudaGetDevice(&ordinal) != cudaSuccess) return WQ_ERR_CUDA;
-    void *scratch = scratch_ptr(ordinal);
+    void *scratch = scratch_ptr();
     if (!scratch) return WQ_ERR_CUDA;
     return wq_gemm_ws(n, m, k, wtype, flags, X, W, bias, residual, Y, scratch,
                       (size_t)WQ_GEMM_NOALLOC_SCRATCH_BYTES, stream);

@@ -185,8 +185,10 @@ WQ_API size_t wq_gemm_workspace_bytes(int n, int m, int k, int wtype, unsigned f
  * weights: n*k <= 8,388,608, e.g. 1500 x 4096).  The call allocates
  * nothing, by any route.  Nothing in the array needs to start at zero: each call
  * writes every byte it later reads.
- * Set-up: the first call on a device (with that device current) looks up the
- * array's address; make that first call before any stream capture begins.
+ * Set-up: every call looks up the array's address on the current device (a
+ * host-side lookup that allocates nothing); the first call on a device may load
+ * the library's device image there, so make that first call before any stream
+ * capture begins.
  * Concurrency: all calls on one device share the one array.  Calls ordered on one
  * stream are safe; calls that may overlap in time (different streams without an
  * ordering between them, or different host threads) race on it and give wrong
