@@ -25,7 +25,7 @@ WQ_OK, WQ_ERR_INVALID_ARG, WQ_ERR_UNSUPPORTED, WQ_ERR_CUDA = 0, 1, 2, 3
 WQ_ERR_DEVICE_TIMEOUT, WQ_ERR_BAD_EXPERT, WQ_ERR_TOO_LARGE, WQ_ERR_BAD_INDEX = 4, 5, 6, 7
 WQ_GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20
 WQ_GEMV_MAX_N = 16
-WQ_MOE_MAX_SLOTS = 256
+WQ_MOE_WINDOW_SLOTS = 256
 
 EXPORTS = ("wq_gemm", "wq_gemm_ws", "wq_gemm_alpha", "wq_gemm_dual", "wq_gemm_workspace_bytes",
            "wq_gemm_noalloc",

@@ -39,7 +39,14 @@
 // tokens use four n-tiles the same way (two token halves).
 // The partial sums of the 16 warps are reduced in shared memory in a fixed
 // order (deterministic) and the epilogue (bias, erf-GELU, residual) is fused
-// into the store.
+// into the store.  Before waiting for the previous grid, a GEMV CTA asks L2 to
+// prefetch its row range of W: no earlier kernel's stores can leave a stale copy
+// behind, as L2 is the point of coherence.
+//
+// MoE routing: the n_tok * topk slots are taken in windows of at most 256; for
+// each window every CTA sorts the window's slots by (expert, slot) in shared
+// memory and runs over the touched experts' row tiles, so a selected expert's
+// weights are read once per window however many of its slots the window holds.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -241,6 +248,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Ask L2 to fetch [p, p + bytes) (16-byte aligned, bytes % 16 == 0) ahead of use.
+__device__ __forceinline__ void prefetch_l2_range(const uint8_t *p, size_t bytes) {
+    constexpr size_t kPiece = 32768;
+    for (size_t o = 0; o < bytes; o += kPiece) {
+        const uint32_t n = (uint32_t)(bytes - o < kPiece ? bytes - o : kPiece);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + o), "r"(n) : "memory");
+    }
+}
+
 // 4-byte global -> shared copy that does not hold a register (completes at
 // cp_async_wait_all).
 __device__ __forceinline__ void cp_async4(float *dst, const float *src) {
@@ -342,39 +358,58 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (threadIdx.x == kCW * 32)  // the producer's thread
+    if (threadIdx.x == kCW * 32) {  // the producer's thread
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap_t)) : "memory");
+        if (!MOE) {  // L2 prefetch of this CTA's rows (weights are never written by an earlier grid)
+            const long long tpe = (m + 15) / 16;
+            const long long u0 = tpe * blockIdx.x / gridDim.x, u1 = tpe * (blockIdx.x + 1) / gridDim.x;
+            const long long r1 = min((long long)m, u1 * 16);
+            if (r1 > u0 * 16)
+                prefetch_l2_range(a.W + (size_t)(u0 * 16) * row_bytes(WT, k), (size_t)(r1 - u0 * 16) * row_bytes(WT, k));
+        }
+    }
     pdl_wait();
     Sched sc;
     sc.tpe = (m + 15) / 16;
+    const int S_all = MOE ? a.n * a.topk : 0;
+    const int n_win = MOE ? (S_all + kMaxSlots - 1) / kMaxSlots : 1;
+    // Ring positions, carried across routing windows.
+    long long q = 0;       // producer: stages issued
+    int qs = 0;            // consumers: stage of the next chunk
+    uint32_t qph = 0u;     // its fill parity
+    bool ok = true;        // consumers: no wait ran out
+
+    for (int win = 0; win < n_win; ++win) {
     if (MOE) {
-        const int Sl = a.n * a.topk;
+        // Sort the window's slots by (expert, slot); bad ids go last.
+        const int base = win * kMaxSlots;
+        const int Sl = min(kMaxSlots, S_all - base);
         const unsigned long long big = 1ull << 62;
-        for (int q = threadIdx.x; q < Sl; q += blockDim.x) {
-            const int e = a.ids[q];
-            const bool ok = e >= 0 && e < a.n_experts;
-            if (!ok && blockIdx.x == 0) record_status(a.status, kStBadExpert);
-            s_key[q] = ok ? ((unsigned long long)e << 16) | (unsigned)q : big | (unsigned)q;
+        for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
+            const int e = a.ids[base + i];
+            const bool okid = e >= 0 && e < a.n_experts;
+            if (!okid && blockIdx.x == 0) record_status(a.status, kStBadExpert);
+            s_key[i] = okid ? ((unsigned long long)e << 16) | (unsigned)i : big | (unsigned)i;
         }
         __syncthreads();
-        for (int q = threadIdx.x; q < Sl; q += blockDim.x) {
-            const unsigned long long kq = s_key[q];
+        for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
+            const unsigned long long ki = s_key[i];
             int r = 0;
-            for (int q2 = 0; q2 < Sl; ++q2) r += s_key[q2] < kq;
-            s_sorted[r] = q;
+            for (int i2 = 0; i2 < Sl; ++i2) r += s_key[i2] < ki;
+            s_sorted[r] = base + i;  // the slot's global index
         }
         __syncthreads();
         if (warp == 0) {  // segment starts of the sorted slots, by ballot and prefix count
             int na = 0;
-            for (int base = 0; base < Sl; base += 32) {
-                const int r = base + lane;
+            for (int b0 = 0; b0 < Sl; b0 += 32) {
+                const int r = b0 + lane;
                 bool valid = false, start = false;
                 int e = 0;
                 if (r < Sl) {
-                    const unsigned long long kr = s_key[s_sorted[r]];
+                    const unsigned long long kr = s_key[s_sorted[r] - base];
                     valid = !(kr & big);
                     e = (int)(kr >> 16);
-                    start = valid && (r == 0 || (int)(s_key[s_sorted[r - 1]] >> 16) != e);
+                    start = valid && (r == 0 || (int)(s_key[s_sorted[r - 1] - base] >> 16) != e);
                 }
                 const unsigned sm = __ballot_sync(0xFFFFFFFFu, start);
                 if (start) {
@@ -386,23 +421,21 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                 const unsigned vm = __ballot_sync(0xFFFFFFFFu, valid);
                 if (vm != 0xFFFFFFFFu) {  // the first invalid slot ends the valid ones
                     if (lane == 0) {
-                        s_seg[na] = base + __popc(vm);
+                        s_seg[na] = b0 + __popc(vm);
                         *s_nact = na;
                     }
                     break;
                 }
-                if (base + 32 >= Sl && lane == 0) {
+                if (b0 + 32 >= Sl && lane == 0) {
                     s_seg[na] = Sl;
                     *s_nact = na;
                 }
             }
         }
-        __syncthreads();
-        sc.n_act = *s_nact;
-    } else {
-        __syncthreads();
-        sc.n_act = 1;
     }
+    __syncthreads();
+    if (*abort_flag) break;  // the same in every thread after the barrier
+    sc.n_act = MOE ? *s_nact : 1;
     const long long units = (long long)sc.n_act * sc.tpe;
     sc.u0 = units * blockIdx.x / gridDim.x;
     sc.u1 = units * (blockIdx.x + 1) / gridDim.x;
@@ -426,13 +459,12 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
         // by the TMA unit); they are computed and never stored.
         if (lane == 0) {
             const uint64_t policy = l2_evict_first();
-            long long q = 0;
-            bool ok = true;
-            for (long long u = sc.u0; u < sc.u1 && ok;) {
+            bool pok = true;
+            for (long long u = sc.u0; u < sc.u1 && pok;) {
                 const int nt = group_tiles<T>(sc, u);
                 int seg0;
                 const int ntok = group_tokens(u, seg0);
-                for (int p0 = 0; p0 < ntok && ok; p0 += P_MAX) {
+                for (int p0 = 0; p0 < ntok && pok; p0 += P_MAX) {
                     for (int c = 0; c < KC; ++c, ++q) {
                         const int s = (int)(q % S);
                         if (q >= S) {
@@ -443,7 +475,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                             if (!w) {
                                 if (!*abort_flag) record_status(a.status, kStTimeout);
                                 *abort_flag = 1u;
-                                ok = false;
+                                pok = false;
                                 break;
                             }
                         }
@@ -467,16 +499,11 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                 }
                 u += nt;
             }
-            for (long long d = (q > S ? q - S : 0); d < q; ++d)
-                mbar_wait(&full[d % S], (uint32_t)((d / S) & 1), kDrainPolls);
         }
-        return;
-    }
+        __syncwarp();
+    } else {
 
     // ---------------------------------------------------------------- consumers
-    int qs = 0;            // stage of the next chunk
-    uint32_t qph = 0u;     // its fill parity
-    bool ok = true;
     for (long long u = sc.u0; u < sc.u1 && ok;) {
         const int ntiles = group_tiles<T>(sc, u);
         int seg0;
@@ -767,6 +794,17 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
             }
         }
         u += ntiles;
+    }
+    }  // consumers
+    // The window's routing tables are rewritten by the next window: every thread is
+    // done with them here.  (Consumers that gave up skipped the rest of the window;
+    // no window is started after an abort.)
+    if (n_win > 1) __syncthreads();
+    }  // windows
+    if (warp == kCW && lane == 0) {
+        // Drain copies that no consumer waited for (only after an abort).
+        for (long long d = (q > S ? q - S : 0); d < q; ++d)
+            mbar_wait(&full[d % S], (uint32_t)((d / S) & 1), kDrainPolls);
     }
 }
 

@@ -277,7 +277,7 @@ wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtyp
     if (s != WQ_OK) return s;
     if (flags & WQ_TC_BF16) return WQ_ERR_INVALID_ARG;
     if ((long long)m * n_experts > 0x7FFFFFFFll) return WQ_ERR_INVALID_ARG;
-    if ((long long)n_tok * topk > WQ_MOE_MAX_SLOTS) return WQ_ERR_UNSUPPORTED;
+    if ((long long)n_tok * topk > 0x7FFFFFFFll) return WQ_ERR_INVALID_ARG;
     DeviceInfo dv;
     if (!device_info(dv)) return WQ_ERR_CUDA;
     const DeviceInfo *dev = &dv;

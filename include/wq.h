@@ -122,8 +122,10 @@ typedef enum {
 
 /* Largest n that wq_gemv accepts. */
 #define WQ_GEMV_MAX_N 16
-/* Largest n_tok * topk that wq_moe_gemv accepts. */
-#define WQ_MOE_MAX_SLOTS 256
+/* wq_moe_gemv routes its n_tok * topk slots in windows of this many: a selected
+ * expert's weights are read once per window that routes slots to it.  Not a
+ * limit on n_tok * topk. */
+#define WQ_MOE_WINDOW_SLOTS 256
 
 /*
  * Y = epi(X . W^T) for any n >= 1 (cortiq-engine ae_gemm semantics).
@@ -240,13 +242,14 @@ WQ_API wq_status wq_gemv(int n, int m, int k, int wtype, unsigned flags, const f
  * at least wq_weight_bytes(wtype, n_experts * m, k) bytes); ids int32
  * [n_tok][topk] on the device; bias f32 [n_experts][m] (per expert, WQ_BIAS);
  * residual f32 [n_tok*topk][m] (WQ_RESIDUAL, may equal Y); Y f32 [n_tok][topk][m].
- * Each selected expert's weights are read once per call whatever the number of
- * slots routed to it.  With topk = 1 and X holding one row per slot this is the
- * page's per-slot form.  An id outside [0, n_experts) leaves that slot's Y row
+ * The slots are routed in windows of WQ_MOE_WINDOW_SLOTS consecutive slots; each
+ * selected expert's weights are read once per window whatever the number of the
+ * window's slots routed to it (once per call when n_tok * topk <= 256).
+ * n_tok * topk may be any value up to 2^31 - 1.  With topk = 1 and X holding
+ * one row per slot this is the page's per-slot form.  An id outside [0, n_experts) leaves that slot's Y row
  * unwritten and sets WQ_ERR_BAD_EXPERT in the device status.
- * Errors: as wq_gemm, plus n_tok*topk > WQ_MOE_MAX_SLOTS (WQ_ERR_UNSUPPORTED),
- * null ids, topk or n_experts <= 0 (WQ_ERR_INVALID_ARG), WQ_TC_BF16
- * (WQ_ERR_INVALID_ARG).
+ * Errors: as wq_gemm, plus null ids, topk or n_experts <= 0, n_tok * topk or
+ * m * n_experts above 2^31 - 1, WQ_TC_BF16 (all WQ_ERR_INVALID_ARG).
  */
 WQ_API wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtype,
                       unsigned flags, const float *X, const void *Wbank, const int32_t *ids,

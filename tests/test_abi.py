@@ -168,8 +168,13 @@ def test_layernorm_workspace_sizes_and_errors(lib):
 def test_unsupported_requests(lib):
     assert wq.wq_gemm(32, 8, 32, wq.WQ_Q8_0, wq.WQ_TC_BF16, A, A, None, None, A, 0) == \
         wq.WQ_ERR_UNSUPPORTED
-    assert wq.wq_moe_gemv(64, 5, 8, 8, 32, wq.WQ_Q4_0, 0, A, A, A, None, None, A, 0) == \
-        wq.WQ_ERR_UNSUPPORTED
+
+
+def test_moe_slot_count_limit(lib):
+    """Any n_tok * topk up to 2^31 - 1 is accepted (routed in windows); beyond the
+    int range the call is refused before touching the device."""
+    assert wq.wq_moe_gemv(1 << 16, (1 << 15) + 1, 8, 8, 32, wq.WQ_Q4_0, 0, A, A, A, None, None,
+                          A, 0) == wq.WQ_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -95,9 +95,13 @@ def test_algorithmic_bytes_of_the_float_gemvs(tag, wbytes):
 
 
 def test_traffic_record_is_dropped_when_its_source_changes(monkeypatch):
-    name = "moe_q4_0_E64_m1408_k2048_t16x6"
-    rec = dict(bench.TRAFFIC[name])
-    assert bench.traffic_for(name) == rec["bytes"]  # recorded on the source as committed
-    monkeypatch.setitem(bench.TRAFFIC, name, dict(rec, sha256="0" * 64))
+    import hashlib
+    src = "gemv_transformer_gb300/csrc/gemv_mma.cu"
+    with open(os.path.join(bench.ROOT, src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    name = "a_workload"
+    monkeypatch.setitem(bench.TRAFFIC, name, {"bytes": 123, "source": src, "sha256": sha})
+    assert bench.traffic_for(name) == 123  # recorded on the source as it stands
+    monkeypatch.setitem(bench.TRAFFIC, name, {"bytes": 123, "source": src, "sha256": "0" * 64})
     assert bench.traffic_for(name) is None
     assert bench.traffic_for("no_such_workload") is None
