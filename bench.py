@@ -47,6 +47,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GEMV HBM GB/s and GEMM TFLOP/s at 1 GB300, as % of roofline"
+WORKLOAD = ("bf16 GEMM n32 + Q8_0 GEMV + Q4_0 GEMV n1/4/8 + encoder GEMMs n1500 (tcgen05) "
+            "+ MoE Q4_0 E64 top6")
 UNIT = "% of roofline"
 N_EVENT_GRAPHS = 64
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
@@ -288,7 +290,21 @@ def cpu_baseline(ws, peaks, budget_s=12.0):
             "kind": "oracle",
             "sample": f"first {frac:.4%} of the output rows of every launch of one step "
                       f"(MoE: of the routed slots), median of 3, scaled to a full step; "
-                      f"full-step estimate {t_step:.2f} s"}
+                      f"full-step estimate {t_step:.2f} s",
+            "sample_fraction": frac,
+            "single_thread": oracle_single_thread(ws, roof, budget_s / 3)}
+
+
+def oracle_single_thread(ws, roof, budget_s):
+    """The same oracle on one host thread: a sample sized to about budget_s seconds,
+    median of 3, scaled to a full step."""
+    frac = 1.0 / 4096
+    t, _ = oracle_step_seconds(ws, frac, threads=1)
+    frac = min(1.0, frac * max(1.0, (budget_s / 3) / max(t, 1e-3)))
+    times = [oracle_step_seconds(ws, frac, threads=1)[0] for _ in range(3)]
+    t_step = float(np.median(times)) / frac
+    return {"value": roof / (t_step * 1e6) * 100.0, "unit": UNIT, "cores": 1,
+            "sample_fraction": frac, "full_step_s": t_step}
 
 
 # ------------------------------------------------------------ reference arm --
@@ -320,11 +336,14 @@ def run_reference(args):
            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "impl": "reference",
-           "config": {"workload": "bf16 GEMM n32 + Q8_0 GEMV + Q4_0 GEMV n1/4/8 + encoder "
-                                  "GEMMs n1500 + MoE Q4_0 E64 top6", "parallelism": "host cores"},
+           "config": {"workload": WORKLOAD, "parallelism": "host cores"},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                             "sample": f"each step: first {frac:.4%} of the output rows of "
-                                      "every launch, scaled to a full step"},
+                                      "every launch, scaled to a full step",
+                            "sample_fraction": frac,
+                            "single_thread": oracle_single_thread(ws, roof, 6.0)},
+           "sample_fraction": frac,
+           "extrapolated": frac < 1.0,
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -506,8 +525,20 @@ def run_gpu(args):
             plain[s % len(plain)].replay()
         torch.cuda.synchronize()
 
+        # Untimed replays for about 0.3 s before and after the timed region keep the
+        # GPU under the same load while nvidia-smi samples its clocks, so even a short
+        # timed region gets a clock record (samples every 50 ms over >= 0.6 s).
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for s in range(4):
+            plain[s % len(plain)].replay()
+        e1.record()
+        torch.cuda.synchronize()
+        roll = max(1, int(0.3e3 / max(e0.elapsed_time(e1) / 4, 1e-3)))
         clocks = ClockSampler(local)
         clocks.start()
+        for s in range(roll):
+            plain[s % len(plain)].replay()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         barrier(world)
@@ -518,7 +549,11 @@ def run_gpu(args):
         t_end.record()
         torch.cuda.synchronize()
         barrier(world)
+        for s in range(roll):
+            plain[s % len(plain)].replay()
+        torch.cuda.synchronize()
         clk = clocks.stop()
+        clk["window"] = f"{roll} untimed replays before and after the timed region"
         el_ms = t_start.elapsed_time(t_end)
         st = wq.wq_get_device_status()
         if st != 0:
@@ -642,8 +677,7 @@ def run_gpu(args):
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
            "data": "synthetic (seeded; shapes and distributions of the five workloads)",
-           "config": {"workload": "bf16 GEMM n32 + Q8_0 GEMV + Q4_0 GEMV n1/4/8 + encoder "
-                                  "GEMMs n1500 (tcgen05) + MoE Q4_0 E64 top6",
+           "config": {"workload": WORKLOAD,
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                       "l2": "inputs larger than L2: 2 rotating input sets of ~340 MB",
                       "calls_per_step": nl,

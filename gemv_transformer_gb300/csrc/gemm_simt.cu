@@ -11,10 +11,13 @@
 // serial f32 chain per output to k/32 + 32 terms.
 //
 // Grids smaller than one wave (small n and m, e.g. n = 32, m = 512) instead run
-// gemm_splitk_kernel: 32 x 32 output tiles, the k steps of a tile split across the
-// KS CTAs of a thread-block cluster (KS <= 8), each CTA summing its steps the same
-// way; each CTA then adds the KS partials of one slice of the tile, in rank order,
-// through distributed shared memory (deterministic) and applies the epilogue.
+// gemm_rows_kernel when k <= 2048: 32 x 8 output blocks, one per CTA, each with
+// the whole k loop (one warp per W row, one lane per X row).  With larger k they
+// run gemm_splitk_kernel: 32 x 32 output tiles, the k steps of a tile split across
+// the KS CTAs of a thread-block cluster (KS <= 8), each CTA summing its steps the
+// same way; each CTA then adds the KS partials of one slice of the tile, in rank
+// order, through distributed shared memory (deterministic) and applies the
+// epilogue.
 #include <cooperative_groups.h>
 
 #include "wq_device.cuh"
@@ -276,6 +279,76 @@ __global__ void __launch_bounds__(256) gemm_splitk_kernel(const GemmArgs a, int 
     cluster.sync();  // every rank keeps its shared memory until all slices are read
 }
 
+// Small grids with moderate k: one warp per W row and one lane per X row (32 x 8
+// outputs per CTA), the whole k loop in one CTA -- no cluster, no cross-CTA
+// reduction, so a call costs little more than its launch and two passes over
+// shared memory.  X and W are staged in chunks of RK values of k (W decoded
+// exactly into f32), all of a chunk's loads in flight at once; each lane sums each
+// chunk in four interleaved chains that are then added in a fixed order
+// (deterministic).
+constexpr int RK = 256;
+
+template <int WT, bool DUAL>
+__global__ void __launch_bounds__(256) gemm_rows_kernel(const GemmArgs a) {
+    pdl_enter();
+    __shared__ __align__(16) float xs[32][RK + 4];  // [token][k], padded: conflict-free float4 reads
+    __shared__ __align__(16) float ws[8][RK];       // [row][k], read as a warp broadcast
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 8;
+    const size_t rb = row_bytes(WT, a.k);
+    const int i = i0 + lane, j = j0 + warp;
+    // The epilogue's inputs are requested first, so their latency overlaps the loop.
+    const bool out = i < a.n && j < a.m;
+    const size_t o = (size_t)i * a.ldy + j;
+    const float bj = (out && (a.flags & kBias)) ? __ldg(a.bias + j) : 0.f;
+    const float rij = (out && (a.flags & kResidual)) ? a.R[o] : 0.f;  // may alias Y: plain load
+    float acc = 0.f;
+    for (int k0 = 0; k0 < a.k; k0 += RK) {
+        {   // X: row r, float4s q, q + 8, q + 16, q + 24 of the chunk (k % 4 == 0)
+            const int r = tid >> 3, q = tid & 7, i = i0 + r;
+#pragma unroll
+            for (int u = 0; u < RK / 32; ++u) {
+                const int t = k0 + 4 * (q + 8 * u);
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < a.n && t < a.k)
+                    v = __ldg(reinterpret_cast<const float4 *>(a.X + (size_t)i * a.k + t));
+                *reinterpret_cast<float4 *>(&xs[r][4 * (q + 8 * u)]) = v;
+            }
+        }
+        if (tid < 8 * (RK / 8)) {   // W: row r, eight weights from t0 (k % 8 == 0)
+            const int r = tid / (RK / 8), g = tid % (RK / 8), j = j0 + r, t0 = k0 + 8 * g;
+            float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (j < a.m && t0 < a.k) decode8<WT>(a.W + (size_t)j * rb, t0, w);
+            *reinterpret_cast<float4 *>(&ws[r][8 * g]) = make_float4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<float4 *>(&ws[r][8 * g + 4]) = make_float4(w[4], w[5], w[6], w[7]);
+        }
+        __syncthreads();
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll 16
+        for (int t = 0; t < RK; t += 4) {
+            const float4 xv = *reinterpret_cast<const float4 *>(&xs[lane][t]);
+            const float4 wv = *reinterpret_cast<const float4 *>(&ws[warp][t]);
+            c0 = fmaf(xv.x, wv.x, c0);
+            c1 = fmaf(xv.y, wv.y, c1);
+            c2 = fmaf(xv.z, wv.z, c2);
+            c3 = fmaf(xv.w, wv.w, c3);
+        }
+        acc += (c0 + c1) + (c2 + c3);
+        __syncthreads();
+    }
+    if (out) {
+        a.Y[o] = epilogue_vals(acc, a.flags, bj, rij, a.alpha);
+        if (DUAL && j < a.dual) a.Y[o + a.m] = acc + a.bias2[j];  // the raw second band
+    }
+}
+
+template <int WT>
+cudaError_t launch_rows_wt(const GemmArgs &a, cudaStream_t stream) {
+    const dim3 grid((unsigned)((a.m + 7) / 8), (unsigned)((a.n + 31) / 32));
+    if (a.dual > 0) return launch_pdl(gemm_rows_kernel<WT, true>, grid, dim3(256), 0, stream, a);
+    return launch_pdl(gemm_rows_kernel<WT, false>, grid, dim3(256), 0, stream, a);
+}
+
 template <int WT>
 cudaError_t launch_splitk_wt(const GemmArgs &a, int tiles_m, int tiles_n, int ks, int spr,
                              cudaStream_t stream) {
@@ -388,6 +461,17 @@ cudaError_t launch_simt(const GemmArgs &a, int wtype, dim3 grid, cudaStream_t st
 cudaError_t launch_gemm_simt(const GemmArgs &a, int wtype, const DeviceInfo &dev,
                              cudaStream_t stream) {
     dim3 grid((a.m + TJ - 1) / TJ, (a.n + TI - 1) / TI);
+    if ((long long)grid.x * grid.y < dev.sm_count && a.k <= 2048 &&
+        (long long)(a.n + 31) / 32 <= 65535) {
+        // Under one wave, moderate k: one CTA per 32 x 8 block of outputs, whole k.
+        switch (wtype) {
+        case kBF16: return launch_rows_wt<kBF16>(a, stream);
+        case kF16: return launch_rows_wt<kF16>(a, stream);
+        case kF32: return launch_rows_wt<kF32>(a, stream);
+        case kQ8_0: return launch_rows_wt<kQ8_0>(a, stream);
+        default: return launch_rows_wt<kQ4_0>(a, stream);
+        }
+    }
     if ((long long)grid.x * grid.y < dev.sm_count) {
         // Under one wave: split k across a cluster so that about one wave of CTAs runs.
         const long long tm = (a.m + SK - 1) / SK, tn = (a.n + SK - 1) / SK;

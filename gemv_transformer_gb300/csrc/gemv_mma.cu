@@ -39,9 +39,7 @@
 // tokens use four n-tiles the same way (two token halves).
 // The partial sums of the 16 warps are reduced in shared memory in a fixed
 // order (deterministic) and the epilogue (bias, erf-GELU, residual) is fused
-// into the store.  Before waiting for the previous grid, a GEMV CTA asks L2 to
-// prefetch its row range of W: no earlier kernel's stores can leave a stale copy
-// behind, as L2 is the point of coherence.
+// into the store.
 //
 // MoE routing: the n_tok * topk slots are taken in windows of at most 256; for
 // each window every CTA sorts the window's slots by (expert, slot) in shared
@@ -248,15 +246,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// Ask L2 to fetch [p, p + bytes) (16-byte aligned, bytes % 16 == 0) ahead of use.
-__device__ __forceinline__ void prefetch_l2_range(const uint8_t *p, size_t bytes) {
-    constexpr size_t kPiece = 32768;
-    for (size_t o = 0; o < bytes; o += kPiece) {
-        const uint32_t n = (uint32_t)(bytes - o < kPiece ? bytes - o : kPiece);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + o), "r"(n) : "memory");
-    }
-}
-
 // 4-byte global -> shared copy that does not hold a register (completes at
 // cp_async_wait_all).
 __device__ __forceinline__ void cp_async4(float *dst, const float *src) {
@@ -358,16 +347,8 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (threadIdx.x == kCW * 32) {  // the producer's thread
+    if (threadIdx.x == kCW * 32)  // the producer's thread
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap_t)) : "memory");
-        if (!MOE) {  // L2 prefetch of this CTA's rows (weights are never written by an earlier grid)
-            const long long tpe = (m + 15) / 16;
-            const long long u0 = tpe * blockIdx.x / gridDim.x, u1 = tpe * (blockIdx.x + 1) / gridDim.x;
-            const long long r1 = min((long long)m, u1 * 16);
-            if (r1 > u0 * 16)
-                prefetch_l2_range(a.W + (size_t)(u0 * 16) * row_bytes(WT, k), (size_t)(r1 - u0 * 16) * row_bytes(WT, k));
-        }
-    }
     pdl_wait();
     Sched sc;
     sc.tpe = (m + 15) / 16;
