@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     int *s_act = s_seg + kMaxSlots + 1;
     int *s_nact = s_act + kMaxSlots;
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(s_nact + 1);
+    // the producer's count of stages issued, kept here between routing windows so
+    // that it occupies no register of the consumer warps
+    long long *s_q = reinterpret_cast<long long *>(((uintptr_t)(s_nact + 2) + 7) & ~(uintptr_t)7);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -345,6 +348,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
             mbar_init(&empty[s], kCW);
         }
         *abort_flag = 0u;
+        *s_q = 0;
         fence_mbar_init();
     }
     if (threadIdx.x == kCW * 32)  // the producer's thread
@@ -355,7 +359,6 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     const int S_all = MOE ? a.n * a.topk : 0;
     const int n_win = MOE ? (S_all + kMaxSlots - 1) / kMaxSlots : 1;
     // Ring positions, carried across routing windows.
-    long long q = 0;       // producer: stages issued
     int qs = 0;            // consumers: stage of the next chunk
     uint32_t qph = 0u;     // its fill parity
     bool ok = true;        // consumers: no wait ran out
@@ -440,6 +443,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
         // by the TMA unit); they are computed and never stored.
         if (lane == 0) {
             const uint64_t policy = l2_evict_first();
+            long long q = *s_q;
             bool pok = true;
             for (long long u = sc.u0; u < sc.u1 && pok;) {
                 const int nt = group_tiles<T>(sc, u);
@@ -480,6 +484,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                 }
                 u += nt;
             }
+            *s_q = q;
         }
         __syncwarp();
     } else {
@@ -784,6 +789,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     }  // windows
     if (warp == kCW && lane == 0) {
         // Drain copies that no consumer waited for (only after an abort).
+        const long long q = *s_q;
         for (long long d = (q > S ? q - S : 0); d < q; ++d)
             mbar_wait(&full[d % S], (uint32_t)((d / S) & 1), kDrainPolls);
     }
@@ -808,7 +814,7 @@ constexpr size_t smem_bytes() {
     using L = Layout<WT, MODE, T, CW>;
     return (size_t)L::kStages * L::kStageBytes + L::kRedBytes + L::kEpiBytes +
            2 * L::kStages * sizeof(uint64_t) +
-           kMaxSlots * sizeof(unsigned long long) + (3 * kMaxSlots + 4) * sizeof(int) + 16;
+           kMaxSlots * sizeof(unsigned long long) + (3 * kMaxSlots + 4) * sizeof(int) + 32;
 }
 
 // The weight image as a 3-D tensor [matrices][m][row bytes] (one matrix for a GEMV,
