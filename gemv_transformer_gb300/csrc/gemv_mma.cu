@@ -201,6 +201,14 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
     return r;
 }
 
+// (a & b) | c as one three-input logic instruction (written out because the
+// compiler otherwise issues the AND and the OR separately here).
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
 // Q4_0: the four code bytes v = qs[4t..4t+3] of one row -> the A registers of the
 // block's two MMA k-steps, as exact f16 (q - 8).  Low nibbles (elements 4t..4t+3):
 // 0x6400 | q is 1024 + q, minus 1032.  High nibbles (elements 16+4t..16+4t+3) sit
@@ -211,10 +219,10 @@ __device__ __forceinline__ void decode_q4(uint32_t v, uint32_t &l02, uint32_t &l
                                           uint32_t &h02, uint32_t &h13) {
     const uint32_t v8 = v >> 8;
     const uint32_t one16 = 0x2C002C00u, m72 = 0xD480D480u, c1032 = 0x64086408u;
-    l02 = hsub2((v & 0x000F000Fu) | 0x64006400u, c1032);
-    l13 = hsub2((v8 & 0x000F000Fu) | 0x64006400u, c1032);
-    h02 = hfma2((v & 0x00F000F0u) | 0x64006400u, one16, m72);
-    h13 = hfma2((v8 & 0x00F000F0u) | 0x64006400u, one16, m72);
+    l02 = hsub2(and_or(v, 0x000F000Fu, 0x64006400u), c1032);
+    l13 = hsub2(and_or(v8, 0x000F000Fu, 0x64006400u), c1032);
+    h02 = hfma2(and_or(v, 0x00F000F0u, 0x64006400u), one16, m72);
+    h13 = hfma2(and_or(v8, 0x00F000F0u, 0x64006400u), one16, m72);
 }
 
 // Q8_0: four signed code bytes v = qs[j..j+3] -> f16 pairs (j, j+2) and (j+1, j+3),
@@ -290,14 +298,33 @@ struct Sched {
     long long u0, u1;   // this CTA's unit range
 };
 
-template <int T>
-__device__ __forceinline__ int group_tiles(const Sched &sc, long long u) {
-    const long long end_e = (u / sc.tpe + 1) * sc.tpe;
-    long long e = u + T;
-    if (e > end_e) e = end_e;
-    if (e > sc.u1) e = sc.u1;
-    return (int)(e - u);
-}
+// A walk over the CTA's unit range by row groups.  The position (slot ai among
+// the active experts, tile tl within it) is advanced by addition: one division
+// when the walk starts, none per group or per chunk.
+struct Walk {
+    long long u, u1;  // next unit, end of the range
+    int ai, tl, tpe;
+    __device__ __forceinline__ explicit Walk(const Sched &sc) : u(sc.u0), u1(sc.u1), tpe(sc.tpe) {
+        ai = (int)(u / tpe);
+        tl = (int)(u - (long long)ai * tpe);
+    }
+    __device__ __forceinline__ bool more() const { return u < u1; }
+    // Tiles in the next group: at most T, never past the expert or the range.
+    template <int T>
+    __device__ __forceinline__ int group() const {
+        long long e = T < tpe - tl ? T : tpe - tl;
+        if (e > u1 - u) e = u1 - u;
+        return (int)e;
+    }
+    __device__ __forceinline__ void advance(int nt) {
+        u += nt;
+        tl += nt;
+        if (tl == tpe) {
+            tl = 0;
+            ++ai;
+        }
+    }
+};
 
 template <int WT, bool MOE, int MODE, int T, int CW>
 __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
@@ -424,17 +451,6 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     sc.u0 = units * blockIdx.x / gridDim.x;
     sc.u1 = units * (blockIdx.x + 1) / gridDim.x;
 
-    auto group_tokens = [&](long long u, int &seg0) -> int {
-        if (!MOE) {
-            seg0 = 0;
-            return a.n;
-        }
-        const int ai = (int)(u / sc.tpe);
-        seg0 = s_seg[ai];
-        return s_seg[ai + 1] - seg0;
-    };
-    auto tile_row = [&](long long u) -> int { return (int)(u % sc.tpe) * 16; };
-    auto tile_mat = [&](long long u) -> int { return MOE ? s_act[(int)(u / sc.tpe)] : 0; };
 
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
@@ -443,17 +459,27 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
         // by the TMA unit); they are computed and never stored.
         if (lane == 0) {
             const uint64_t policy = l2_evict_first();
-            long long q = *s_q;
+            long long q = *s_q;                 // stages issued so far
+            int s = (int)(q % S);               // the next one's ring slot
+            uint32_t wrap = (uint32_t)((q / S) & 1);  // and the parity of its round
             bool pok = true;
-            for (long long u = sc.u0; u < sc.u1 && pok;) {
-                const int nt = group_tiles<T>(sc, u);
-                int seg0;
-                const int ntok = group_tokens(u, seg0);
+            for (Walk wk(sc); wk.more() && pok;) {
+                const int nt = wk.group<T>();
+                const int seg0 = MOE ? s_seg[wk.ai] : 0;
+                const int ntok = MOE ? s_seg[wk.ai + 1] - seg0 : a.n;
+                const int trow = wk.tl * 16, tmat = MOE ? s_act[wk.ai] : 0;
                 for (int p0 = 0; p0 < ntok && pok; p0 += P_MAX) {
+                    const int npass = min(P_MAX, ntok - p0);
+                    // X rows of the pass's tokens (MoE: the token of a slot is slot / topk).
+                    int tok[MOE ? P_MAX : 1];
+                    if constexpr (MOE) {
+    #pragma unroll
+                        for (int i = 0; i < P_MAX; ++i)
+                            tok[i] = i < npass ? s_sorted[seg0 + p0 + i] / a.topk : 0;
+                    }
                     for (int c = 0; c < KC; ++c, ++q) {
-                        const int s = (int)(q % S);
-                        if (q >= S) {
-                            const uint32_t par = (uint32_t)(((q / S) - 1) & 1);
+                        if (q >= S) {  // wait until the consumers released the slot's previous round
+                            const uint32_t par = wrap ^ 1u;
                             bool w = mbar_test_wait(&empty[s], par);
                             for (uint64_t i = 1; !w && i < limit && !*abort_flag; ++i)
                                 w = mbar_try_wait(&empty[s], par);
@@ -465,24 +491,28 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                             }
                         }
                         // X of the pass's tokens for this chunk (256 or 512 floats each).
-                        const int npass = min(P_MAX, ntok - p0);
                         const uint32_t xbytes = (uint32_t)min(kBlocks * 32, k - c * kBlocks * 32) * 4u;
                         mbar_arrive_expect_tx(&full[s], (uint32_t)L::kWBytes + npass * xbytes);
                         uint8_t *dst = stages + (size_t)s * L::kStageBytes;
                         for (int bx = 0; bx < F::NBOX; ++bx) {
                             const int x = (c * F::NBOX + bx) * (F::ROWB / 2);
-                            tma_load_3d(dst + bx * L::kBoxBytes, &wmap_t, x, tile_row(u), tile_mat(u),
-                                        &full[s], policy);
+                            tma_load_3d(dst + bx * L::kBoxBytes, &wmap_t, x, trow, tmat, &full[s],
+                                        policy);
                         }
-                        for (int i = 0; i < npass; ++i) {
-                            const int tok = MOE ? s_sorted[seg0 + p0 + i] / a.topk : p0 + i;
-                            bulk_g2s_nohint(dst + L::kWBytes + i * kXChunkBytes,
-                                            a.X + (size_t)tok * k + (size_t)c * kBlocks * 32,
-                                            xbytes, &full[s]);
+    #pragma unroll
+                        for (int i = 0; i < P_MAX; ++i)
+                            if (i < npass)
+                                bulk_g2s_nohint(dst + L::kWBytes + i * kXChunkBytes,
+                                                a.X + (size_t)(MOE ? tok[MOE ? i : 0] : p0 + i) * k +
+                                                    (size_t)c * kBlocks * 32,
+                                                xbytes, &full[s]);
+                        if (++s == S) {
+                            s = 0;
+                            wrap ^= 1u;
                         }
                     }
                 }
-                u += nt;
+                wk.advance(nt);
             }
             *s_q = q;
         }
@@ -490,13 +520,12 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     } else {
 
     // ---------------------------------------------------------------- consumers
-    for (long long u = sc.u0; u < sc.u1 && ok;) {
-        const int ntiles = group_tiles<T>(sc, u);
-        int seg0;
-        const int ntok_all = group_tokens(u, seg0);
-        const int ai = (int)(u / sc.tpe);
-        const int e = MOE ? s_act[ai] : 0;
-        const int row0 = (int)(u % sc.tpe) * 16;
+    for (Walk wk(sc); wk.more() && ok;) {
+        const int ntiles = wk.group<T>();
+        const int seg0 = MOE ? s_seg[wk.ai] : 0;
+        const int ntok_all = MOE ? s_seg[wk.ai + 1] - seg0 : a.n;
+        const int e = MOE ? s_act[wk.ai] : 0;
+        const int row0 = wk.tl * 16;
         for (int p0 = 0; p0 < ntok_all && ok; p0 += P_MAX) {
             const int ntok = min(P_MAX, ntok_all - p0);
             // One pass over the group's chunks; the column layout is a compile-time
@@ -779,7 +808,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                 pass(std::false_type{});
             }
         }
-        u += ntiles;
+        wk.advance(ntiles);
     }
     }  // consumers
     // The window's routing tables are rewritten by the next window: every thread is
