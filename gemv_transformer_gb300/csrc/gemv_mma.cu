@@ -117,15 +117,19 @@ struct Layout {
     static constexpr int kStageBytes = kWBytes + Mode<MODE>::P_MAX * Warps<CW>::kXChunkBytes;
     // epilogue inputs staged at the start of a pass: residual [P_MAX][T*16], bias [T*16]
     static constexpr int kEpiBytes = (T * 16 * Mode<MODE>::P_MAX + T * 16) * 4;
+    // per consumer warp: two tokens x two terms x four threads x 16 bytes of B
+    // fragments, then 16 zero bytes for the padding columns
+    static constexpr int kCoopBytes = MODE == kPacked ? CW * 272 : 0;
     // Partial-sum buffers of the ordered reduction: 8 (two rounds of warps, three
     // barriers per pass) when they cost no pipeline stage, else 4 (four rounds).
     static constexpr int stages_with(int bufs) {
-        return (kBudgetAll - bufs * T * 16 * Mode<MODE>::C * 4 - kEpiBytes) / kStageBytes;
+        return (kBudgetAll - bufs * T * 16 * Mode<MODE>::C * 4 - kEpiBytes - kCoopBytes) /
+               kStageBytes;
     }
     static constexpr int kRedBufs =
         (stages_with(8) >= 8 || stages_with(8) == stages_with(4)) ? 8 : 4;
     static constexpr int kRedBytes = kRedBufs * T * 16 * Mode<MODE>::C * 4;
-    static constexpr int kBudget = kBudgetAll - kRedBytes - kEpiBytes;
+    static constexpr int kBudget = kBudgetAll - kRedBytes - kEpiBytes - kCoopBytes;
     static constexpr int kStages = (kBudget / kStageBytes) > 8 ? 8 : (kBudget / kStageBytes);
     static_assert(kStages >= 2, "at least two stages");
 };
@@ -237,11 +241,27 @@ __device__ __forceinline__ void decode_q8(uint32_t v, uint32_t &p02, uint32_t &p
 // The power of two s = 2^e that brings a block's largest |x| into [2^14, 2^15)
 // (so every scaled value is below f16's 65504), and 1/s; e is clamped to
 // [-113, 126] so both stay normal f32.
-__device__ __forceinline__ void block_scale(float mx, float &s, float &inv) {
-    const int E = (int)((__float_as_uint(mx) >> 23) & 0xFFu);
+__device__ __forceinline__ void block_scale_bits(uint32_t mx_bits, float &s, float &inv) {
+    const int E = (int)((mx_bits >> 23) & 0xFFu);
     const int sb = min(253, max(1, 268 - E));
     s = __uint_as_float((uint32_t)sb << 23);
     inv = __uint_as_float((uint32_t)(254 - sb) << 23);
+}
+
+__device__ __forceinline__ void block_scale(float mx, float &s, float &inv) {
+    block_scale_bits(__float_as_uint(mx), s, inv);
+}
+
+// f32 -> f16 bits (round to nearest even) and back.
+__device__ __forceinline__ uint16_t f16_rn(float v) {
+    unsigned short h;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(v));
+    return h;
+}
+__device__ __forceinline__ float f16_f32(uint16_t h) {
+    float v;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(v) : "h"(h));
+    return v;
 }
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y,
@@ -305,7 +325,7 @@ struct Walk {
     long long u, u1;  // next unit, end of the range
     int ai, tl, tpe;
     __device__ __forceinline__ explicit Walk(const Sched &sc) : u(sc.u0), u1(sc.u1), tpe(sc.tpe) {
-        ai = (int)(u / tpe);
+        ai = u < (1ll << 32) ? (int)((uint32_t)u / (uint32_t)tpe) : (int)(u / tpe);
         tl = (int)(u - (long long)ai * tpe);
     }
     __device__ __forceinline__ bool more() const { return u < u1; }
@@ -350,7 +370,8 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     float *red = reinterpret_cast<float *>(smem + (size_t)S * L::kStageBytes);  // [4][T*16][C]
     float *s_res = red + L::kRedBufs * T * 16 * C;   // [P_MAX][T*16]
     float *s_bias = s_res + T * 16 * P_MAX;           // [T*16]
-    uint64_t *full = reinterpret_cast<uint64_t *>(s_bias + T * 16);
+    uint8_t *s_coop = reinterpret_cast<uint8_t *>(s_bias + T * 16);  // [CW][272], 16-aligned
+    uint64_t *full = reinterpret_cast<uint64_t *>(s_coop + L::kCoopBytes);
     uint64_t *empty = full + S;
     unsigned long long *s_key = reinterpret_cast<unsigned long long *>(empty + S);
     int *s_sorted = reinterpret_cast<int *>(s_key + kMaxSlots);
@@ -378,6 +399,8 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
         *s_q = 0;
         fence_mbar_init();
     }
+    if (L::kCoopBytes > 0 && warp < kCW && lane < 4)
+        reinterpret_cast<uint32_t *>(s_coop + warp * 272 + 256)[lane] = 0u;
     if (threadIdx.x == kCW * 32)  // the producer's thread
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap_t)) : "memory");
     pdl_wait();
@@ -448,8 +471,14 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     if (*abort_flag) break;  // the same in every thread after the barrier
     sc.n_act = MOE ? *s_nact : 1;
     const long long units = (long long)sc.n_act * sc.tpe;
-    sc.u0 = units * blockIdx.x / gridDim.x;
-    sc.u1 = units * (blockIdx.x + 1) / gridDim.x;
+    if (units * gridDim.x < (1ll << 32)) {  // the usual case: 32-bit divisions
+        const uint32_t uu = (uint32_t)units;
+        sc.u0 = uu * blockIdx.x / gridDim.x;
+        sc.u1 = uu * (blockIdx.x + 1) / gridDim.x;
+    } else {
+        sc.u0 = units * blockIdx.x / gridDim.x;
+        sc.u1 = units * (blockIdx.x + 1) / gridDim.x;
+    }
 
 
     if (warp == kCW) {
@@ -530,10 +559,13 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
             const int ntok = min(P_MAX, ntok_all - p0);
             // One pass over the group's chunks; the column layout is a compile-time
             // choice so the tile loop carries no layout branches.
-            auto pass = [&](auto pk) {
+            auto pass = [&](auto pk, auto ck) {
                 // packed: 1-4 tokens, column g = term (g / P) of token (g % P), one n-tile;
                 // else split-major: n-tile s, column g = token g (+8 for the second half).
                 constexpr bool packed = decltype(pk)::value;
+                // one- and two-token packed passes: each lane splits one element of its
+                // block per token and the warp shares the B fragments through s_coop
+                constexpr bool COOP = packed && decltype(ck)::value && L::kCoopBytes > 0;
                 const int P = packed ? ntok : (WIDE ? 16 : 8);
                 int xslot[NH];  // the token slot of this thread's B column in the stage
                 bool tok_ok[NH];
@@ -545,6 +577,16 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                     xslot[h] = tok_ok[h] ? i : 0;
                 }
                 if (packed) col_s = g / P;
+                int coop_w = 0, coop_r = 256;  // u16 index of lane's write; byte offset of the read
+                if constexpr (COOP) {
+                    const int j = lane;
+                    const int tt = WT == kQ4_0 ? (j & 15) >> 2 : j >> 3;
+                    const int w = WT == kQ4_0 ? j & 3 : j & 7;
+                    const int pair = WT == kQ4_0 ? 2 * (j >> 4) + (w & 1) : 2 * (w >> 2) + (w & 1);
+                    const int half = WT == kQ4_0 ? w >> 1 : (w >> 1) & 1;
+                    coop_w = tt * 8 + pair * 2 + half;
+                    if (g < 2 * P) coop_r = (((g % P) * 2 + g / P) * 4 + t) * 16;
+                }
 
                 // Stage this pass's bias and residual values in shared memory now, so the
                 // epilogue does not wait on global loads (same index map as the epilogue).
@@ -600,64 +642,98 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                     if (c * kBlocks + wb < nb) {
                         // B: each token's block scaled by a power of two (block_scale), then
                         // split into two f16 terms; pairs in the A decode's order.
-                        uint32_t sp[NH][4][2];
-                        float inv_own[NH];
-                        const uint8_t *xst = stages + (size_t)s * L::kStageBytes + L::kWBytes;
-    #pragma unroll
-                        for (int h = 0; h < NH; ++h) {
-                            // This thread's 8 values of its column's token, in the A decode's
-                            // order (zeros for a padding column).
-                            float xv[8];
-                            float4 u0v = make_float4(0.f, 0.f, 0.f, 0.f), u1v = u0v;
-                            if (tok_ok[h]) {
-                                const float *xp = reinterpret_cast<const float *>(
-                                    xst + xslot[h] * kXChunkBytes) + wb * 32;
-                                u0v = *reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 4 * t : 8 * t));
-                                u1v = *reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 16 + 4 * t : 8 * t + 4));
-                            }
-                            xv[0] = u0v.x; xv[1] = u0v.y; xv[2] = u0v.z; xv[3] = u0v.w;
-                            xv[4] = u1v.x; xv[5] = u1v.y; xv[6] = u1v.z; xv[7] = u1v.w;
-                            float mx = 0.f;
-    #pragma unroll
-                            for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(xv[j]));
-                            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-                            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-                            float sc;
-                            block_scale(mx, sc, inv_own[h]);
-                            float xs[8];
-    #pragma unroll
-                            for (int j = 0; j < 8; ++j) xs[j] = xv[j] * sc;
-                            split2(xs[0], xs[2], sp[h][0][0], sp[h][0][1]);
-                            split2(xs[1], xs[3], sp[h][1][0], sp[h][1][1]);
-                            split2(xs[4], xs[6], sp[h][2][0], sp[h][2][1]);
-                            split2(xs[5], xs[7], sp[h][3][0], sp[h][3][1]);
-                        }
-                        // 1/scale of the accumulator columns 2t and 2t+1: that of the threads
-                        // whose B column they are (g = 2t, 2t+1).
-                        float inv0[NH], inv1[NH];
-    #pragma unroll
-                        for (int h = 0; h < NH; ++h) {
-                            inv0[h] = __shfl_sync(0xFFFFFFFFu, inv_own[h], 8 * t);
-                            inv1[h] = __shfl_sync(0xFFFFFFFFu, inv_own[h], 8 * t + 4);
-                        }
-                        // B fragments [k-step][n-tile][reg]: k-step 0 uses pairs 0,1; k-step 1 pairs 2,3.
                         uint32_t bf[2][NT][2];
+                        float inv0[NH], inv1[NH];
+                        if constexpr (COOP) {
+                            // Lane j takes element j of the block for each token: scale, split,
+                            // and store both terms at the fragment slot that wants them
+                            // ([token][term][thread t][pair][half], f16).
+                            const float *xb = reinterpret_cast<const float *>(
+                                stages + (size_t)s * L::kStageBytes + L::kWBytes) + wb * 32 + lane;
+                            uint16_t *cw = reinterpret_cast<uint16_t *>(s_coop + wb * 272) + coop_w;
+                            float invp[2];
+                            auto split_one = [&](int p) {
+                                const float x = xb[p * (kXChunkBytes / 4)];
+                                const uint32_t mb =
+                                    __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(x) & 0x7FFFFFFFu);
+                                float sc;
+                                block_scale_bits(mb, sc, invp[p]);
+                                const float xs = x * sc;
+                                const uint16_t h1 = f16_rn(xs);
+                                cw[p * 64] = h1;
+                                cw[p * 64 + 32] = f16_rn(xs - f16_f32(h1));
+                            };
+                            split_one(0);
+                            if (ntok > 1)
+                                split_one(1);
+                            else
+                                invp[1] = invp[0];
+                            __syncwarp();
+                            const uint4 bv = *reinterpret_cast<const uint4 *>(s_coop + wb * 272 + coop_r);
+                            bf[0][0][0] = bv.x;
+                            bf[0][0][1] = bv.y;
+                            bf[1][0][0] = bv.z;
+                            bf[1][0][1] = bv.w;
+                            inv0[0] = invp[0];
+                            inv1[0] = invp[1];
+                        } else {
+                            uint32_t sp[NH][4][2];
+                            float inv_own[NH];
+                            const uint8_t *xst = stages + (size_t)s * L::kStageBytes + L::kWBytes;
     #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
+                            for (int h = 0; h < NH; ++h) {
+                                // This thread's 8 values of its column's token, in the A decode's
+                                // order (zeros for a padding column).
+                                float xv[8];
+                                float4 u0v = make_float4(0.f, 0.f, 0.f, 0.f), u1v = u0v;
+                                if (tok_ok[h]) {
+                                    const float *xp = reinterpret_cast<const float *>(
+                                        xst + xslot[h] * kXChunkBytes) + wb * 32;
+                                    u0v = *reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 4 * t : 8 * t));
+                                    u1v = *reinterpret_cast<const float4 *>(xp + (WT == kQ4_0 ? 16 + 4 * t : 8 * t + 4));
+                                }
+                                xv[0] = u0v.x; xv[1] = u0v.y; xv[2] = u0v.z; xv[3] = u0v.w;
+                                xv[4] = u1v.x; xv[5] = u1v.y; xv[6] = u1v.z; xv[7] = u1v.w;
+                                float mx = 0.f;
     #pragma unroll
-                            for (int ks = 0; ks < 2; ++ks) {
+                                for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(xv[j]));
+                                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+                                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+                                float sc;
+                                block_scale(mx, sc, inv_own[h]);
+                                float xs[8];
     #pragma unroll
-                                for (int rr = 0; rr < 2; ++rr) {
-                                    const int pr = ks * 2 + rr;
-                                    uint32_t v;
-                                    if (WIDE) {
-                                        v = sp[nt & 1][pr][nt >> 1];  // n-tile = 2 * term + half
-                                    } else if (packed) {
-                                        v = col_s == 0 ? sp[0][pr][0] : sp[0][pr][1];
-                                    } else {
-                                        v = sp[0][pr][nt];            // n-tile = term
+                                for (int j = 0; j < 8; ++j) xs[j] = xv[j] * sc;
+                                split2(xs[0], xs[2], sp[h][0][0], sp[h][0][1]);
+                                split2(xs[1], xs[3], sp[h][1][0], sp[h][1][1]);
+                                split2(xs[4], xs[6], sp[h][2][0], sp[h][2][1]);
+                                split2(xs[5], xs[7], sp[h][3][0], sp[h][3][1]);
+                            }
+                            // 1/scale of the accumulator columns 2t and 2t+1: that of the threads
+                            // whose B column they are (g = 2t, 2t+1).
+    #pragma unroll
+                            for (int h = 0; h < NH; ++h) {
+                                inv0[h] = __shfl_sync(0xFFFFFFFFu, inv_own[h], 8 * t);
+                                inv1[h] = __shfl_sync(0xFFFFFFFFu, inv_own[h], 8 * t + 4);
+                            }
+                            // B fragments [k-step][n-tile][reg]: k-step 0 uses pairs 0,1; k-step 1 pairs 2,3.
+    #pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+    #pragma unroll
+                                for (int ks = 0; ks < 2; ++ks) {
+    #pragma unroll
+                                    for (int rr = 0; rr < 2; ++rr) {
+                                        const int pr = ks * 2 + rr;
+                                        uint32_t v;
+                                        if (WIDE) {
+                                            v = sp[nt & 1][pr][nt >> 1];  // n-tile = 2 * term + half
+                                        } else if (packed) {
+                                            v = col_s == 0 ? sp[0][pr][0] : sp[0][pr][1];
+                                        } else {
+                                            v = sp[0][pr][nt];            // n-tile = term
+                                        }
+                                        bf[ks][nt][rr] = v;
                                     }
-                                    bf[ks][nt][rr] = v;
                                 }
                             }
                         }
@@ -797,15 +873,22 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                 }
                 consumers_sync<CW>();
             };
+            using Y = std::true_type;
+            using N = std::false_type;
             if constexpr (MODE == kPacked) {
-                pass(std::true_type{});
-            } else if constexpr (MODE == kMixed) {
-                if (ntok <= 4)
-                    pass(std::true_type{});
+                if (ntok <= 2)
+                    pass(Y{}, Y{});
                 else
-                    pass(std::false_type{});
+                    pass(Y{}, N{});
+            } else if constexpr (MODE == kMixed) {
+                // (MoE: with eight consumer warps per CTA the shared split's longer
+                // dependency chain per chunk costs more than it saves; measured)
+                if (ntok <= 4)
+                    pass(Y{}, N{});
+                else
+                    pass(N{}, N{});
             } else {
-                pass(std::false_type{});
+                pass(N{}, N{});
             }
         }
         wk.advance(ntiles);
@@ -841,7 +924,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 template <int WT, int MODE, int T, int CW>
 constexpr size_t smem_bytes() {
     using L = Layout<WT, MODE, T, CW>;
-    return (size_t)L::kStages * L::kStageBytes + L::kRedBytes + L::kEpiBytes +
+    return (size_t)L::kStages * L::kStageBytes + L::kRedBytes + L::kEpiBytes + L::kCoopBytes +
            2 * L::kStages * sizeof(uint64_t) +
            kMaxSlots * sizeof(unsigned long long) + (3 * kMaxSlots + 4) * sizeof(int) + 32;
 }
