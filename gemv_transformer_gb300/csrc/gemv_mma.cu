@@ -346,9 +346,16 @@ struct Walk {
     }
 };
 
+// Tensor maps of the weight image, one per box height: the group's T tiles, and
+// 4, 2 and 1 tiles, from which a shorter group's rows are composed (binary
+// decomposition of its tile count), so that a short group moves only its own rows.
+struct WMaps {
+    CUtensorMap full, b4, b2, b1;
+};
+
 template <int WT, bool MOE, int MODE, int T, int CW>
 __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
-    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap_t, const StreamArgs a) {
+    gemv_mma_kernel(const __grid_constant__ WMaps wm, const StreamArgs a) {
     // The barriers and the weight map's descriptor are set up before waiting for
     // the previous grid (they touch nothing it writes); global memory after.
     pdl_launch();
@@ -402,7 +409,12 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     if (L::kCoopBytes > 0 && warp < kCW && lane < 4)
         reinterpret_cast<uint32_t *>(s_coop + warp * 272 + 256)[lane] = 0u;
     if (threadIdx.x == kCW * 32)  // the producer's thread
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap_t)) : "memory");
+    {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wm.full)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wm.b1)) : "memory");
+        if (T > 2) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wm.b2)) : "memory");
+        if (T > 4) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wm.b4)) : "memory");
+    }
     pdl_wait();
     Sched sc;
     sc.tpe = (m + 15) / 16;
@@ -418,21 +430,65 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
         // Sort the window's slots by (expert, slot); bad ids go last.
         const int base = win * kMaxSlots;
         const int Sl = min(kMaxSlots, S_all - base);
-        const unsigned long long big = 1ull << 62;
-        for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
-            const int e = a.ids[base + i];
-            const bool okid = e >= 0 && e < a.n_experts;
-            if (!okid && blockIdx.x == 0) record_status(a.status, kStBadExpert);
-            s_key[i] = okid ? ((unsigned long long)e << 16) | (unsigned)i : big | (unsigned)i;
+        const bool k32_ok = a.n_experts < (1 << 24) - 1;
+        uint32_t *k32 = reinterpret_cast<uint32_t *>(s_key);
+        if (k32_ok) {
+            // 32-bit keys expert << 8 | slot (a bad id as expert 0xFFFFFF), padded to
+            // a whole number of 16-byte quads with keys that rank below none; each
+            // key's rank is counted by up to four threads over slices of the quads.
+            int *s_rank = reinterpret_cast<int *>(k32 + kMaxSlots);
+            for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
+                const int e = a.ids[base + i];
+                const bool okid = e >= 0 && e < a.n_experts;
+                if (!okid && blockIdx.x == 0) record_status(a.status, kStBadExpert);
+                k32[i] = ((okid ? (uint32_t)e : 0xFFFFFFu) << 8) | (uint32_t)i;
+                s_rank[i] = 0;
+            }
+            const int nq = (Sl + 3) / 4;
+            if (threadIdx.x < 4 * nq - Sl) k32[Sl + threadIdx.x] = 0xFFFFFFFFu;
+            __syncthreads();
+            const int parts = max(1, min(4, (int)blockDim.x / Sl));
+            const int qper = (nq + parts - 1) / parts;
+            for (int idx = threadIdx.x; idx < Sl * parts; idx += blockDim.x) {
+                const int part = idx / Sl, i = idx - part * Sl;
+                const uint32_t ki = k32[i];
+                int r = 0;
+                const int q1 = min(nq, (part + 1) * qper);
+                for (int q = part * qper; q < q1; ++q) {
+                    const uint4 kk = reinterpret_cast<const uint4 *>(k32)[q];
+                    r += (int)(kk.x < ki) + (int)(kk.y < ki) + (int)(kk.z < ki) + (int)(kk.w < ki);
+                }
+                atomicAdd(&s_rank[i], r);
+            }
+            __syncthreads();
+            for (int i = threadIdx.x; i < Sl; i += blockDim.x) s_sorted[s_rank[i]] = base + i;
+        } else {
+            const unsigned long long big = 1ull << 62;
+            for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
+                const int e = a.ids[base + i];
+                const bool okid = e >= 0 && e < a.n_experts;
+                if (!okid && blockIdx.x == 0) record_status(a.status, kStBadExpert);
+                s_key[i] = okid ? ((unsigned long long)e << 16) | (unsigned)i : big | (unsigned)i;
+            }
+            __syncthreads();
+            for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
+                const unsigned long long ki = s_key[i];
+                int r = 0;
+                for (int i2 = 0; i2 < Sl; ++i2) r += s_key[i2] < ki;
+                s_sorted[r] = base + i;  // the slot's global index
+            }
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
-            const unsigned long long ki = s_key[i];
-            int r = 0;
-            for (int i2 = 0; i2 < Sl; ++i2) r += s_key[i2] < ki;
-            s_sorted[r] = base + i;  // the slot's global index
-        }
-        __syncthreads();
+        // The expert of the r-th sorted slot, or -1 for a bad id.
+        auto sorted_expert = [&](int r) -> int {
+            const int i = s_sorted[r] - base;
+            if (k32_ok) {
+                const uint32_t e = k32[i] >> 8;
+                return e == 0xFFFFFFu ? -1 : (int)e;
+            }
+            const unsigned long long kr = s_key[i];
+            return (kr >> 62) ? -1 : (int)(kr >> 16);
+        };
         if (warp == 0) {  // segment starts of the sorted slots, by ballot and prefix count
             int na = 0;
             for (int b0 = 0; b0 < Sl; b0 += 32) {
@@ -440,10 +496,9 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                 bool valid = false, start = false;
                 int e = 0;
                 if (r < Sl) {
-                    const unsigned long long kr = s_key[s_sorted[r] - base];
-                    valid = !(kr & big);
-                    e = (int)(kr >> 16);
-                    start = valid && (r == 0 || (int)(s_key[s_sorted[r - 1] - base] >> 16) != e);
+                    e = sorted_expert(r);
+                    valid = e >= 0;
+                    start = valid && (r == 0 || sorted_expert(r - 1) != e);
                 }
                 const unsigned sm = __ballot_sync(0xFFFFFFFFu, start);
                 if (start) {
@@ -471,7 +526,31 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     if (*abort_flag) break;  // the same in every thread after the barrier
     sc.n_act = MOE ? *s_nact : 1;
     const long long units = (long long)sc.n_act * sc.tpe;
-    if (units * gridDim.x < (1ll << 32)) {  // the usual case: 32-bit divisions
+    bool by_group = false;
+    if (MOE && units * gridDim.x < (1ll << 32)) {
+        // MoE: split by whole groups of T tiles when that is cheaper.  A pass over a
+        // group costs about seven tiles' worth of per-chunk work besides its tiles
+        // (measured), and a split by tiles gives a CTA an extra, short group wherever
+        // its range crosses an expert's end.
+        const uint32_t tpe = (uint32_t)sc.tpe, grid = gridDim.x;
+        const uint32_t gpe = (tpe + T - 1) / T;                 // groups per expert
+        const uint32_t G = (uint32_t)sc.n_act * gpe;
+        const uint32_t per_g = (G + grid - 1) / grid;
+        const uint32_t per_t = ((uint32_t)units + grid - 1) / grid;
+        const uint32_t cost_g = per_g * (7 + T);
+        const uint32_t cost_t = ((per_t + T - 1) / T + (per_t > 1 ? 1 : 0)) * 7 + per_t;
+        if (cost_g < cost_t) {
+            by_group = true;
+            auto unit_of = [&](uint32_t gi) -> long long {
+                const uint32_t e = gi / gpe;
+                return (long long)e * tpe + (long long)(gi - e * gpe) * T;
+            };
+            sc.u0 = unit_of(G * blockIdx.x / grid);
+            sc.u1 = unit_of(G * (blockIdx.x + 1) / grid);
+        }
+    }
+    if (by_group) {
+    } else if (units * gridDim.x < (1ll << 32)) {  // the usual case: 32-bit divisions
         const uint32_t uu = (uint32_t)units;
         sc.u0 = uu * blockIdx.x / gridDim.x;
         sc.u1 = uu * (blockIdx.x + 1) / gridDim.x;
@@ -483,9 +562,9 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
 
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
-        // Every group is one tall box per NBOX (T tiles of rows).  A short group's
-        // extra rows belong to the next group or lie past the matrix (zero-filled
-        // by the TMA unit); they are computed and never stored.
+        // A full group is one tall box per NBOX (T tiles of rows); a shorter one is
+        // composed of boxes of 4, 2 and 1 tiles.  Rows past the matrix's end are
+        // zero-filled by the TMA unit; they are computed and never stored.
         if (lane == 0) {
             const uint64_t policy = l2_evict_first();
             long long q = *s_q;                 // stages issued so far
@@ -521,12 +600,30 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                         }
                         // X of the pass's tokens for this chunk (256 or 512 floats each).
                         const uint32_t xbytes = (uint32_t)min(kBlocks * 32, k - c * kBlocks * 32) * 4u;
-                        mbar_arrive_expect_tx(&full[s], (uint32_t)L::kWBytes + npass * xbytes);
+                        const uint32_t wbytes =
+                            nt == T ? (uint32_t)L::kWBytes : (uint32_t)(F::NBOX * nt * L::kTileBytes);
+                        mbar_arrive_expect_tx(&full[s], wbytes + npass * xbytes);
                         uint8_t *dst = stages + (size_t)s * L::kStageBytes;
                         for (int bx = 0; bx < F::NBOX; ++bx) {
                             const int x = (c * F::NBOX + bx) * (F::ROWB / 2);
-                            tma_load_3d(dst + bx * L::kBoxBytes, &wmap_t, x, trow, tmat, &full[s],
-                                        policy);
+                            uint8_t *bd = dst + bx * L::kBoxBytes;
+                            if (nt == T) {
+                                tma_load_3d(bd, &wm.full, x, trow, tmat, &full[s], policy);
+                            } else {  // tile tt of the group lands where it would in a full box
+                                int t0 = 0;
+                                if (T > 4 && (nt & 4)) {
+                                    tma_load_3d(bd, &wm.b4, x, trow, tmat, &full[s], policy);
+                                    t0 = 4;
+                                }
+                                if (T > 2 && (nt & 2)) {
+                                    tma_load_3d(bd + t0 * L::kTileBytes, &wm.b2, x, trow + 16 * t0,
+                                                tmat, &full[s], policy);
+                                    t0 += 2;
+                                }
+                                if (nt & 1)
+                                    tma_load_3d(bd + t0 * L::kTileBytes, &wm.b1, x, trow + 16 * t0,
+                                                tmat, &full[s], policy);
+                            }
                         }
     #pragma unroll
                         for (int i = 0; i < P_MAX; ++i)
@@ -738,12 +835,13 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                             }
                         }
                         const uint8_t *st = stages + (size_t)s * L::kStageBytes + blk_off;
-                        // Every tile of the stage is computed; rows of tiles past the group's
-                        // end hold stale bytes and are never reduced or stored.
-                        auto tiles = [&](auto aligned) {
+                        // Only the group's tiles are loaded and computed.
+                        auto tiles = [&](auto aligned, auto whole) {
                             constexpr bool AL = decltype(aligned)::value;
+                            constexpr bool FULL = decltype(whole)::value;
     #pragma unroll
                             for (int tt = 0; tt < T; ++tt) {
+                                if (!FULL && tt >= ntiles) break;
                                 const uint8_t *r0p = st + tt * L::kTileBytes;
                                 const uint8_t *r1p = r0p + 8 * F::ROWB;
                                 const float d0 = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(r0p));
@@ -809,10 +907,19 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                                 }
                             }
                         };
-                        if (qs_aligned)
-                            tiles(std::integral_constant<bool, true>{});
-                        else
-                            tiles(std::integral_constant<bool, false>{});
+                        using Yes = std::true_type;
+                        using No = std::false_type;
+                        if (ntiles == T) {  // (a separate copy keeps the full group's schedule)
+                            if (qs_aligned)
+                                tiles(Yes{}, Yes{});
+                            else
+                                tiles(No{}, Yes{});
+                        } else {
+                            if (qs_aligned)
+                                tiles(Yes{}, No{});
+                            else
+                                tiles(No{}, No{});
+                        }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[s]);
@@ -952,8 +1059,13 @@ template <int WT, bool MOE, int MODE, int T, int CW = 16>
 cudaError_t launch_inst(const StreamArgs &a, long long matrices, int grid, const DeviceInfo &dev,
                         cudaStream_t stream) {
     static std::atomic<unsigned long long> smem_set{0};
-    CUtensorMap map_t;
-    if (!make_map(map_t, a, WT, matrices, T * 16, Fmt<WT, CW>::ROWB)) return cudaErrorInvalidValue;
+    WMaps maps;
+    constexpr int rb = Fmt<WT, CW>::ROWB;
+    if (!make_map(maps.full, a, WT, matrices, T * 16, rb) ||
+        !make_map(maps.b4, a, WT, matrices, (T > 4 ? 4 : T) * 16, rb) ||
+        !make_map(maps.b2, a, WT, matrices, (T > 2 ? 2 : T) * 16, rb) ||
+        !make_map(maps.b1, a, WT, matrices, 16, rb))
+        return cudaErrorInvalidValue;
     auto kern = gemv_mma_kernel<WT, MOE, MODE, T, CW>;
     constexpr size_t bytes = smem_bytes<WT, MODE, T, CW>();
     static_assert(Warps<CW>::kCtas * (bytes + 1024) <= 228 * 1024, "CTAs per SM");
@@ -970,7 +1082,7 @@ cudaError_t launch_inst(const StreamArgs &a, long long matrices, int grid, const
             carve_set.fetch_or(bit, std::memory_order_acq_rel);
         }
     }
-    return launch_pdl(kern, dim3(grid), dim3(Warps<CW>::kThreads), bytes, stream, map_t, a);
+    return launch_pdl(kern, dim3(grid), dim3(Warps<CW>::kThreads), bytes, stream, maps, a);
 }
 
 template <int WT, int MODE>
