@@ -389,6 +389,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     // the producer's count of stages issued, kept here between routing windows so
     // that it occupies no register of the consumer warps
     long long *s_q = reinterpret_cast<long long *>(((uintptr_t)(s_nact + 2) + 7) & ~(uintptr_t)7);
+    int *s_wcnt = reinterpret_cast<int *>(s_q + 1);  // per-warp counts of the routing scan [32]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -489,36 +490,39 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
             const unsigned long long kr = s_key[i];
             return (kr >> 62) ? -1 : (int)(kr >> 16);
         };
-        if (warp == 0) {  // segment starts of the sorted slots, by ballot and prefix count
-            int na = 0;
-            for (int b0 = 0; b0 < Sl; b0 += 32) {
-                const int r = b0 + lane;
-                bool valid = false, start = false;
-                int e = 0;
-                if (r < Sl) {
-                    e = sorted_expert(r);
-                    valid = e >= 0;
-                    start = valid && (r == 0 || sorted_expert(r - 1) != e);
-                }
-                const unsigned sm = __ballot_sync(0xFFFFFFFFu, start);
-                if (start) {
-                    const int idx = na + __popc(sm & ((1u << lane) - 1u));
-                    s_seg[idx] = r;
-                    s_act[idx] = e;
-                }
-                na += __popc(sm);
-                const unsigned vm = __ballot_sync(0xFFFFFFFFu, valid);
-                if (vm != 0xFFFFFFFFu) {  // the first invalid slot ends the valid ones
-                    if (lane == 0) {
-                        s_seg[na] = b0 + __popc(vm);
-                        *s_nact = na;
-                    }
-                    break;
-                }
-                if (b0 + 32 >= Sl && lane == 0) {
-                    s_seg[na] = Sl;
-                    *s_nact = na;
-                }
+        // Segments of the sorted slots, one thread per position (blockDim >= 256):
+        // position r starts one when its expert differs from r - 1's, and the starts
+        // are numbered by a count over the warps' ballots.
+        {
+            const int r = threadIdx.x;
+            int e = -1;
+            bool start = false, last = false;
+            if (r < Sl) {
+                e = sorted_expert(r);
+                start = e >= 0 && (r == 0 || sorted_expert(r - 1) != e);
+                last = e >= 0 && (r == Sl - 1 || sorted_expert(r + 1) < 0);
+            }
+            const unsigned bm = __ballot_sync(0xFFFFFFFFu, start);
+            if (lane == 0) s_wcnt[warp] = __popc(bm);
+            __syncthreads();
+            int before = 0, total = 0;
+            for (int w = 0; w < (Sl + 31) / 32; ++w) {
+                const int c = s_wcnt[w];
+                before += w < warp ? c : 0;
+                total += c;
+            }
+            if (start) {
+                const int idx = before + __popc(bm & ((1u << lane) - 1u));
+                s_seg[idx] = r;
+                s_act[idx] = e;
+            }
+            if (last) {  // the valid slots end here (bad ids sort last)
+                s_seg[total] = r + 1;
+                *s_nact = total;
+            }
+            if (r == 0 && e < 0) {  // no valid slot in the window
+                s_seg[0] = 0;
+                *s_nact = 0;
             }
         }
     }
@@ -1033,7 +1037,7 @@ constexpr size_t smem_bytes() {
     using L = Layout<WT, MODE, T, CW>;
     return (size_t)L::kStages * L::kStageBytes + L::kRedBytes + L::kEpiBytes + L::kCoopBytes +
            2 * L::kStages * sizeof(uint64_t) +
-           kMaxSlots * sizeof(unsigned long long) + (3 * kMaxSlots + 4) * sizeof(int) + 32;
+           kMaxSlots * sizeof(unsigned long long) + (3 * kMaxSlots + 4 + 32) * sizeof(int) + 32;
 }
 
 // The weight image as a 3-D tensor [matrices][m][row bytes] (one matrix for a GEMV,
