@@ -279,14 +279,13 @@ __global__ void __launch_bounds__(256) gemm_splitk_kernel(const GemmArgs a, int 
     cluster.sync();  // every rank keeps its shared memory until all slices are read
 }
 
-// Small grids with moderate k: 32 x 8 outputs per CTA (one lane per X row, all
-// eight W rows per thread), the whole k loop in one CTA -- no cluster, no
-// cross-CTA reduction, so a call costs little more than its launch.  X and W are
-// staged in chunks of RK values of k (W decoded exactly into f32), all of a
-// chunk's loads in flight at once.  Warp w takes the w-th eighth of every chunk
-// for all eight W rows, so each X value is read from shared memory once and each
-// W value is a broadcast (shared-memory bandwidth bounds this loop); the eight
-// warps' partial sums are then added in warp order (deterministic).
+// Small grids with moderate k: one warp per W row and one lane per X row (32 x 8
+// outputs per CTA), the whole k loop in one CTA -- no cluster, no cross-CTA
+// reduction, so a call costs little more than its launch and two passes over
+// shared memory.  X and W are staged in chunks of RK values of k (W decoded
+// exactly into f32), all of a chunk's loads in flight at once; each lane sums each
+// chunk in four interleaved chains that are then added in a fixed order
+// (deterministic).
 constexpr int RK = 256;
 
 template <int WT, bool DUAL>
@@ -303,7 +302,7 @@ __global__ void __launch_bounds__(256) gemm_rows_kernel(const GemmArgs a) {
     const size_t o = (size_t)i * a.ldy + j;
     const float bj = (out && (a.flags & kBias)) ? __ldg(a.bias + j) : 0.f;
     const float rij = (out && (a.flags & kResidual)) ? a.R[o] : 0.f;  // may alias Y: plain load
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // W rows j0 .. j0 + 7
+    float acc = 0.f;
     for (int k0 = 0; k0 < a.k; k0 += RK) {
         {   // X: row r, float4s q, q + 8, q + 16, q + 24 of the chunk (k % 4 == 0)
             const int r = tid >> 3, q = tid & 7, i = i0 + r;
@@ -324,31 +323,22 @@ __global__ void __launch_bounds__(256) gemm_rows_kernel(const GemmArgs a) {
             *reinterpret_cast<float4 *>(&ws[r][8 * g + 4]) = make_float4(w[4], w[5], w[6], w[7]);
         }
         __syncthreads();
-#pragma unroll
-        for (int t = warp * (RK / 8); t < (warp + 1) * (RK / 8); t += 4) {
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll 16
+        for (int t = 0; t < RK; t += 4) {
             const float4 xv = *reinterpret_cast<const float4 *>(&xs[lane][t]);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 wv = *reinterpret_cast<const float4 *>(&ws[c][t]);
-                acc[c] = fmaf(xv.x, wv.x, acc[c]);
-                acc[c] = fmaf(xv.y, wv.y, acc[c]);
-                acc[c] = fmaf(xv.z, wv.z, acc[c]);
-                acc[c] = fmaf(xv.w, wv.w, acc[c]);
-            }
+            const float4 wv = *reinterpret_cast<const float4 *>(&ws[warp][t]);
+            c0 = fmaf(xv.x, wv.x, c0);
+            c1 = fmaf(xv.y, wv.y, c1);
+            c2 = fmaf(xv.z, wv.z, c2);
+            c3 = fmaf(xv.w, wv.w, c3);
         }
+        acc += (c0 + c1) + (c2 + c3);
         __syncthreads();
     }
-    // The warps' partial sums, [warp][W row][X row], reuse the X staging buffer.
-    float *red = &xs[0][0];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) red[(warp * 8 + c) * 32 + lane] = acc[c];
-    __syncthreads();
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) v += red[(w * 8 + warp) * 32 + lane];  // this thread: W row j0 + warp
     if (out) {
-        a.Y[o] = epilogue_vals(v, a.flags, bj, rij, a.alpha);
-        if (DUAL && j < a.dual) a.Y[o + a.m] = v + a.bias2[j];  // the raw second band
+        a.Y[o] = epilogue_vals(acc, a.flags, bj, rij, a.alpha);
+        if (DUAL && j < a.dual) a.Y[o + a.m] = acc + a.bias2[j];  // the raw second band
     }
 }
 

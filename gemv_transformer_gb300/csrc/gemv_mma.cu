@@ -72,22 +72,18 @@ constexpr int kMaxSlots = 256;
 
 // A stage holds, for every row of the group, the NB blocks of one chunk, loaded as
 // NBOX tall TMA boxes (the box inner size is at most 256 u16, so Q8_0's 544-byte
-// row of a 16-block chunk takes two boxes of 8 blocks).  A 16-block Q4_0 chunk is
-// also loaded as two boxes of 8 blocks when the group has four tiles or more: rows
-// 288 bytes apart put the fragment loads of rows g and g + 4 in the same shared-
-// memory banks, rows 144 bytes apart do not (measured: 45 % of the load wavefronts
-// were conflicts); with fewer tiles the smaller boxes cost more than they save.
-template <int WT, int NB, int T>
+// row of a 16-block chunk takes two boxes of 8 blocks).
+template <int WT, int NB>
 struct Fmt;
-template <int NB, int T>
-struct Fmt<kQ4_0, NB, T> {
-    static constexpr int BB = 18;                          // block bytes
-    static constexpr int BOXB = (NB == 16 && T >= 4) ? 8 : NB;  // blocks per box row
-    static constexpr int NBOX = NB / BOXB;
-    static constexpr int ROWB = 18 * BOXB;                 // bytes per box row
+template <int NB>
+struct Fmt<kQ4_0, NB> {
+    static constexpr int BB = 18;        // block bytes
+    static constexpr int BOXB = NB;      // blocks per box row
+    static constexpr int NBOX = 1;
+    static constexpr int ROWB = 18 * NB; // bytes per box row
 };
-template <int NB, int T>
-struct Fmt<kQ8_0, NB, T> {
+template <int NB>
+struct Fmt<kQ8_0, NB> {
     static constexpr int BB = 34;
     static constexpr int BOXB = 8;
     static constexpr int NBOX = NB / 8;
@@ -113,7 +109,7 @@ struct Mode {
 
 template <int WT, int MODE, int T, int CW>
 struct Layout {
-    using F = Fmt<WT, CW, T>;
+    using F = Fmt<WT, CW>;
     static constexpr int kBudgetAll = Warps<CW>::kSmemBudget;
     static constexpr int kTileBytes = 16 * F::ROWB;             // one tile, one box
     static constexpr int kBoxBytes = T * kTileBytes;            // the group's rows, one box
@@ -1068,7 +1064,7 @@ cudaError_t launch_inst(const StreamArgs &a, long long matrices, int grid, const
                         cudaStream_t stream) {
     static std::atomic<unsigned long long> smem_set{0};
     WMaps maps;
-    constexpr int rb = Fmt<WT, CW, T>::ROWB;
+    constexpr int rb = Fmt<WT, CW>::ROWB;
     if (!make_map(maps.full, a, WT, matrices, T * 16, rb) ||
         !make_map(maps.b4, a, WT, matrices, (T > 4 ? 4 : T) * 16, rb) ||
         !make_map(maps.b2, a, WT, matrices, (T > 2 ? 2 : T) * 16, rb) ||
