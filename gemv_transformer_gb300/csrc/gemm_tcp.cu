@@ -88,10 +88,12 @@ struct PLayout {
 };
 
 // Helper mode: the owners' share of a tile's KB stages.  The helper's share is
-// three quarters of an even split (KB / (h + 1) per tile), since each hand-over
-// (a 64 KB store while its next segment streams in) costs it about two stages.
+// seven eighths of an even split (KB / (h + 1) per tile), since each hand-over
+// (a 64 KB store while its next segment streams in) costs it some time (for the
+// encoder down projection, KB = 32, h = 3: owners 25 stages; 24 or 26 made the
+// whole benchmark step 0.7-0.8 us slower in an A/B on GB300).
 __host__ __device__ constexpr int help_split(int KB, int h) {
-    return KB - ((3 * KB) / (4 * (h + 1)) > 1 ? (3 * KB) / (4 * (h + 1)) : 1);
+    return KB - ((7 * KB) / (8 * (h + 1)) > 1 ? (7 * KB) / (8 * (h + 1)) : 1);
 }
 
 // DUAL: the epilogue also writes the second output band (columns m.. of Y); a
