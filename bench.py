@@ -90,7 +90,8 @@ def extra_workloads():
     large-n tensor-core GEMM (a prompt through GGML weights), the LayerNorm fused
     before the encoder qkv projection, the token-embedding gather, a q projection
     without and with a second output band (dual outputs), and one-token GEMVs
-    through bf16 / F16 / F32 weights (the weight-streaming kernel)."""
+    through bf16 weights (the bf16 tensor-core GEMV) and F16 / F32 weights (the
+    weight-streaming kernel)."""
     import synth
     return [synth.workload_quant_prefill(wtype=synth.WTYPE_Q4_0),
             synth.workload_quant_prefill(wtype=synth.WTYPE_Q8_0),

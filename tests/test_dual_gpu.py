@@ -86,6 +86,7 @@ def windows_of(m, dual, w=96):
 ROUTES = [  # ((n, m, k, wtype), flags, workspace, tau, dual)
     ((3, 640, 1024, wq.WQ_Q4_0), BIAS | GELU | RES, False, 1e-5, 100),    # GEMV, mma
     ((5, 300, 520, wq.WQ_BF16), BIAS | RES, False, 1e-5, 37),              # GEMV, stream kernel
+    ((5, 300, 512, wq.WQ_BF16), BIAS | GELU | RES, False, 1e-5, 37),       # GEMV, bf16 mma
     ((9, 200, 96, wq.WQ_F16), BIAS | wq.WQ_SILU, False, 1e-5, 200),        # GEMV, dual = m
     ((48, 200, 256, wq.WQ_Q8_0), BIAS | GELU | RES, False, 1e-5, 77),      # f32-FMA split-k
     ((700, 900, 64, wq.WQ_Q8_0), BIAS | RES, False, 1e-5, 130),            # f32-FMA tiles

@@ -375,7 +375,8 @@ def test_bit_identical_reruns(wtype):
 # ------------------------------------------------------- bounded waits --
 
 @pytest.mark.parametrize("wtype,n,m,k", [(Q4_0, 4, 14336, 8192),   # tensor-core GEMV
-                                         (BF16, 1, 4096, 16384)])   # streaming GEMV
+                                         (BF16, 1, 4096, 16384),    # bf16 tensor-core GEMV
+                                         (BF16, 1, 4096, 16392)])   # streaming GEMV
 def test_wait_limit_expires_without_hang(oracle_mod, wtype, n, m, k):
     """A one-poll wait limit makes the stage waits give up as soon as a stage is not
     yet filled: the kernel records WQ_ERR_DEVICE_TIMEOUT, drains its copies and
