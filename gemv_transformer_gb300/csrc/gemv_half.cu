@@ -1,22 +1,25 @@
-// gemv_bf16.cu -- small-n GEMV with bf16-pair weights on the tensor cores.
+// gemv_half.cu -- small-n GEMV with bf16-pair or F16 weights on the tensor cores.
 //
-// Computes the same contraction as gemv_stream.cu for bf16 weights (cortiq-engine
-// 0.8.49 AudioEncoder::gemm / ae_gemm: W as bf16 pairs, Y (=|+=) X.W^T with the
-// ae_put epilogue; wavo Pass::gemv for the small-n call), for 1 <= n <= 16 and
-// k % 256 == 0.
+// Computes the same contraction as gemv_stream.cu for 16-bit float weights
+// (cortiq-engine 0.8.49 AudioEncoder::gemm / ae_gemm: W as bf16 pairs, Y (=|+=)
+// X.W^T with the ae_put epilogue; wavo's F16 weights and Pass::gemv for the small-n
+// call), for 1 <= n <= 16 and k % 256 == 0.
 //
-// A bf16 weight is exact as an operand of mma.sync.m16n8k16 (bf16 x bf16 -> f32),
-// so the weights are not decoded at all: a producer warp streams 16-row tiles by
-// TMA into shared memory in the 128-byte-swizzled layout, and ldmatrix hands each
-// warp its A fragments directly.  X is split into three bf16 terms, x ~ t1 + t2 +
-// t3 with |x - t1 - t2 - t3| <= 2^-24 |x| (each term holds the next 8 bits of the
-// significand), after scaling each token's 64-element slice of a chunk by a power
-// of two that keeps the third term a normal number; every product of a weight and
-// a term is exact in f32, and the three terms of a token occupy three n-tiles
-// whose MMAs accumulate into one partial sum.  The slice's partial sums are then
-// multiplied by the inverse power of two into the f32 accumulator (one rounding
-// per 64 elements of k), so the result is within 2^-22 sum|x||w| plus f32
-// rounding of the sums -- inside the 1e-5 sum|x||w| contract.
+// A bf16 or f16 weight is exact as an operand of mma.sync.m16n8k16 (bf16 x bf16 or
+// f16 x f16 -> f32), so the weights are not decoded at all: a producer warp streams
+// 16-row tiles by TMA into shared memory in the 128-byte-swizzled layout, and
+// ldmatrix hands each warp its A fragments directly.  X is split into terms of the
+// weights' type after scaling each token's 64-element slice of a chunk by a power
+// of two: bf16, three terms, x ~ t1 + t2 + t3 with |x - t1 - t2 - t3| <= 2^-24 |x|
+// (each term the next 8 bits of the significand; the scale keeps the third term a
+// normal number); f16, two terms with the slice's largest |x| scaled into [2^14,
+// 2^15), |x - t1 - t2| <= 2^-22 |x| (below 2^-17 of that largest |x| an absolute
+// 2^-39 of it, f16's subnormal floor).  Every product of a weight and a term is
+// exact in f32, and the terms of a token occupy separate n-tiles whose MMAs add
+// into one partial sum per slice; the slice's partial sums are multiplied by the
+// inverse power of two into the f32 accumulator (one rounding per 64 elements of
+// k), so the result is within 2^-22 sum|x||w| plus f32 rounding of the sums --
+// inside the 1e-5 sum|x||w| contract.
 //
 // Work: every CTA takes groups of T 16-row tiles; the producer warp loads a chunk
 // of 256 k for the whole group per stage (four 64-element TMA boxes of T*16 rows,
@@ -49,10 +52,19 @@ constexpr int kParts = kChunk / kBoxK;   // 64-element slices per chunk
 constexpr int kKSteps = kChunk / 16;     // MMA k-steps per chunk
 constexpr int kBudget = 200 * 1024;      // stages + B fragments
 
+// The X terms of each weight type: bf16 three (scaled to 2^62), f16 two (scaled to
+// 2^14, below f16's largest finite value).
+template <int WT>
+struct Terms {
+    static constexpr int kN = WT == kBF16 ? 3 : 2;
+    static constexpr int kTarget = WT == kBF16 ? 62 : 14;  // log2 of the scaled largest |x|
+};
+
 // T tiles per group; KS slices of each chunk's k (a warp per tile and slice); NH
 // halves of eight tokens (n <= 8 NH).
-template <int T, int KS, int NH>
+template <int WT, int T, int KS, int NH>
 struct BL {
+    static constexpr int TN = Terms<WT>::kN;
     static constexpr int kCW = T * KS;                    // consumer warps
     static constexpr int kPP = kParts / KS;               // 64-element slices per warp
     static constexpr int kThreads = (kCW + 1) * 32;
@@ -62,7 +74,7 @@ struct BL {
     static constexpr int kStageBytes = kWBytes + kXBytes;
     // B fragments of one chunk, u32 [k-step][term][half][lane][2], and the slices'
     // inverse scales, f32 [part][token]
-    static constexpr int kFragWords = kKSteps * 3 * NH * 32 * 2;
+    static constexpr int kFragWords = kKSteps * TN * NH * 32 * 2;
     static constexpr int kInvWords = kParts * 16;
     static constexpr int kBufWords = kFragWords + kInvWords;
     // the tiles' partial sums per slice, f32 [KS][T][lane][NH * 4]
@@ -83,20 +95,50 @@ __device__ __forceinline__ uint16_t bf16_rn(float v) {
 
 __device__ __forceinline__ float bf16_val(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
+__device__ __forceinline__ uint16_t f16_rn(float v) {
+    unsigned short h;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(v));
+    return h;
+}
+
+__device__ __forceinline__ float f16_val(uint16_t h) {
+    float v;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(v) : "h"(h));
+    return v;
+}
+
+// A term of the weights' type, rounded to nearest even, and its value.
+template <int WT>
+__device__ __forceinline__ uint16_t term_rn(float v) {
+    return WT == kBF16 ? bf16_rn(v) : f16_rn(v);
+}
+template <int WT>
+__device__ __forceinline__ float term_val(uint16_t h) {
+    return WT == kBF16 ? bf16_val(h) : f16_val(h);
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
 
-// d += A.B (bf16 operands, f32 accumulation).
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// d += A.B (bf16 or f16 operands, f32 accumulation).
+template <int WT>
+__device__ __forceinline__ void mma_16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                       uint32_t b1) {
+    if (WT == kBF16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -123,15 +165,16 @@ __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
 }
 
-template <int T, int KS, int NH>
-__global__ void __launch_bounds__(BL<T, KS, NH>::kThreads, 1)
-    gemv_bf16_kernel(const __grid_constant__ CUtensorMap wmap, const StreamArgs a) {
+template <int WT, int T, int KS, int NH>
+__global__ void __launch_bounds__(BL<WT, T, KS, NH>::kThreads, 1)
+    gemv_half_kernel(const __grid_constant__ CUtensorMap wmap, const StreamArgs a) {
     // Barriers and the descriptor are set up before waiting for the previous grid
     // (they touch nothing it writes); global memory after.
     pdl_launch();
-    using L = BL<T, KS, NH>;
+    using L = BL<WT, T, KS, NH>;
     constexpr int S = L::kStages;
     constexpr int CW = L::kCW;
+    constexpr int TN = L::TN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *stages = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // swizzle atoms: 1 KB
@@ -233,7 +276,7 @@ __global__ void __launch_bounds__(BL<T, KS, NH>::kThreads, 1)
             float *invb = reinterpret_cast<float *>(fb + L::kFragWords);
             if (w) {
                 // B: one warp per (token, 64-element slice): scale by a power of two,
-                // split into three bf16 terms, store each where its fragment wants it.
+                // split into TN terms, store each where its fragment wants it.
                 const float *xs = reinterpret_cast<const float *>(st + L::kWBytes);
                 uint16_t *f16 = reinterpret_cast<uint16_t *>(fb);
                 for (int it = warp; it < n * kParts; it += CW) {
@@ -243,30 +286,30 @@ __global__ void __launch_bounds__(BL<T, KS, NH>::kThreads, 1)
                     const uint32_t mb = __reduce_max_sync(
                         0xFFFFFFFFu, max(__float_as_uint(x0) & 0x7FFFFFFFu,
                                          __float_as_uint(x1) & 0x7FFFFFFFu));
-                    // sc = 2^(sb - 127) with the slice's largest |x| * sc in [2^62, 2^63)
-                    // (E is that |x|'s biased exponent); sb kept in [1, 253] so that sc
-                    // and 1/sc are normal.
+                    // sc = 2^(sb - 127) with the slice's largest |x| * sc in [2^target,
+                    // 2^(target + 1)) (E is that |x|'s biased exponent); sb kept in [1,
+                    // 253] so that sc and 1/sc are normal.
                     const int E = (int)((mb >> 23) & 0xFFu);
-                    const int sb = min(253, max(1, 316 - E));
+                    const int sb = min(253, max(1, 254 + Terms<WT>::kTarget - E));
                     const float sc = __uint_as_float((uint32_t)sb << 23);
                     if (lane == 0) invb[p * 16 + tok] = __uint_as_float((uint32_t)(254 - sb) << 23);
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const float xv = (e ? x1 : x0) * sc;
-                        const uint16_t h1 = bf16_rn(xv);
-                        const float r1 = xv - bf16_val(h1);
-                        const uint16_t h2 = bf16_rn(r1);
-                        const uint16_t h3 = bf16_rn(r1 - bf16_val(h2));
+                        const uint16_t h1 = term_rn<WT>(xv);
+                        const float r1 = xv - term_val<WT>(h1);
+                        const uint16_t h2 = term_rn<WT>(r1);
                         // element kc of the chunk -> k-step kk, register reg of thread
                         // (g = token % 8, tt), low or high half
                         const int kc = p * kBoxK + e * 32 + lane;
                         const int kk = kc >> 4, r = kc & 15;
                         const int reg = r >> 3, tt = (r & 7) >> 1, half = r & 1;
                         const int ln = (tok & 7) * 4 + tt;
-                        const int i0 = (((kk * 3 * NH + (tok >> 3)) * 32 + ln) * 2 + reg) * 2 + half;
+                        const int i0 = (((kk * TN * NH + (tok >> 3)) * 32 + ln) * 2 + reg) * 2 + half;
                         f16[i0] = h1;                   // term 0
                         f16[i0 + NH * 128] = h2;        // term 1: + NH * 32 lanes * 2 regs * 2
-                        f16[i0 + 2 * NH * 128] = h3;    // term 2
+                        if (TN == 3)                    // term 2
+                            f16[i0 + 2 * NH * 128] = term_rn<WT>(r1 - term_val<WT>(h2));
                     }
                 }
             }
@@ -276,11 +319,11 @@ __global__ void __launch_bounds__(BL<T, KS, NH>::kThreads, 1)
             // partial sum per slice (per term, added after the slice's MMAs).
 #pragma unroll 1
             for (int p = sw * L::kPP; p < (sw + 1) * L::kPP; ++p) {
-                float part[NH][3][4];
+                float part[NH][TN][4];
 #pragma unroll
                 for (int h = 0; h < NH; ++h)
 #pragma unroll
-                    for (int term = 0; term < 3; ++term)
+                    for (int term = 0; term < TN; ++term)
 #pragma unroll
                         for (int r = 0; r < 4; ++r) part[h][term][r] = 0.f;
                 const uint8_t *box = st + p * L::kBoxBytes;
@@ -298,10 +341,10 @@ __global__ void __launch_bounds__(BL<T, KS, NH>::kThreads, 1)
 #pragma unroll
                     for (int h = 0; h < NH; ++h)
 #pragma unroll
-                        for (int term = 0; term < 3; ++term) {
+                        for (int term = 0; term < TN; ++term) {
                             const uint2 b = *reinterpret_cast<const uint2 *>(
-                                fb + (((kk * 3 + term) * NH + h) * 32 + lane) * 2);
-                            mma_bf16(part[h][term], A, b.x, b.y);
+                                fb + (((kk * TN + term) * NH + h) * 32 + lane) * 2);
+                            mma_16<WT>(part[h][term], A, b.x, b.y);
                         }
                 }
 #pragma unroll
@@ -309,7 +352,9 @@ __global__ void __launch_bounds__(BL<T, KS, NH>::kThreads, 1)
                     const float2 iv = *reinterpret_cast<const float2 *>(invb + p * 16 + h * 8 + 2 * t);
                     float v[4];
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) v[r] = (part[h][0][r] + part[h][1][r]) + part[h][2][r];
+                    for (int r = 0; r < 4; ++r)
+                        v[r] = TN == 3 ? (part[h][0][r] + part[h][1][r]) + part[h][TN - 1][r]
+                                       : part[h][0][r] + part[h][1][r];
                     acc[h][0] = fmaf(iv.x, v[0], acc[h][0]);
                     acc[h][1] = fmaf(iv.y, v[1], acc[h][1]);
                     acc[h][2] = fmaf(iv.x, v[2], acc[h][2]);
@@ -379,24 +424,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int T, int KS, int NH>
+template <int WT, int T, int KS, int NH>
 cudaError_t launch_t(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
-    using L = BL<T, KS, NH>;
+    using L = BL<WT, T, KS, NH>;
     static std::atomic<unsigned long long> smem_set{0};
     auto encode = encode_fn();
     if (!encode) return cudaErrorInvalidValue;
-    // W as a 2-D bf16 tensor [m][k]; boxes of 64 elements x T*16 rows, 128-byte
-    // swizzle (rows past m read as zero).
+    // W as a 2-D tensor of 16-bit elements [m][k]; boxes of 64 elements x T*16 rows,
+    // 128-byte swizzle (rows past m read as zero).
     CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)a.k, (cuuint64_t)a.m};
     const cuuint64_t strides[1] = {(cuuint64_t)a.k * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kBoxK, (cuuint32_t)(T * 16)};
     const cuuint32_t estr[2] = {1, 1};
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t *>(a.W), dims,
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t *>(a.W), dims,
                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    auto kern = gemv_bf16_kernel<T, KS, NH>;
+    auto kern = gemv_half_kernel<WT, T, KS, NH>;
     static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
     cudaError_t err = ensure_smem(kern, (int)L::kBytes, dev, smem_set);
     if (err != cudaSuccess) return err;
@@ -407,23 +452,32 @@ cudaError_t launch_t(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t st
 
 }  // namespace
 
-bool bf16_gemv_supported(int wtype, int n, int k) {
-    return wtype == kBF16 && n >= 1 && n <= 16 && k % kChunk == 0 && encode_fn() != nullptr;
-}
-
-cudaError_t launch_bf16_gemv(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
+namespace {
+template <int WT>
+cudaError_t launch_wt(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
     // T tiles per group: about one group per SM (the groups of a CTA share nothing);
     // k slices so that 8-16 consumer warps hide the latencies of each warp's MMAs.
     const long long tiles = (a.m + 15) / 16;
     const long long per = (tiles + dev.sm_count - 1) / dev.sm_count;
     if (a.n > 8) {
-        if (per <= 2) return launch_t<2, 4, 2>(a, dev, stream);
-        return launch_t<4, 2, 2>(a, dev, stream);
+        if (per <= 2) return launch_t<WT, 2, 4, 2>(a, dev, stream);
+        return launch_t<WT, 4, 2, 2>(a, dev, stream);
     }
-    if (per <= 2) return launch_t<2, 4, 1>(a, dev, stream);
-    if (per <= 4) return launch_t<4, 4, 1>(a, dev, stream);
-    if (per <= 6) return launch_t<6, 2, 1>(a, dev, stream);
-    return launch_t<8, 2, 1>(a, dev, stream);
+    if (per <= 2) return launch_t<WT, 2, 4, 1>(a, dev, stream);
+    if (per <= 4) return launch_t<WT, 4, 4, 1>(a, dev, stream);
+    if (per <= 6) return launch_t<WT, 6, 2, 1>(a, dev, stream);
+    return launch_t<WT, 8, 2, 1>(a, dev, stream);
+}
+}  // namespace
+
+bool half_gemv_supported(int wtype, int n, int k) {
+    return (wtype == kBF16 || wtype == kF16) && n >= 1 && n <= 16 && k % kChunk == 0 &&
+           encode_fn() != nullptr;
+}
+
+cudaError_t launch_half_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,
+                             cudaStream_t stream) {
+    return wtype == kBF16 ? launch_wt<kBF16>(a, dev, stream) : launch_wt<kF16>(a, dev, stream);
 }
 
 }  // namespace wq

@@ -143,8 +143,8 @@ static wq_status gemv_impl(int n, int m, int k, int wtype, unsigned flags, const
     fill_args(a, n, m, k, flags, X, W, bias, residual, Y, *dev, ex);
     if (mma_gemv_supported(wtype, k))
         return cuda_status(launch_mma_gemv(a, wtype, *dev, (cudaStream_t)stream));
-    if (bf16_gemv_supported(wtype, n, k))
-        return cuda_status(launch_bf16_gemv(a, *dev, (cudaStream_t)stream));
+    if (half_gemv_supported(wtype, n, k))
+        return cuda_status(launch_half_gemv(a, wtype, *dev, (cudaStream_t)stream));
     return cuda_status(launch_stream_gemv(a, wtype, *dev, (cudaStream_t)stream));
 }
 

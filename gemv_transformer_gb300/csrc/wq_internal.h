@@ -99,9 +99,10 @@ cudaError_t launch_stream_gemv(const StreamArgs &a, int wtype, const DeviceInfo 
 cudaError_t launch_stream_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,
                               cudaStream_t stream);
 bool mma_gemv_supported(int wtype, int k);
-// bf16 weights, 1 <= n <= 16, k % 256 == 0: the tensor-core GEMV of gemv_bf16.cu.
-bool bf16_gemv_supported(int wtype, int n, int k);
-cudaError_t launch_bf16_gemv(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t stream);
+// bf16 or F16 weights, 1 <= n <= 16, k % 256 == 0: the tensor-core GEMV of gemv_half.cu.
+bool half_gemv_supported(int wtype, int n, int k);
+cudaError_t launch_half_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,
+                             cudaStream_t stream);
 cudaError_t launch_mma_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,
                             cudaStream_t stream);
 cudaError_t launch_mma_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,
