@@ -661,7 +661,8 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
             // One pass over the group's chunks; the column layout is a compile-time
             // choice so the tile loop carries no layout branches.
             auto pass = [&](auto pk, auto ck) {
-                // packed: 1-4 tokens, column g = term (g / P) of token (g % P), one n-tile;
+                // packed: 1-4 tokens, column g = term (g % 2) of token (g / 2), one n-tile
+                // (a thread's two accumulator columns are one token's two terms);
                 // else split-major: n-tile s, column g = token g (+8 for the second half).
                 constexpr bool packed = decltype(pk)::value;
                 // one- and two-token packed passes: each lane splits one element of its
@@ -673,11 +674,11 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                 int col_s = 0;  // packed: which split this thread's column carries
     #pragma unroll
                 for (int h = 0; h < NH; ++h) {
-                    const int i = packed ? g % P : h * 8 + g;
+                    const int i = packed ? g >> 1 : h * 8 + g;
                     tok_ok[h] = packed ? (g < 2 * P) : (i < ntok);
                     xslot[h] = tok_ok[h] ? i : 0;
                 }
-                if (packed) col_s = g / P;
+                if (packed) col_s = g & 1;
                 int coop_w = 0, coop_r = 256;  // u16 index of lane's write; byte offset of the read
                 if constexpr (COOP) {
                     const int j = lane;
@@ -686,7 +687,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                     const int pair = WT == kQ4_0 ? 2 * (j >> 4) + (w & 1) : 2 * (w >> 2) + (w & 1);
                     const int half = WT == kQ4_0 ? w >> 1 : (w >> 1) & 1;
                     coop_w = tt * 8 + pair * 2 + half;
-                    if (g < 2 * P) coop_r = (((g % P) * 2 + g / P) * 4 + t) * 16;
+                    if (g < 2 * P) coop_r = (g * 4 + t) * 16;  // [token][term][t] = [g][t]
                 }
 
                 // Stage this pass's bias and residual values in shared memory now, so the
@@ -775,8 +776,8 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                             bf[0][0][1] = bv.y;
                             bf[1][0][0] = bv.z;
                             bf[1][0][1] = bv.w;
-                            inv0[0] = invp[0];
-                            inv1[0] = invp[1];
+                            inv0[0] = t == 0 ? invp[0] : invp[1];  // the columns of token t
+                            inv1[0] = inv0[0];
                         } else {
                             uint32_t sp[NH][4][2];
                             float inv_own[NH];
@@ -815,7 +816,8 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     #pragma unroll
                             for (int h = 0; h < NH; ++h) {
                                 inv0[h] = __shfl_sync(0xFFFFFFFFu, inv_own[h], 8 * t);
-                                inv1[h] = __shfl_sync(0xFFFFFFFFu, inv_own[h], 8 * t + 4);
+                                inv1[h] = packed ? inv0[h]  // packed: both columns are token t's
+                                                 : __shfl_sync(0xFFFFFFFFu, inv_own[h], 8 * t + 4);
                             }
                             // B fragments [k-step][n-tile][reg]: k-step 0 uses pairs 0,1; k-step 1 pairs 2,3.
     #pragma unroll
@@ -887,10 +889,13 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                                     decode_q8(v11, a2[1], a2[3]);
                                 }
                                 if (packed) {
+                                    // columns 2t, 2t + 1: token t's two terms, one scale;
+                                    // accumulators [0] and [1] hold rows g and g + 8
                                     float part[4];
                                     mma_f16_z(part, a1, bf[0][0][0], bf[0][0][1]);
                                     mma_f16(part, a2, bf[1][0][0], bf[1][0][1]);
-                                    scale_acc(acc[tt][0], part, d0, d1, inv0[0], inv1[0]);
+                                    acc[tt][0][0] = fmaf(d0 * inv0[0], part[0] + part[1], acc[tt][0][0]);
+                                    acc[tt][0][1] = fmaf(d1 * inv0[0], part[2] + part[3], acc[tt][0][1]);
                                 } else {
                                     // The two terms of a token sit in the same thread and column
                                     // of two n-tiles: one accumulator chain sums them.
@@ -940,14 +945,22 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     #pragma unroll
                     for (int tt = 0; tt < T; ++tt) {
                         if (tt < ntiles) {
+                            if (packed) {  // token t of rows g, g + 8 in column t
     #pragma unroll
-                            for (int j = 0; j < NA; ++j) {
+                                for (int r = 0; r < 2; ++r) {
+                                    float *dst = &buf[(tt * 16 + g + 8 * r) * C + t];
+                                    *dst = (rnd == 0) ? acc[tt][0][r] : *dst + acc[tt][0][r];
+                                }
+                            } else {
     #pragma unroll
-                                for (int r = 0; r < 4; ++r) {
-                                    const int row = tt * 16 + g + (r >= 2 ? 8 : 0);
-                                    const int col = j * 8 + 2 * t + (r & 1);
-                                    float *dst = &buf[row * C + col];
-                                    *dst = (rnd == 0) ? acc[tt][j][r] : *dst + acc[tt][j][r];
+                                for (int j = 0; j < NA; ++j) {
+    #pragma unroll
+                                    for (int r = 0; r < 4; ++r) {
+                                        const int row = tt * 16 + g + (r >= 2 ? 8 : 0);
+                                        const int col = j * 8 + 2 * t + (r & 1);
+                                        float *dst = &buf[row * C + col];
+                                        *dst = (rnd == 0) ? acc[tt][j][r] : *dst + acc[tt][j][r];
+                                    }
                                 }
                             }
                         }
@@ -973,7 +986,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     #pragma unroll
                         for (int b = 0; b < NB; ++b) {
                             const float *rp = red + b * RT + r * C;
-                            v += packed ? rp[i] + rp[P + i] : rp[i];
+                            v += rp[i];  // packed: the token's two terms already summed
                         }
                         const int yrow = MOE ? s_sorted[seg0 + p0 + i] : p0 + i;
                         // MoE has no second band: its rows are m wide.
