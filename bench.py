@@ -90,8 +90,9 @@ def extra_workloads():
     large-n tensor-core GEMM (a prompt through GGML weights), the LayerNorm fused
     before the encoder qkv projection, the token-embedding gather, a q projection
     without and with a second output band (dual outputs), and one-token GEMVs
-    through bf16 weights (the bf16 tensor-core GEMV) and F16 / F32 weights (the
-    weight-streaming kernel)."""
+    through bf16 and F16 weights (the half-precision tensor-core GEMV) and F32
+    weights (the weight-streaming kernel), and the routed MoE through a bf16 bank
+    (the half-precision tensor-core MoE)."""
     import synth
     return [synth.workload_quant_prefill(wtype=synth.WTYPE_Q4_0),
             synth.workload_quant_prefill(wtype=synth.WTYPE_Q8_0),
@@ -102,7 +103,8 @@ def extra_workloads():
             synth.workload_dual_q(dual=True),
             synth.workload_float_gemv(wtype=synth.WTYPE_BF16),
             synth.workload_float_gemv(wtype=synth.WTYPE_F16),
-            synth.workload_float_gemv(wtype=synth.WTYPE_F32)]
+            synth.workload_float_gemv(wtype=synth.WTYPE_F32),
+            synth.workload_moe(wtype=synth.WTYPE_BF16)]
 
 
 def algorithmic(w):
@@ -140,23 +142,31 @@ def kernels_per_call(w):
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of `python bench.py --case NAME`, keyed by workload, with the SHA-256 of
-# the kernel source it was taken on; reported only while that source is unchanged.
+# the kernel's sources (concatenated in the order listed) it was taken on; reported
+# only while those sources are unchanged.
 TRAFFIC = {
     # one ncu capture: 86,189,312 B read + 2,276,096 B written per launch
     "moe_q4_0_E64_m1408_k2048_t16x6": {
-        "bytes": 88465408, "source": "gemv_transformer_gb300/csrc/gemv_mma.cu",
+        "bytes": 88465408,
+        "sources": ["gemv_transformer_gb300/csrc/gemv_mma.cu",
+                    "gemv_transformer_gb300/csrc/tile_sched.cuh"],
         "sha256": "8e0f508c202c913096da636d22b6caeb75036d3ad96079043545b1c4b898c82d"},
 }
 
 
-def traffic_for(name):
+def sources_sha256(sources):
     import hashlib
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_for(name):
     rec = TRAFFIC.get(name)
-    if not rec:
+    if not rec or sources_sha256(rec["sources"]) != rec["sha256"]:
         return None
-    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
-            return None
     return rec["bytes"]
 
 

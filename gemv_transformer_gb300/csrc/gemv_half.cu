@@ -42,6 +42,7 @@
 
 #include "wq_device.cuh"
 #include "wq_internal.h"
+#include "tile_sched.cuh"
 
 namespace wq {
 namespace {
@@ -150,19 +151,106 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// Global -> shared bulk copy completing on `bar`, default L2 policy (X is read by
-// every CTA).
-__device__ __forceinline__ void bulk_g2s_x(void *dst, const void *src, uint32_t bytes,
-                                           uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
+
+// The B fragments of one chunk for tokens [0, nt): one warp per (token, 64-element
+// slice) scales by a power of two, splits into TN terms and stores each term where
+// its fragment wants it; lane 0 keeps the slice's inverse scale.
+template <class L, int WT, int NH, int CW>
+__device__ __forceinline__ void build_b(const uint8_t *st, uint32_t *fb, float *invb, int nt,
+                                        int warp, int lane) {
+    constexpr int TN = L::TN;
+    // B: one warp per (token, 64-element slice): scale by a power of two,
+    // split into TN terms, store each where its fragment wants it.
+    const float *xs = reinterpret_cast<const float *>(st + L::kWBytes);
+    uint16_t *f16 = reinterpret_cast<uint16_t *>(fb);
+    for (int it = warp; it < nt * kParts; it += CW) {
+        const int tok = it / kParts, p = it % kParts;
+        const float x0 = xs[tok * kChunk + p * kBoxK + lane];
+        const float x1 = xs[tok * kChunk + p * kBoxK + 32 + lane];
+        const uint32_t mb = __reduce_max_sync(
+            0xFFFFFFFFu, max(__float_as_uint(x0) & 0x7FFFFFFFu,
+                             __float_as_uint(x1) & 0x7FFFFFFFu));
+        // sc = 2^(sb - 127) with the slice's largest |x| * sc in [2^target,
+        // 2^(target + 1)) (E is that |x|'s biased exponent); sb kept in [1,
+        // 253] so that sc and 1/sc are normal.
+        const int E = (int)((mb >> 23) & 0xFFu);
+        const int sb = min(253, max(1, 254 + Terms<WT>::kTarget - E));
+        const float sc = __uint_as_float((uint32_t)sb << 23);
+        if (lane == 0) invb[p * 16 + tok] = __uint_as_float((uint32_t)(254 - sb) << 23);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float xv = (e ? x1 : x0) * sc;
+            const uint16_t h1 = term_rn<WT>(xv);
+            const float r1 = xv - term_val<WT>(h1);
+            const uint16_t h2 = term_rn<WT>(r1);
+            // element kc of the chunk -> k-step kk, register reg of thread
+            // (g = token % 8, tt), low or high half
+            const int kc = p * kBoxK + e * 32 + lane;
+            const int kk = kc >> 4, r = kc & 15;
+            const int reg = r >> 3, tt = (r & 7) >> 1, half = r & 1;
+            const int ln = (tok & 7) * 4 + tt;
+            const int i0 = (((kk * TN * NH + (tok >> 3)) * 32 + ln) * 2 + reg) * 2 + half;
+            f16[i0] = h1;                   // term 0
+            f16[i0 + NH * 128] = h2;        // term 1: + NH * 32 lanes * 2 regs * 2
+            if (TN == 3)                    // term 2
+                f16[i0 + 2 * NH * 128] = term_rn<WT>(r1 - term_val<WT>(h2));
+        }
+    }
 }
 
-template <int CW>
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
+// This warp's 64-element slices of one chunk for the 16 rows of its tile, added
+// into acc (rows g, g + 8 x tokens 2t, 2t + 1 of each half).
+template <class L, int WT, int NH>
+__device__ __forceinline__ void tile_chunk(const uint8_t *st, const uint32_t *fb,
+                                           const float *invb, float (&acc)[NH][4], int tw,
+                                           int sw, int lane, int t) {
+    constexpr int TN = L::TN;
+    // The tile: 16 rows over this warp's 64-element slices of the chunk, a
+    // partial sum per slice (per term, added after the slice's MMAs).
+#pragma unroll 1
+    for (int p = sw * L::kPP; p < (sw + 1) * L::kPP; ++p) {
+        float part[NH][TN][4];
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+#pragma unroll
+            for (int term = 0; term < TN; ++term)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) part[h][term][r] = 0.f;
+        const uint8_t *box = st + p * L::kBoxBytes;
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = p * 4 + k4;
+            // ldmatrix.x4: matrices (rows 0-7, k 0-7), (8-15, 0-7), (0-7, 8-15),
+            // (8-15, 8-15) of the tile: lane l gives row (l & 8) + (l & 7) of
+            // matrix l / 8, 16-byte chunk 2 * k4 + l / 16, swizzled by row.
+            const int mi = lane >> 3;
+            const int row = tw * 16 + ((mi & 1) << 3) + (lane & 7);
+            const int ch = 2 * k4 + (mi >> 1);
+            uint32_t A[4];
+            ldmatrix_x4(A, smem_addr(box + row * 128 + ((ch ^ (row & 7)) << 4)));
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+#pragma unroll
+                for (int term = 0; term < TN; ++term) {
+                    const uint2 b = *reinterpret_cast<const uint2 *>(
+                        fb + (((kk * TN + term) * NH + h) * 32 + lane) * 2);
+                    mma_16<WT>(part[h][term], A, b.x, b.y);
+                }
+        }
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            const float2 iv = *reinterpret_cast<const float2 *>(invb + p * 16 + h * 8 + 2 * t);
+            float v[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                v[r] = TN == 3 ? (part[h][0][r] + part[h][1][r]) + part[h][TN - 1][r]
+                               : part[h][0][r] + part[h][1][r];
+            acc[h][0] = fmaf(iv.x, v[0], acc[h][0]);
+            acc[h][1] = fmaf(iv.y, v[1], acc[h][1]);
+            acc[h][2] = fmaf(iv.x, v[2], acc[h][2]);
+            acc[h][3] = fmaf(iv.y, v[3], acc[h][3]);
+        }
+    }
 }
 
 template <int WT, int T, int KS, int NH>
@@ -235,7 +323,7 @@ __global__ void __launch_bounds__(BL<WT, T, KS, NH>::kThreads, 1)
                         tma_load_2d(dst + b * L::kBoxBytes, &wmap, c * kChunk + b * kBoxK, row0,
                                     &full[s], policy);
                     for (int i = 0; i < n; ++i)
-                        bulk_g2s_x(dst + L::kWBytes + i * kChunk * 4,
+                        bulk_g2s_nohint(dst + L::kWBytes + i * kChunk * 4,
                                    a.X + (size_t)i * k + (size_t)c * kChunk, kChunk * 4, &full[s]);
                     if (++s == S) {
                         s = 0;
@@ -269,98 +357,14 @@ __global__ void __launch_bounds__(BL<WT, T, KS, NH>::kThreads, 1)
                 if (!*abort_flag) record_status(a.status, kStTimeout);
                 *abort_flag = 1u;
             }
-            // Every consumer warp meets here each chunk, timed out or not; the flag
-            // read after the barrier is the same in all of them.
+            // Every consumer warp meets here each chunk, timed out or not, and all of
+            // them get the same answer (lane 0 of a warp that gave up set the flag).
             const uint8_t *st = stages + (size_t)s * L::kStageBytes;
             uint32_t *fb = bufs + (int)(q & 1) * L::kBufWords;
             float *invb = reinterpret_cast<float *>(fb + L::kFragWords);
-            if (w) {
-                // B: one warp per (token, 64-element slice): scale by a power of two,
-                // split into TN terms, store each where its fragment wants it.
-                const float *xs = reinterpret_cast<const float *>(st + L::kWBytes);
-                uint16_t *f16 = reinterpret_cast<uint16_t *>(fb);
-                for (int it = warp; it < n * kParts; it += CW) {
-                    const int tok = it / kParts, p = it % kParts;
-                    const float x0 = xs[tok * kChunk + p * kBoxK + lane];
-                    const float x1 = xs[tok * kChunk + p * kBoxK + 32 + lane];
-                    const uint32_t mb = __reduce_max_sync(
-                        0xFFFFFFFFu, max(__float_as_uint(x0) & 0x7FFFFFFFu,
-                                         __float_as_uint(x1) & 0x7FFFFFFFu));
-                    // sc = 2^(sb - 127) with the slice's largest |x| * sc in [2^target,
-                    // 2^(target + 1)) (E is that |x|'s biased exponent); sb kept in [1,
-                    // 253] so that sc and 1/sc are normal.
-                    const int E = (int)((mb >> 23) & 0xFFu);
-                    const int sb = min(253, max(1, 254 + Terms<WT>::kTarget - E));
-                    const float sc = __uint_as_float((uint32_t)sb << 23);
-                    if (lane == 0) invb[p * 16 + tok] = __uint_as_float((uint32_t)(254 - sb) << 23);
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float xv = (e ? x1 : x0) * sc;
-                        const uint16_t h1 = term_rn<WT>(xv);
-                        const float r1 = xv - term_val<WT>(h1);
-                        const uint16_t h2 = term_rn<WT>(r1);
-                        // element kc of the chunk -> k-step kk, register reg of thread
-                        // (g = token % 8, tt), low or high half
-                        const int kc = p * kBoxK + e * 32 + lane;
-                        const int kk = kc >> 4, r = kc & 15;
-                        const int reg = r >> 3, tt = (r & 7) >> 1, half = r & 1;
-                        const int ln = (tok & 7) * 4 + tt;
-                        const int i0 = (((kk * TN * NH + (tok >> 3)) * 32 + ln) * 2 + reg) * 2 + half;
-                        f16[i0] = h1;                   // term 0
-                        f16[i0 + NH * 128] = h2;        // term 1: + NH * 32 lanes * 2 regs * 2
-                        if (TN == 3)                    // term 2
-                            f16[i0 + 2 * NH * 128] = term_rn<WT>(r1 - term_val<WT>(h2));
-                    }
-                }
-            }
-            consumers_sync<CW>();
-            if (*abort_flag) return;
-            // The tile: 16 rows over this warp's 64-element slices of the chunk, a
-            // partial sum per slice (per term, added after the slice's MMAs).
-#pragma unroll 1
-            for (int p = sw * L::kPP; p < (sw + 1) * L::kPP; ++p) {
-                float part[NH][TN][4];
-#pragma unroll
-                for (int h = 0; h < NH; ++h)
-#pragma unroll
-                    for (int term = 0; term < TN; ++term)
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) part[h][term][r] = 0.f;
-                const uint8_t *box = st + p * L::kBoxBytes;
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int kk = p * 4 + k4;
-                    // ldmatrix.x4: matrices (rows 0-7, k 0-7), (8-15, 0-7), (0-7, 8-15),
-                    // (8-15, 8-15) of the tile: lane l gives row (l & 8) + (l & 7) of
-                    // matrix l / 8, 16-byte chunk 2 * k4 + l / 16, swizzled by row.
-                    const int mi = lane >> 3;
-                    const int row = tw * 16 + ((mi & 1) << 3) + (lane & 7);
-                    const int ch = 2 * k4 + (mi >> 1);
-                    uint32_t A[4];
-                    ldmatrix_x4(A, smem_addr(box + row * 128 + ((ch ^ (row & 7)) << 4)));
-#pragma unroll
-                    for (int h = 0; h < NH; ++h)
-#pragma unroll
-                        for (int term = 0; term < TN; ++term) {
-                            const uint2 b = *reinterpret_cast<const uint2 *>(
-                                fb + (((kk * TN + term) * NH + h) * 32 + lane) * 2);
-                            mma_16<WT>(part[h][term], A, b.x, b.y);
-                        }
-                }
-#pragma unroll
-                for (int h = 0; h < NH; ++h) {
-                    const float2 iv = *reinterpret_cast<const float2 *>(invb + p * 16 + h * 8 + 2 * t);
-                    float v[4];
-#pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        v[r] = TN == 3 ? (part[h][0][r] + part[h][1][r]) + part[h][TN - 1][r]
-                                       : part[h][0][r] + part[h][1][r];
-                    acc[h][0] = fmaf(iv.x, v[0], acc[h][0]);
-                    acc[h][1] = fmaf(iv.y, v[1], acc[h][1]);
-                    acc[h][2] = fmaf(iv.x, v[2], acc[h][2]);
-                    acc[h][3] = fmaf(iv.y, v[3], acc[h][3]);
-                }
-            }
+            if (w) build_b<L, WT, NH, CW>(st, fb, invb, n, warp, lane);
+            if (consumers_sync_any<CW>(*abort_flag != 0u)) return;
+            tile_chunk<L, WT, NH>(st, fb, invb, acc, tw, sw, lane, t);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             if (++s == S) {
@@ -410,6 +414,240 @@ __global__ void __launch_bounds__(BL<WT, T, KS, NH>::kThreads, 1)
     }
 }
 
+// Tensor maps of a weight bank [E][m][k]: boxes of the group's T tiles, and of 2 and
+// 1 tiles, from which a shorter group's rows are composed (rows past an expert's m
+// read as zero: the bank is a 3-D tensor).
+struct BankMaps {
+    CUtensorMap full, b2, b1;
+};
+
+// The routed MoE matvec (hanzo-ml 0.11.13 moe_matvec_gpu) with bf16 or F16 weights:
+// y[s] = W[ids[s]] . x[s / topk] for every slot s, through the epilogue.  The
+// arithmetic per chunk is the GEMV kernel's (build_b, tile_chunk); around it, each
+// window of kMaxSlots slots is routed in shared memory (route_window) and the CTAs
+// walk the active experts' 16-row tiles in groups of T (never across an expert),
+// once per pass of up to eight of the expert's slots.  Output row s of Y and of the
+// residual is slot s's; bias row e of [E][m] is expert e's.
+//
+// A wait that runs out sets the CTA's abort flag: the consumers leave their pass
+// together (the answer of consumers_sync_any), the producer stops issuing, no window
+// is routed after it, and the producer drains its copies in flight at the end --
+// no thread leaves while others still wait at a barrier that counts it.
+template <int WT, int T, int KS>
+__global__ void __launch_bounds__(BL<WT, T, KS, 1>::kThreads, 1)
+    moe_half_kernel(const __grid_constant__ BankMaps wm, const StreamArgs a) {
+    pdl_launch();
+    using L = BL<WT, T, KS, 1>;
+    constexpr int S = L::kStages;
+    constexpr int CW = L::kCW;
+    static_assert(L::kThreads >= kMaxSlots, "routing: one thread per slot of a window");
+    static_assert(T == 1 || T == 2 || T == 4, "short groups are composed of 2- and 1-tile boxes");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t *stages = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint32_t *bufs = reinterpret_cast<uint32_t *>(stages + (size_t)S * L::kStageBytes);
+    float *red = reinterpret_cast<float *>(bufs + 2 * L::kBufWords);
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + L::kRedWords);
+    uint64_t *empty = full + S;
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(empty + S);
+    // the producer's count of stages issued, kept here between windows so that it
+    // occupies no register of the consumer warps
+    long long *s_q = reinterpret_cast<long long *>(empty + S) + 1;
+    RouteSmem rs;
+    rs.key = reinterpret_cast<unsigned long long *>(s_q + 1);
+    rs.sorted = reinterpret_cast<int *>(rs.key + kMaxSlots);
+    rs.seg = rs.sorted + kMaxSlots;
+    rs.act = rs.seg + kMaxSlots + 1;
+    rs.nact = rs.act + kMaxSlots;
+    rs.wcnt = rs.nact + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int tw = warp % T, sw = warp / T;
+    const int m = a.m, k = a.k;
+    const int KC = k / kChunk;
+    const uint64_t limit = a.wait_limit;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CW);
+        }
+        *abort_flag = 0u;
+        *s_q = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x == CW * 32) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wm.full)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wm.b1)) : "memory");
+        if (T > 2) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wm.b2)) : "memory");
+    }
+    for (int i = threadIdx.x; i < 2 * L::kBufWords; i += blockDim.x) bufs[i] = 0u;
+    pdl_wait();
+
+    Sched sc;
+    sc.tpe = (m + 15) / 16;
+    const int S_all = a.n * a.topk;
+    const int n_win = (S_all + kMaxSlots - 1) / kMaxSlots;
+    // consumers: ring position of the next chunk, carried across windows
+    long long q = 0;
+    int s = 0;
+    uint32_t ph = 0u;
+    bool ok = true;
+
+    for (int win = 0; win < n_win; ++win) {
+        const int base = win * kMaxSlots;
+        __syncthreads();  // the previous window's tables are no longer read
+        route_window(a, base, min(kMaxSlots, S_all - base), rs);
+        __syncthreads();
+        if (*abort_flag) break;  // the same in every thread: no one writes it here
+        sc.n_act = *rs.nact;
+        split_units<T>(sc, true, 7u);
+
+        if (warp == CW) {
+            // ------------------------------------------------------------ producer
+            if (lane == 0) {
+                const uint64_t policy = l2_evict_first();
+                long long qp = *s_q;
+                int sp = (int)(qp % S);
+                uint32_t wrap = (uint32_t)((qp / S) & 1);
+                bool pok = true;
+                for (Walk wk(sc); wk.more() && pok;) {
+                    const int nt = wk.group<T>();
+                    const int seg0 = rs.seg[wk.ai];
+                    const int ntok = rs.seg[wk.ai + 1] - seg0;
+                    const int trow = wk.tl * 16, ex = rs.act[wk.ai];
+                    for (int p0 = 0; p0 < ntok && pok; p0 += 8) {
+                        const int npass = min(8, ntok - p0);
+                        int tok[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            tok[i] = i < npass ? rs.sorted[seg0 + p0 + i] / a.topk : 0;
+                        for (int c = 0; c < KC; ++c, ++qp) {
+                            if (qp >= S) {  // the consumers released the slot's previous round
+                                bool w = mbar_test_wait(&empty[sp], wrap ^ 1u);
+                                for (uint64_t i = 1; !w && i < limit && !*abort_flag; ++i)
+                                    w = mbar_try_wait(&empty[sp], wrap ^ 1u);
+                                if (!w) {
+                                    if (!*abort_flag) record_status(a.status, kStTimeout);
+                                    *abort_flag = 1u;
+                                    pok = false;
+                                    break;
+                                }
+                            }
+                            uint8_t *dst = stages + (size_t)sp * L::kStageBytes;
+                            mbar_arrive_expect_tx(&full[sp], (uint32_t)(kParts * nt * 16 * 128 +
+                                                                        npass * kChunk * 4));
+                            for (int b = 0; b < kParts; ++b) {
+                                const int x = c * kChunk + b * kBoxK;
+                                uint8_t *bd = dst + b * L::kBoxBytes;
+                                if (nt == T) {
+                                    tma_load_3d(bd, &wm.full, x, trow, ex, &full[sp], policy);
+                                } else {  // tile tt of the group lands where it would in a full box
+                                    int t0 = 0;
+                                    if (T > 2 && (nt & 2)) {
+                                        tma_load_3d(bd, &wm.b2, x, trow, ex, &full[sp], policy);
+                                        t0 = 2;
+                                    }
+                                    if (nt & 1)
+                                        tma_load_3d(bd + t0 * 16 * 128, &wm.b1, x, trow + 16 * t0,
+                                                    ex, &full[sp], policy);
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                if (i < npass)
+                                    bulk_g2s_nohint(dst + L::kWBytes + i * kChunk * 4,
+                                               a.X + (size_t)tok[i] * k + (size_t)c * kChunk,
+                                               kChunk * 4, &full[sp]);
+                            if (++sp == S) {
+                                sp = 0;
+                                wrap ^= 1u;
+                            }
+                        }
+                    }
+                    wk.advance(nt);
+                }
+                *s_q = qp;
+            }
+            __syncwarp();
+        } else {
+            // ------------------------------------------------------------ consumers
+            for (Walk wk(sc); wk.more() && ok;) {
+                const int nt = wk.group<T>();
+                const int seg0 = rs.seg[wk.ai];
+                const int ntok = rs.seg[wk.ai + 1] - seg0;
+                const int row0 = wk.tl * 16, ex = rs.act[wk.ai];
+                for (int p0 = 0; p0 < ntok && ok; p0 += 8) {
+                    const int npass = min(8, ntok - p0);
+                    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+                    for (int c = 0; c < KC; ++c, ++q) {
+                        bool w = mbar_test_wait(&full[s], ph);
+                        for (uint64_t i = 1; !w && i < limit && !*abort_flag; ++i)
+                            w = mbar_try_wait(&full[s], ph);
+                        w = __all_sync(0xFFFFFFFFu, w);
+                        if (!w && lane == 0) {
+                            if (!*abort_flag) record_status(a.status, kStTimeout);
+                            *abort_flag = 1u;
+                        }
+                        const uint8_t *st = stages + (size_t)s * L::kStageBytes;
+                        uint32_t *fb = bufs + (int)(q & 1) * L::kBufWords;
+                        float *invb = reinterpret_cast<float *>(fb + L::kFragWords);
+                        if (w) build_b<L, WT, 1, CW>(st, fb, invb, npass, warp, lane);
+                        if (consumers_sync_any<CW>(*abort_flag != 0u)) {
+                            ok = false;
+                            break;
+                        }
+                        if (tw < nt) tile_chunk<L, WT, 1>(st, fb, invb, acc, tw, sw, lane, t);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[s]);
+                        if (++s == S) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    if (KS > 1) {  // the tile's slices, added in slice order
+                        float *mine = red + ((sw * T + tw) * 32 + lane) * 4;
+                        if (sw > 0)
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) mine[r] = acc[0][r];
+                        consumers_sync<CW>();
+                        if (sw == 0) {
+#pragma unroll 1
+                            for (int s2 = 1; s2 < KS; ++s2) {
+                                const float *o = red + ((s2 * T + tw) * 32 + lane) * 4;
+#pragma unroll
+                                for (int r = 0; r < 4; ++r) acc[0][r] += o[r];
+                            }
+                        }
+                    }
+                    if (sw != 0 || tw >= nt) continue;
+                    // Epilogue: rows g, g + 8 of the tile for the pass's slots 2t, 2t + 1.
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int row = row0 + tw * 16 + g + (r >= 2 ? 8 : 0);
+                        const int i = 2 * t + (r & 1);
+                        if (row < m && i < npass) {
+                            const size_t yo = (size_t)rs.sorted[seg0 + p0 + i] * m + row;
+                            const float bj = (a.flags & kBias) ? a.bias[(size_t)ex * m + row] : 0.f;
+                            const float rij = (a.flags & kResidual) ? a.R[yo] : 0.f;
+                            a.Y[yo] = epilogue_vals(acc[0][r], a.flags, bj, rij, a.alpha);
+                        }
+                    }
+                }
+                wk.advance(nt);
+            }
+        }
+    }
+    if (warp == CW && lane == 0) {
+        // Drain copies that no consumer waited for (only after an abort).
+        const long long qp = *s_q;
+        for (long long d = (qp > S ? qp - S : 0); d < qp; ++d)
+            mbar_wait(&full[d % S], (uint32_t)((d / S) & 1), kDrainPolls);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -450,6 +688,40 @@ cudaError_t launch_t(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t st
     return launch_pdl(kern, dim3(grid), dim3(L::kThreads), L::kBytes, stream, map, a);
 }
 
+// A weight bank as a 3-D tensor of 16-bit elements [E][m][k]: boxes of 64 elements x
+// `rows` rows of one matrix, 128-byte swizzle.
+bool make_bank_map(CUtensorMap &map, const StreamArgs &a, int rows) {
+    auto encode = encode_fn();
+    if (!encode) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)a.k, (cuuint64_t)a.m, (cuuint64_t)a.n_experts};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.k * 2, (cuuint64_t)a.m * a.k * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kBoxK, (cuuint32_t)rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint8_t *>(a.W), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Routing tables and the producer's stage count after the GEMV kernel's layout.
+constexpr size_t kRouteBytes = 8 + kMaxSlots * 8 + (3 * kMaxSlots + 2 + kMaxSlots / 32) * 4;
+
+template <int WT, int T, int KS>
+cudaError_t launch_moe_t(const StreamArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
+    using L = BL<WT, T, KS, 1>;
+    static std::atomic<unsigned long long> smem_set{0};
+    BankMaps maps;
+    if (!make_bank_map(maps.full, a, T * 16) || !make_bank_map(maps.b2, a, (T > 2 ? 2 : T) * 16) ||
+        !make_bank_map(maps.b1, a, 16))
+        return cudaErrorInvalidValue;
+    auto kern = moe_half_kernel<WT, T, KS>;
+    constexpr size_t bytes = L::kBytes + kRouteBytes;
+    static_assert(bytes <= 227 * 1024, "shared memory budget");
+    cudaError_t err = ensure_smem(kern, (int)bytes, dev, smem_set);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3(dev.sm_count), dim3(L::kThreads), bytes, stream, maps, a);
+}
+
 }  // namespace
 
 namespace {
@@ -478,6 +750,18 @@ bool half_gemv_supported(int wtype, int n, int k) {
 cudaError_t launch_half_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,
                              cudaStream_t stream) {
     return wtype == kBF16 ? launch_wt<kBF16>(a, dev, stream) : launch_wt<kF16>(a, dev, stream);
+}
+
+bool half_moe_supported(int wtype, int k) {
+    return (wtype == kBF16 || wtype == kF16) && k % kChunk == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_half_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,
+                            cudaStream_t stream) {
+    // Four 16-row tiles per group and two k slices: eight consumer warps, 288 threads
+    // (routing wants one per slot of a window).
+    return wtype == kBF16 ? launch_moe_t<kBF16, 4, 2>(a, dev, stream)
+                          : launch_moe_t<kF16, 4, 2>(a, dev, stream);
 }
 
 }  // namespace wq

@@ -53,6 +53,7 @@
 
 #include "wq_device.cuh"
 #include "wq_internal.h"
+#include "tile_sched.cuh"
 
 namespace wq {
 namespace {
@@ -68,7 +69,6 @@ struct Warps {
     static constexpr int kXChunkBytes = CW * 32 * 4;        // one token's X for one chunk (f32)
     static constexpr int kSmemBudget = (CW == 16 ? 200 : 108) * 1024;  // stages + reduction
 };
-constexpr int kMaxSlots = 256;
 
 // A stage holds, for every row of the group, the NB blocks of one chunk, loaded as
 // NBOX tall TMA boxes (the box inner size is at most 256 u16, so Q8_0's 544-byte
@@ -264,16 +264,6 @@ __device__ __forceinline__ float f16_f32(uint16_t h) {
     return v;
 }
 
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y,
-                                            int z, uint64_t *bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
-        "l"(policy)
-        : "memory");
-}
-
 // 4-byte global -> shared copy that does not hold a register (completes at
 // cp_async_wait_all).
 __device__ __forceinline__ void cp_async4(float *dst, const float *src) {
@@ -289,62 +279,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Global -> shared bulk copy completing on `bar`, default L2 policy (X is read
-// by every CTA).
-__device__ __forceinline__ void bulk_g2s_nohint(void *dst, const void *src, uint32_t bytes,
-                                                uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-template <int CW>
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
-}
-
-// ------------------------------------------------------------ job schedule --
-//
-// Work units are 16-row tiles; GEMV: tiles 0..ceil(m/16) of the one matrix; MoE:
-// tiles of the active experts in order (expert a owns units [a*tpe, (a+1)*tpe)).
-// A CTA takes a contiguous range of units and processes it in row groups of at
-// most T tiles that never straddle an expert; every group is run once per pass
-// of at most P tokens.
-
-struct Sched {
-    int n_act;          // MoE: active experts; GEMV: 1
-    int tpe;            // tiles per expert (GEMV: per matrix)
-    long long u0, u1;   // this CTA's unit range
-};
-
-// A walk over the CTA's unit range by row groups.  The position (slot ai among
-// the active experts, tile tl within it) is advanced by addition: one division
-// when the walk starts, none per group or per chunk.
-struct Walk {
-    long long u, u1;  // next unit, end of the range
-    int ai, tl, tpe;
-    __device__ __forceinline__ explicit Walk(const Sched &sc) : u(sc.u0), u1(sc.u1), tpe(sc.tpe) {
-        ai = u < (1ll << 32) ? (int)((uint32_t)u / (uint32_t)tpe) : (int)(u / tpe);
-        tl = (int)(u - (long long)ai * tpe);
-    }
-    __device__ __forceinline__ bool more() const { return u < u1; }
-    // Tiles in the next group: at most T, never past the expert or the range.
-    template <int T>
-    __device__ __forceinline__ int group() const {
-        long long e = T < tpe - tl ? T : tpe - tl;
-        if (e > u1 - u) e = u1 - u;
-        return (int)e;
-    }
-    __device__ __forceinline__ void advance(int nt) {
-        u += nt;
-        tl += nt;
-        if (tl == tpe) {
-            tl = 0;
-            ++ai;
-        }
-    }
-};
 
 // Tensor maps of the weight image, one per box height: the group's T tiles, and
 // 4, 2 and 1 tiles, from which a shorter group's rows are composed (binary
@@ -428,141 +362,16 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
 
     for (int win = 0; win < n_win; ++win) {
     if (MOE) {
-        // Sort the window's slots by (expert, slot); bad ids go last.
         const int base = win * kMaxSlots;
-        const int Sl = min(kMaxSlots, S_all - base);
-        const bool k32_ok = a.n_experts < (1 << 24) - 1;
-        uint32_t *k32 = reinterpret_cast<uint32_t *>(s_key);
-        if (k32_ok) {
-            // 32-bit keys expert << 8 | slot (a bad id as expert 0xFFFFFF), padded to
-            // a whole number of 16-byte quads with keys that rank below none; each
-            // key's rank is counted by up to four threads over slices of the quads.
-            int *s_rank = reinterpret_cast<int *>(k32 + kMaxSlots);
-            for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
-                const int e = a.ids[base + i];
-                const bool okid = e >= 0 && e < a.n_experts;
-                if (!okid && blockIdx.x == 0) record_status(a.status, kStBadExpert);
-                k32[i] = ((okid ? (uint32_t)e : 0xFFFFFFu) << 8) | (uint32_t)i;
-                s_rank[i] = 0;
-            }
-            const int nq = (Sl + 3) / 4;
-            if (threadIdx.x < 4 * nq - Sl) k32[Sl + threadIdx.x] = 0xFFFFFFFFu;
-            __syncthreads();
-            const int parts = max(1, min(4, (int)blockDim.x / Sl));
-            const int qper = (nq + parts - 1) / parts;
-            for (int idx = threadIdx.x; idx < Sl * parts; idx += blockDim.x) {
-                const int part = idx / Sl, i = idx - part * Sl;
-                const uint32_t ki = k32[i];
-                int r = 0;
-                const int q1 = min(nq, (part + 1) * qper);
-                for (int q = part * qper; q < q1; ++q) {
-                    const uint4 kk = reinterpret_cast<const uint4 *>(k32)[q];
-                    r += (int)(kk.x < ki) + (int)(kk.y < ki) + (int)(kk.z < ki) + (int)(kk.w < ki);
-                }
-                atomicAdd(&s_rank[i], r);
-            }
-            __syncthreads();
-            for (int i = threadIdx.x; i < Sl; i += blockDim.x) s_sorted[s_rank[i]] = base + i;
-        } else {
-            const unsigned long long big = 1ull << 62;
-            for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
-                const int e = a.ids[base + i];
-                const bool okid = e >= 0 && e < a.n_experts;
-                if (!okid && blockIdx.x == 0) record_status(a.status, kStBadExpert);
-                s_key[i] = okid ? ((unsigned long long)e << 16) | (unsigned)i : big | (unsigned)i;
-            }
-            __syncthreads();
-            for (int i = threadIdx.x; i < Sl; i += blockDim.x) {
-                const unsigned long long ki = s_key[i];
-                int r = 0;
-                for (int i2 = 0; i2 < Sl; ++i2) r += s_key[i2] < ki;
-                s_sorted[r] = base + i;  // the slot's global index
-            }
-        }
-        __syncthreads();
-        // The expert of the r-th sorted slot, or -1 for a bad id.
-        auto sorted_expert = [&](int r) -> int {
-            const int i = s_sorted[r] - base;
-            if (k32_ok) {
-                const uint32_t e = k32[i] >> 8;
-                return e == 0xFFFFFFu ? -1 : (int)e;
-            }
-            const unsigned long long kr = s_key[i];
-            return (kr >> 62) ? -1 : (int)(kr >> 16);
-        };
-        // Segments of the sorted slots, one thread per position (blockDim >= 256):
-        // position r starts one when its expert differs from r - 1's, and the starts
-        // are numbered by a count over the warps' ballots.
-        {
-            const int r = threadIdx.x;
-            int e = -1;
-            bool start = false, last = false;
-            if (r < Sl) {
-                e = sorted_expert(r);
-                start = e >= 0 && (r == 0 || sorted_expert(r - 1) != e);
-                last = e >= 0 && (r == Sl - 1 || sorted_expert(r + 1) < 0);
-            }
-            const unsigned bm = __ballot_sync(0xFFFFFFFFu, start);
-            if (lane == 0) s_wcnt[warp] = __popc(bm);
-            __syncthreads();
-            int before = 0, total = 0;
-            for (int w = 0; w < (Sl + 31) / 32; ++w) {
-                const int c = s_wcnt[w];
-                before += w < warp ? c : 0;
-                total += c;
-            }
-            if (start) {
-                const int idx = before + __popc(bm & ((1u << lane) - 1u));
-                s_seg[idx] = r;
-                s_act[idx] = e;
-            }
-            if (last) {  // the valid slots end here (bad ids sort last)
-                s_seg[total] = r + 1;
-                *s_nact = total;
-            }
-            if (r == 0 && e < 0) {  // no valid slot in the window
-                s_seg[0] = 0;
-                *s_nact = 0;
-            }
-        }
+        route_window(a, base, min(kMaxSlots, S_all - base),
+                     RouteSmem{s_key, s_sorted, s_seg, s_act, s_nact, s_wcnt});
     }
     __syncthreads();
     if (*abort_flag) break;  // the same in every thread after the barrier
     sc.n_act = MOE ? *s_nact : 1;
-    const long long units = (long long)sc.n_act * sc.tpe;
-    bool by_group = false;
-    if (MOE && units * gridDim.x < (1ll << 32)) {
-        // MoE: split by whole groups of T tiles when that is cheaper.  A pass over a
-        // group costs about seven tiles' worth of per-chunk work besides its tiles
-        // (measured), and a split by tiles gives a CTA an extra, short group wherever
-        // its range crosses an expert's end.
-        const uint32_t tpe = (uint32_t)sc.tpe, grid = gridDim.x;
-        const uint32_t gpe = (tpe + T - 1) / T;                 // groups per expert
-        const uint32_t G = (uint32_t)sc.n_act * gpe;
-        const uint32_t per_g = (G + grid - 1) / grid;
-        const uint32_t per_t = ((uint32_t)units + grid - 1) / grid;
-        const uint32_t cost_g = per_g * (7 + T);
-        const uint32_t cost_t = ((per_t + T - 1) / T + (per_t > 1 ? 1 : 0)) * 7 + per_t;
-        if (cost_g < cost_t) {
-            by_group = true;
-            auto unit_of = [&](uint32_t gi) -> long long {
-                const uint32_t e = gi / gpe;
-                return (long long)e * tpe + (long long)(gi - e * gpe) * T;
-            };
-            sc.u0 = unit_of(G * blockIdx.x / grid);
-            sc.u1 = unit_of(G * (blockIdx.x + 1) / grid);
-        }
-    }
-    if (by_group) {
-    } else if (units * gridDim.x < (1ll << 32)) {  // the usual case: 32-bit divisions
-        const uint32_t uu = (uint32_t)units;
-        sc.u0 = uu * blockIdx.x / gridDim.x;
-        sc.u1 = uu * (blockIdx.x + 1) / gridDim.x;
-    } else {
-        sc.u0 = units * blockIdx.x / gridDim.x;
-        sc.u1 = units * (blockIdx.x + 1) / gridDim.x;
-    }
-
+    // (a pass over a group costs about seven tiles' worth of per-chunk work besides
+    // its tiles: measured)
+    split_units<T>(sc, MOE, 7u);
 
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
@@ -968,10 +777,10 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                 };
                 round(0);
                 cp_async_wait_all();  // staged bias/residual: visible to all after the barrier
-                // Every consumer warp gets here, aborted or not; the flag read after the
-                // barrier is the same in all of them, so they leave (or go on) together.
-                consumers_sync<CW>();
-                ok = *abort_flag == 0u;
+                // Every consumer warp gets here, aborted or not, and all of them get the
+                // same answer, so they leave (or go on) together (lane 0 of a warp that
+                // gave up has set the flag itself).
+                ok = !consumers_sync_any<CW>(*abort_flag != 0u);
                 if (!ok) return;
                 for (int rnd = 1; rnd < kCW / NB; ++rnd) {
                     round(rnd);

@@ -290,6 +290,8 @@ wq_status wq_moe_gemv(int n_tok, int topk, int n_experts, int m, int k, int wtyp
     a.n_experts = n_experts;
     if (mma_gemv_supported(wtype, k))
         return cuda_status(launch_mma_moe(a, wtype, *dev, (cudaStream_t)stream));
+    if (half_moe_supported(wtype, k))
+        return cuda_status(launch_half_moe(a, wtype, *dev, (cudaStream_t)stream));
     return cuda_status(launch_stream_moe(a, wtype, *dev, (cudaStream_t)stream));
 }
 

@@ -103,6 +103,10 @@ bool mma_gemv_supported(int wtype, int k);
 bool half_gemv_supported(int wtype, int n, int k);
 cudaError_t launch_half_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,
                              cudaStream_t stream);
+// bf16 / F16 routed MoE matvec on the tensor cores (k % 256 == 0).
+bool half_moe_supported(int wtype, int k);
+cudaError_t launch_half_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,
+                            cudaStream_t stream);
 cudaError_t launch_mma_gemv(const StreamArgs &a, int wtype, const DeviceInfo &dev,
                             cudaStream_t stream);
 cudaError_t launch_mma_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev,

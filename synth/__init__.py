@@ -249,12 +249,15 @@ def workload_encoder_gemms(seed=4, n=1500, d=1024, inter=4096):
     return out
 
 
-def workload_moe(seed=5, n_experts=64, m=1408, k=2048, n_tok=16, topk=6):
-    """MoE Q4_0 routed GEMV over one weight bank ``[E][m][k]``."""
+def workload_moe(seed=5, n_experts=64, m=1408, k=2048, n_tok=16, topk=6, wtype=WTYPE_Q4_0):
+    """MoE routed GEMV over one weight bank ``[E][m][k]`` (Q4_0 unless ``wtype``
+    says otherwise)."""
     g = rng(seed)
-    bank = draw_q4_0_weights(g, n_experts * m, k).reshape(n_experts, m, -1)
-    return dict(name=f"moe_q4_0_E{n_experts}_m{m}_k{k}_t{n_tok}x{topk}", kind="moe",
-                wtype=WTYPE_Q4_0, n_tok=n_tok, topk=topk, n_experts=n_experts, m=m, k=k,
+    bank = draw_weights(g, wtype, n_experts * m, k).reshape(n_experts, m, -1)
+    tag = {WTYPE_Q4_0: "q4_0", WTYPE_Q8_0: "q8_0", WTYPE_BF16: "bf16", WTYPE_F16: "f16",
+           WTYPE_F32: "f32"}[wtype]
+    return dict(name=f"moe_{tag}_E{n_experts}_m{m}_k{k}_t{n_tok}x{topk}", kind="moe",
+                wtype=wtype, n_tok=n_tok, topk=topk, n_experts=n_experts, m=m, k=k,
                 flags=0, W=bank, X=normal_f32(g, (n_tok, k)),
                 ids=moe_ids(g, n_tok, topk, n_experts), bias=None, residual=None)
 

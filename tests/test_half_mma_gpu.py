@@ -156,3 +156,136 @@ def test_bit_identical_reruns(wt):
     Y1 = run(n, m, k, 0, X, img, wt=wt)
     Y2 = run(n, m, k, 0, X, img, wt=wt)
     assert (Y1.view(np.int32) == Y2.view(np.int32)).all()
+
+
+# -------------------------------------------------------------------- MoE --
+# wq_moe_gemv with bf16 or F16 banks and k % 256 == 0 runs the same arithmetic per
+# chunk (hanzo-ml 0.11.13 moe_matvec_gpu: y[s] = W[ids[s]] . x[s / topk]), with the
+# window's slots sorted by expert in shared memory and groups of four 16-row tiles
+# that never cross an expert; short groups (m / 16 not a multiple of 4) load only
+# their own rows.
+
+def run_moe(oracle_mod, wt, n_tok, topk, E, m, k, flags, ids, seed, slots=None):
+    g = synth.rng(seed)
+    bank = synth.draw_weights(g, wt, E * m, k).reshape(E, m, -1)
+    X = synth.normal_f32(g, (n_tok, k))
+    bias = synth.normal_f32(g, (E, m), 0.1) if flags & BIAS else None
+    R = synth.normal_f32(g, (n_tok * topk, m)) if flags & RES else None
+    out = Guarded(n_tok * topk * m)
+    wq.check(wq.wq_moe_gemv(n_tok, topk, E, m, k, wt, flags, dev(X),
+                            weights_dev(bank, wt, E * m, k), dev(ids),
+                            None if bias is None else dev(bias),
+                            None if R is None else dev(R), out.view), "wq_moe_gemv")
+    torch.cuda.synchronize()
+    status_ok()
+    Y = out.result().reshape(n_tok * topk, m)
+    q0, q1 = slots or (0, n_tok * topk)
+    Yref, S = oracle_mod.moe(n_tok, topk, E, m, k, wt, flags, X, bank, ids, bias=bias,
+                             residual=R, slots=(q0, q1))
+    extra = np.zeros((n_tok * topk, m))
+    if bias is not None:
+        extra += np.abs(bias[ids.reshape(-1)])
+    if R is not None:
+        extra += np.abs(R)
+    sl = slice(q0, q1)
+    assert_within(Y[sl], Yref[sl], S[sl], TAU, gelu=bool(flags & GELU), R=extra[sl],
+                  what=f"moe wtype {wt} slots={n_tok * topk} E={E} m={m} k={k}")
+    return Y
+
+
+MOE_CFGS = [(1, 1, 1, 33, 256),        # one slot; three tiles: a 2 + 1 short group
+            (3, 2, 5, 70, 512),        # five tiles: a full group and a 1-tile group
+            (16, 6, 64, 140, 2048),    # the decode routing of a 64-expert layer
+            (8, 3, 4, 257, 4096),      # a ragged last tile
+            (32, 8, 4, 72, 512)]       # ~64 slots per expert: eight passes of 8 slots
+
+
+@HALF
+@pytest.mark.parametrize("cfg", MOE_CFGS)
+def test_moe(oracle_mod, wt, cfg):
+    n_tok, topk, E, m, k = cfg
+    g = synth.rng(sum(cfg) + 60 * wt)
+    ids = synth.moe_ids(g, n_tok, topk, E) if topk <= E else \
+        g.integers(0, E, size=(n_tok, topk)).astype(np.int32)
+    run_moe(oracle_mod, wt, n_tok, topk, E, m, k, BIAS | GELU | RES, ids, sum(cfg) + wt)
+
+
+@HALF
+def test_moe_windows(oracle_mod, wt):
+    """512 tokens at top-6: 3,072 slots, twelve routing windows."""
+    n_tok, topk, E, m, k = 512, 6, 64, 72, 512
+    ids = synth.moe_ids(synth.rng(910 + wt), n_tok, topk, E)
+    run_moe(oracle_mod, wt, n_tok, topk, E, m, k, BIAS | RES, ids, 911 + wt)
+
+
+@HALF
+def test_moe_one_expert_takes_every_slot(oracle_mod, wt):
+    n_tok, topk, E, m, k = 1024, 3, 8, 40, 256
+    ids = np.full((n_tok, topk), 5, np.int32)
+    run_moe(oracle_mod, wt, n_tok, topk, E, m, k, 0, ids, 960 + wt)
+
+
+@HALF
+def test_moe_window_edge(oracle_mod, wt):
+    """257 slots: one full window and a window of one slot."""
+    n_tok, topk, E, m, k = 257, 1, 7, 33, 512
+    ids = synth.rng(987).integers(0, E, size=(n_tok, topk)).astype(np.int32)
+    run_moe(oracle_mod, wt, n_tok, topk, E, m, k, BIAS, ids, 988 + wt)
+
+
+@HALF
+def test_moe_repeated_expert_and_bad_id(oracle_mod, wt):
+    """A token may route twice to one expert; a bad id sets the device status and
+    leaves only its own slot's row unwritten."""
+    n_tok, topk, E, m, k = 4, 3, 6, 50, 256
+    g = synth.rng(12 + wt)
+    bank = synth.draw_weights(g, wt, E * m, k).reshape(E, m, -1)
+    X = synth.normal_f32(g, (n_tok, k))
+    ids = np.array([[1, 1, 2], [5, 0, 1], [3, 9, 3], [2, 2, 2]], np.int32)  # 9 is out of range
+    out = Guarded(n_tok * topk * m)
+    wq.check(wq.wq_moe_gemv(n_tok, topk, E, m, k, wt, 0, dev(X), weights_dev(bank, wt, E * m, k),
+                            dev(ids), None, None, out.view), "wq_moe_gemv")
+    torch.cuda.synchronize()
+    assert wq.wq_get_device_status() == wq.WQ_ERR_BAD_EXPERT
+    status_ok()  # cleared by the read
+    Y = out.result().reshape(n_tok * topk, m)
+    bad = 2 * topk + 1
+    assert (Y[bad].view(np.int32) == -1).all()
+    good = [q for q in range(n_tok * topk) if q != bad]
+    ids_ok = ids.copy()
+    ids_ok[2, 1] = 0
+    Yref, S = oracle_mod.moe(n_tok, topk, E, m, k, wt, 0, X, bank, ids_ok)
+    assert_within(Y[good], Yref[good], S[good], TAU, what="moe repeated ids")
+
+
+@HALF
+def test_moe_exact_integers(oracle_mod, wt):
+    """Small integers in X and the bank: every product and partial sum is exact, so
+    each slot's row equals the oracle's bit for bit."""
+    n_tok, topk, E, m, k = 6, 4, 5, 90, 768
+    g = synth.rng(78 + wt)
+    X = g.integers(-8, 9, size=(n_tok, k)).astype(np.float32)
+    Wf = g.integers(-8, 9, size=(E * m, k)).astype(np.float32)
+    if wt == BF16:
+        img = synth.bf16_pairs((Wf.view(np.uint32) >> 16).astype(np.uint16))
+    else:
+        img = Wf.astype(np.float16).view(np.uint8).reshape(E * m, 2 * k)
+    bank = img.reshape(E, m, -1)
+    ids = synth.moe_ids(g, n_tok, topk, E)
+    out = Guarded(n_tok * topk * m)
+    wq.check(wq.wq_moe_gemv(n_tok, topk, E, m, k, wt, 0, dev(X), weights_dev(bank, wt, E * m, k),
+                            dev(ids), None, None, out.view), "wq_moe_gemv")
+    torch.cuda.synchronize()
+    status_ok()
+    Y = out.result().reshape(n_tok * topk, m)
+    Yref, _ = oracle_mod.moe(n_tok, topk, E, m, k, wt, 0, X, bank, ids)
+    assert (Y == Yref.astype(np.float32)).all()
+
+
+@HALF
+def test_moe_bit_identical_reruns(oracle_mod, wt):
+    n_tok, topk, E, m, k = 16, 6, 64, 300, 1024
+    ids = synth.moe_ids(synth.rng(4), n_tok, topk, E)
+    Y1 = run_moe(oracle_mod, wt, n_tok, topk, E, m, k, BIAS, ids, 5, slots=(0, 8))
+    Y2 = run_moe(oracle_mod, wt, n_tok, topk, E, m, k, BIAS, ids, 5, slots=(0, 8))
+    assert (Y1.view(np.int32) == Y2.view(np.int32)).all()

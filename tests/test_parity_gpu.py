@@ -405,3 +405,36 @@ def test_wait_limit_expires_without_hang(oracle_mod, wtype, n, m, k):
     Yref, S = oracle_mod.gemm(n, m, k, wtype, 0, X, img, rows=rows)
     got = Y.cpu().numpy().reshape(n, m)
     assert_within(got[:, :256], Yref[:, :256], S[:, :256], TAU)
+
+
+@pytest.mark.parametrize("wtype", [Q4_0, BF16])  # tensor-core MoE: quantized / bf16 bank
+def test_moe_wait_limit_expires_without_hang(oracle_mod, wtype):
+    """The same with the routed MoE kernels, over two routing windows: a wait that
+    gives up must not strand the other warps of its CTA at a barrier, in this window
+    or the next; the next call (default limit) is correct."""
+    n_tok, topk, E, m, k = 64, 8, 8, 4096, 4096
+    g = synth.rng(6 + wtype)
+    bank = synth.draw_weights(g, wtype, E * m, k).reshape(E, m, -1)
+    X = synth.normal_f32(g, (n_tok, k))
+    ids = synth.moe_ids(g, n_tok, topk, E)
+    Xd, Wd, idd = dev(X), weights_dev(bank, wtype, E * m, k), dev(ids)
+    Y = torch.zeros(n_tok * topk * m, device="cuda")
+    seen = []
+    wq.wq_set_wait_limit(1)
+    try:
+        for _ in range(5):
+            wq.check(wq.wq_moe_gemv(n_tok, topk, E, m, k, wtype, 0, Xd, Wd, idd, None, None, Y))
+            seen.append(wq.wq_get_device_status())
+            if seen[-1] == wq.WQ_ERR_DEVICE_TIMEOUT:
+                break
+    finally:
+        wq.wq_set_wait_limit(0)
+    assert wq.WQ_ERR_DEVICE_TIMEOUT in seen, seen
+    assert set(seen) <= {wq.WQ_OK, wq.WQ_ERR_DEVICE_TIMEOUT}
+    assert wq.wq_get_device_status() == wq.WQ_OK
+    wq.check(wq.wq_moe_gemv(n_tok, topk, E, m, k, wtype, 0, Xd, Wd, idd, None, None, Y))
+    status_ok()
+    q0, q1 = 300, 306  # slots of the second window
+    Yref, S = oracle_mod.moe(n_tok, topk, E, m, k, wtype, 0, X, bank, ids, slots=(q0, q1))
+    got = Y.cpu().numpy().reshape(n_tok * topk, m)
+    assert_within(got[q0:q1], Yref[q0:q1], S[q0:q1], TAU)

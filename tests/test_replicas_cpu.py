@@ -96,12 +96,19 @@ def test_algorithmic_bytes_of_the_float_gemvs(tag, wbytes):
 
 def test_traffic_record_is_dropped_when_its_source_changes(monkeypatch):
     import hashlib
-    src = "gemv_transformer_gb300/csrc/gemv_mma.cu"
-    with open(os.path.join(bench.ROOT, src), "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()
+    srcs = ["gemv_transformer_gb300/csrc/gemv_mma.cu", "gemv_transformer_gb300/csrc/tile_sched.cuh"]
+    h = hashlib.sha256()
+    for src in srcs:
+        with open(os.path.join(bench.ROOT, src), "rb") as f:
+            h.update(f.read())
     name = "a_workload"
-    monkeypatch.setitem(bench.TRAFFIC, name, {"bytes": 123, "source": src, "sha256": sha})
-    assert bench.traffic_for(name) == 123  # recorded on the source as it stands
-    monkeypatch.setitem(bench.TRAFFIC, name, {"bytes": 123, "source": src, "sha256": "0" * 64})
+    monkeypatch.setitem(bench.TRAFFIC, name, {"bytes": 123, "sources": srcs, "sha256": h.hexdigest()})
+    assert bench.traffic_for(name) == 123  # recorded on the sources as they stand
+    monkeypatch.setitem(bench.TRAFFIC, name, {"bytes": 123, "sources": srcs, "sha256": "0" * 64})
+    assert bench.traffic_for(name) is None
+    # a record on the first source alone is not one on both
+    with open(os.path.join(bench.ROOT, srcs[0]), "rb") as f:
+        one = hashlib.sha256(f.read()).hexdigest()
+    monkeypatch.setitem(bench.TRAFFIC, name, {"bytes": 123, "sources": srcs, "sha256": one})
     assert bench.traffic_for(name) is None
     assert bench.traffic_for("no_such_workload") is None
