@@ -262,7 +262,6 @@ __global__ void __launch_bounds__(BL<WT, T, KS, NH>::kThreads, 1)
     using L = BL<WT, T, KS, NH>;
     constexpr int S = L::kStages;
     constexpr int CW = L::kCW;
-    constexpr int TN = L::TN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *stages = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // swizzle atoms: 1 KB
@@ -293,6 +292,24 @@ __global__ void __launch_bounds__(BL<WT, T, KS, NH>::kThreads, 1)
     // Both B buffers start at zero: the columns of tokens >= n are never written.
     for (int i = threadIdx.x; i < 2 * L::kBufWords; i += blockDim.x) bufs[i] = 0u;
     __syncthreads();
+    // No kernel of this library writes a weight image, so the producer requests the
+    // weight boxes of its first stage before the grid-dependency wait, while the
+    // previous kernel finishes; its X follows after the wait (the stage barrier
+    // expects both).  One stage, as in the quantised GEMV: with more, the first X
+    // copy queues behind the early boxes.
+    constexpr int kEarly = 1;
+    int early = 0;  // stages whose weight boxes went out before the wait
+    if (threadIdx.x == CW * 32) {
+        const uint64_t policy = l2_evict_first();
+        for (int grp = blockIdx.x; grp < groups && early < kEarly; grp += gridDim.x)
+            for (int c = 0; c < KC && early < kEarly; ++c, ++early) {
+                uint8_t *dst = stages + (size_t)early * L::kStageBytes;
+                mbar_arrive_expect_tx(&full[early], (uint32_t)(L::kWBytes + n * kChunk * 4));
+                for (int b = 0; b < kParts; ++b)
+                    tma_load_2d(dst + b * L::kBoxBytes, &wmap, c * kChunk + b * kBoxK,
+                                grp * T * 16, &full[early], policy);
+            }
+    }
     pdl_wait();
 
     if (warp == CW) {
@@ -318,10 +335,12 @@ __global__ void __launch_bounds__(BL<WT, T, KS, NH>::kThreads, 1)
                         }
                     }
                     uint8_t *dst = stages + (size_t)s * L::kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(L::kWBytes + n * kChunk * 4));
-                    for (int b = 0; b < kParts; ++b)
-                        tma_load_2d(dst + b * L::kBoxBytes, &wmap, c * kChunk + b * kBoxK, row0,
-                                    &full[s], policy);
+                    if (q >= early) {
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(L::kWBytes + n * kChunk * 4));
+                        for (int b = 0; b < kParts; ++b)
+                            tma_load_2d(dst + b * L::kBoxBytes, &wmap, c * kChunk + b * kBoxK,
+                                        row0, &full[s], policy);
+                    }
                     for (int i = 0; i < n; ++i)
                         bulk_g2s_nohint(dst + L::kWBytes + i * kChunk * 4,
                                    a.X + (size_t)i * k + (size_t)c * kChunk, kChunk * 4, &full[s]);

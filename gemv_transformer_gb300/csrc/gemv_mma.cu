@@ -178,12 +178,6 @@ __device__ __forceinline__ void mma_f16_z(float (&d)[4], const uint32_t (&a)[4],
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
 }
 
-__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
 // acc[0..1] += (d0 * inv0, d0 * inv1) * p[0..1]; acc[2..3] += (d1 * inv0, d1 * inv1) * p[2..3].
 __device__ __forceinline__ void scale_acc(float (&acc)[4], const float (&p)[4], float d0,
                                           float d1, float inv0, float inv1) {
@@ -350,6 +344,72 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
         if (T > 2) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wm.b2)) : "memory");
         if (T > 4) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wm.b4)) : "memory");
     }
+    // The weight boxes of one stage: a full group is one tall box per NBOX (T tiles
+    // of rows); a shorter one is composed of boxes of 4, 2 and 1 tiles, each tile
+    // landing where it would in a full box.  Rows past the matrix's end are
+    // zero-filled by the TMA unit; they are computed and never stored.
+    auto issue_w = [&](uint8_t *dst, uint64_t *bar, int nt, int c, int trow, int tmat,
+                       uint64_t policy) {
+        for (int bx = 0; bx < F::NBOX; ++bx) {
+            const int x = (c * F::NBOX + bx) * (F::ROWB / 2);
+            uint8_t *bd = dst + bx * L::kBoxBytes;
+            if (nt == T) {
+                tma_load_3d(bd, &wm.full, x, trow, tmat, bar, policy);
+            } else {
+                int t0 = 0;
+                if (T > 4 && (nt & 4)) {
+                    tma_load_3d(bd, &wm.b4, x, trow, tmat, bar, policy);
+                    t0 = 4;
+                }
+                if (T > 2 && (nt & 2)) {
+                    tma_load_3d(bd + t0 * L::kTileBytes, &wm.b2, x, trow + 16 * t0, tmat, bar,
+                                policy);
+                    t0 += 2;
+                }
+                if (nt & 1)
+                    tma_load_3d(bd + t0 * L::kTileBytes, &wm.b1, x, trow + 16 * t0, tmat, bar,
+                                policy);
+            }
+        }
+    };
+    auto chunk_bytes = [&](int nt, int c, uint32_t &wbytes, uint32_t &xbytes) {
+        // X of one token for the chunk (256 or 512 floats); the group's weight rows
+        xbytes = (uint32_t)min(kBlocks * 32, k - c * kBlocks * 32) * 4u;
+        wbytes = nt == T ? (uint32_t)L::kWBytes : (uint32_t)(F::NBOX * nt * L::kTileBytes);
+    };
+    // GEMV: no kernel of this library writes a weight image, so the producer requests
+    // the weight boxes of its first stage before the grid-dependency wait, while the
+    // previous kernel finishes; its X follows after the wait (the stage barrier
+    // expects both).  One stage measured best: with all S stages the first X copy
+    // queues behind every early box (benchmark step 164.4 us with one, 164.5 with
+    // two, 166.9 with all, 167.8 with none).  MoE rows depend on the ids, which are
+    // read after the wait.
+    constexpr int kEarly = 1;
+    int early = 0;  // stages whose weight boxes went out before the wait
+    if constexpr (!MOE) {
+        __syncthreads();  // the stage barriers are initialised
+        if (threadIdx.x == kCW * 32) {
+            Sched s0;
+            s0.tpe = (m + 15) / 16;
+            s0.n_act = 1;
+            split_units<T>(s0, false, 7u);
+            const uint64_t policy = l2_evict_first();
+            for (Walk wk(s0); wk.more() && early < kEarly;) {
+                const int nt = wk.group<T>();
+                for (int p0 = 0; p0 < a.n && early < kEarly; p0 += P_MAX) {
+                    const int npass = min(P_MAX, a.n - p0);
+                    for (int c = 0; c < KC && early < kEarly; ++c, ++early) {
+                        uint32_t wbytes, xbytes;
+                        chunk_bytes(nt, c, wbytes, xbytes);
+                        mbar_arrive_expect_tx(&full[early], wbytes + npass * xbytes);
+                        issue_w(stages + (size_t)early * L::kStageBytes, &full[early], nt, c,
+                                wk.tl * 16, 0, policy);
+                    }
+                }
+                wk.advance(nt);
+            }
+        }
+    }
     pdl_wait();
     Sched sc;
     sc.tpe = (m + 15) / 16;
@@ -375,9 +435,6 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
 
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
-        // A full group is one tall box per NBOX (T tiles of rows); a shorter one is
-        // composed of boxes of 4, 2 and 1 tiles.  Rows past the matrix's end are
-        // zero-filled by the TMA unit; they are computed and never stored.
         if (lane == 0) {
             const uint64_t policy = l2_evict_first();
             long long q = *s_q;                 // stages issued so far
@@ -411,32 +468,12 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
                                 break;
                             }
                         }
-                        // X of the pass's tokens for this chunk (256 or 512 floats each).
-                        const uint32_t xbytes = (uint32_t)min(kBlocks * 32, k - c * kBlocks * 32) * 4u;
-                        const uint32_t wbytes =
-                            nt == T ? (uint32_t)L::kWBytes : (uint32_t)(F::NBOX * nt * L::kTileBytes);
-                        mbar_arrive_expect_tx(&full[s], wbytes + npass * xbytes);
+                        uint32_t wbytes, xbytes;
+                        chunk_bytes(nt, c, wbytes, xbytes);
                         uint8_t *dst = stages + (size_t)s * L::kStageBytes;
-                        for (int bx = 0; bx < F::NBOX; ++bx) {
-                            const int x = (c * F::NBOX + bx) * (F::ROWB / 2);
-                            uint8_t *bd = dst + bx * L::kBoxBytes;
-                            if (nt == T) {
-                                tma_load_3d(bd, &wm.full, x, trow, tmat, &full[s], policy);
-                            } else {  // tile tt of the group lands where it would in a full box
-                                int t0 = 0;
-                                if (T > 4 && (nt & 4)) {
-                                    tma_load_3d(bd, &wm.b4, x, trow, tmat, &full[s], policy);
-                                    t0 = 4;
-                                }
-                                if (T > 2 && (nt & 2)) {
-                                    tma_load_3d(bd + t0 * L::kTileBytes, &wm.b2, x, trow + 16 * t0,
-                                                tmat, &full[s], policy);
-                                    t0 += 2;
-                                }
-                                if (nt & 1)
-                                    tma_load_3d(bd + t0 * L::kTileBytes, &wm.b1, x, trow + 16 * t0,
-                                                tmat, &full[s], policy);
-                            }
+                        if (q >= early) {
+                            mbar_arrive_expect_tx(&full[s], wbytes + npass * xbytes);
+                            issue_w(dst, &full[s], nt, c, trow, tmat, policy);
                         }
     #pragma unroll
                         for (int i = 0; i < P_MAX; ++i)
