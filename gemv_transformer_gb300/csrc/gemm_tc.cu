@@ -510,6 +510,7 @@ size_t gemm_tc_w_workspace_bytes(int m, int k) {
 cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
                               const DeviceInfo &dev, cudaStream_t stream, bool x_ready) {
     GemmArgs g = a;
+    g.w_early = wtype == kBF16;  // else W is the bf16 copy the next kernel writes
     if (wtype != kBF16) {
         // The weights first: bf16 after X in the workspace, then the bf16 GEMM.
         uint8_t *wb = static_cast<uint8_t *>(workspace) + gemm_tc_workspace_bytes(a.n, a.k);

@@ -216,6 +216,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
         __syncthreads();
     tc_fence_after();
+    // Stage s of one operand: KS swizzle atoms of k at row y (pair mode: the copies
+    // of both CTAs complete on the even CTA's full[s]).
+    auto load_stage = [&](bool isA, int s, int kb, int y) {
+        const CUtensorMap *map = isA ? &xmap : &wmap;
+        const int atom = isA ? kAtomA : L::kBAtom;
+        const int sbytes = isA ? L::kABytes : L::kBBytes;
+        uint8_t *dst = (isA ? sA : sB) + (size_t)s * sbytes;
+        if (PAIR) {
+            if (leader) mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * sbytes));
+            const uint32_t bar = map_to_rank(&full[s], 0);
+#pragma unroll
+            for (int u = 0; u < KS; ++u)
+                tma_load_2d_pair(dst + u * atom, map, (kb * KS + u) * BK, y, bar);
+        } else {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)sbytes);
+#pragma unroll
+            for (int u = 0; u < KS; ++u)
+                tma_load_2d(dst + u * atom, map, (kb * KS + u) * BK, y, &full[s]);
+        }
+    };
+    auto row_of = [&](bool isA, int t) {
+        return isA ? (t % RB) * TM + (PAIR ? (int)rank * BM : 0)
+                   : (t / RB) * BN + (PAIR ? (int)rank * L::kBRows : 0);
+    };
+    // The caller's weights are not written by the previous kernel: the B producer
+    // requests its first stage before the grid-dependency wait, while that kernel
+    // finishes (X, which it may write, waits).
+    const bool b_early = a.w_early && nseg > 0 && kb0 < kb1;
+    if (b_early && warp == 1 && lane == 0) load_stage(false, 0, kb0, row_of(false, seg_tile(0)));
     pdl_wait();
     const uint32_t tmem = *tmem_slot;
 
@@ -224,16 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Warp 0 loads A (X rows), warp 1 loads B (W rows); KS atoms per stage.
         if (lane == 0) {
             const bool isA = warp == 0;
-            const CUtensorMap *map = isA ? &xmap : &wmap;
-            const int atom = isA ? kAtomA : L::kBAtom;
-            uint8_t *base = isA ? sA : sB;
-            const int sbytes = isA ? L::kABytes : L::kBBytes;
             long long q = 0;  // stages issued
             bool ok = true;
             for (int i = 0; i < nseg && ok; ++i) {
-                const int t = seg_tile(i);
-                const int y = isA ? (t % RB) * TM + (PAIR ? (int)rank * BM : 0)
-                                  : (t / RB) * BN + (PAIR ? (int)rank * L::kBRows : 0);
+                const int y = row_of(isA, seg_tile(i));
                 for (int kb = kb0; kb < kb1; ++kb, ++q) {
                     const int s = (int)(q % S);
                     if (q >= S && !wait_or_abort(&empty[s], (uint32_t)(((q / S) - 1) & 1),
@@ -241,20 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t *dst = base + (size_t)s * sbytes;
-                    if (PAIR) {
-                        // Copies of both CTAs complete on the even CTA's full[s].
-                        if (leader) mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * sbytes));
-                        const uint32_t bar = map_to_rank(&full[s], 0);
-#pragma unroll
-                        for (int u = 0; u < KS; ++u)
-                            tma_load_2d_pair(dst + u * atom, map, (kb * KS + u) * BK, y, bar);
-                    } else {
-                        mbar_arrive_expect_tx(&full[s], (uint32_t)sbytes);
-#pragma unroll
-                        for (int u = 0; u < KS; ++u)
-                            tma_load_2d(dst + u * atom, map, (kb * KS + u) * BK, y, &full[s]);
-                    }
+                    if (q == 0 && !isA && b_early) continue;  // issued before the wait
+                    load_stage(isA, s, kb, y);
                 }
             }
             if (!PAIR || leader) {

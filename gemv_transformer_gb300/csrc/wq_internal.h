@@ -45,6 +45,10 @@ struct GemmArgs {
     int ldy = 0;           // row stride of Y and R: m + dual
     int dual = 0;          // columns j < dual also stored as acc + bias2[j] at m + j
     const float *bias2 = nullptr;  // [dual]
+    // W is the caller's weight image (not a workspace copy written by the kernel
+    // launched just before): its first tiles may be requested before the wait for
+    // that kernel.
+    bool w_early = false;
 };
 
 struct DeviceInfo {

@@ -41,6 +41,12 @@
  *   - W is the storage-format byte image [m][row_bytes], 16-byte aligned, and its
  *     buffer must hold at least wq_weight_bytes(wtype, m, k) bytes: the format's
  *     size rounded up to a multiple of 16.  The padding is read, never used.
+ *   - W is read as constant data: a call may start reading W before the kernel
+ *     launched just before it on the same stream has finished (libwq's kernels use
+ *     programmatic dependent launch and request their first weight tiles ahead of
+ *     the wait for that kernel), so that kernel must not write W.  libwq's own
+ *     kernels never write a weight image; a weight image produced on the device
+ *     needs any other launch, an event wait or a synchronisation in between.
  *   - bias is f32 [m] (read when WQ_BIAS is set, else ignored, may be NULL).
  *   - residual is f32 [n][m] (read when WQ_RESIDUAL is set); it may equal Y, which
  *     gives the in-place "Y +=" form.  No other argument may overlap Y.
