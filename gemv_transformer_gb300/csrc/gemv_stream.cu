@@ -24,6 +24,7 @@
 // read once per window no matter how many of its slots the window holds.
 #include "wq_device.cuh"
 #include "wq_internal.h"
+#include "tile_sched.cuh"
 
 namespace wq {
 namespace {
@@ -31,7 +32,6 @@ namespace {
 constexpr int kWarps = 16;
 constexpr int kStages = 4;
 constexpr int kStageBytes = 2336;  // largest piece (2304 B) + 16 B head + 16 B tail
-constexpr int kMaxSlots = 256;
 
 // Weights per piece: Q8_0 64 blocks (2176 B), Q4_0 128 blocks (2304 B), bf16 2048 B.
 template <int WT>
@@ -61,7 +61,7 @@ constexpr size_t kSmemStages = (size_t)kWarps * kStages * kStageBytes;
 constexpr size_t kSmemBars = (size_t)kWarps * kStages * sizeof(uint64_t);
 constexpr size_t kSmemTot = (size_t)kWarps * kMaxSlots * sizeof(float);
 constexpr size_t kSmemMoe = (size_t)kMaxSlots * sizeof(unsigned long long) +  // keys
-                            (size_t)(3 * kMaxSlots + 3) * sizeof(int);
+                            (size_t)(3 * kMaxSlots + 3 + kMaxSlots / 32) * sizeof(int);
 constexpr size_t kSmemBytes = kSmemStages + kSmemBars + kSmemTot + kSmemMoe;
 
 template <int WT, bool MOE, int NT>
@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) stream_kernel(const StreamArgs
     int *s_act = s_seg + kMaxSlots + 1;                         // expert of each segment
     int *s_nact = s_act + kMaxSlots;                            // number of segments
     volatile unsigned *s_abort = reinterpret_cast<volatile unsigned *>(s_nact + 1);
+    int *s_wcnt = s_nact + 2;                                   // routing: per-warp counts
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k = a.k, m = a.m;
@@ -104,40 +105,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) stream_kernel(const StreamArgs
     for (int win = 0; win < n_win; ++win) {
         long long n_jobs;
         if (MOE) {
-            // Sort the window's slots by (expert, slot) with a rank sort; bad ids go last.
             const int base = win * kMaxSlots;
-            const int S = min(kMaxSlots, S_all - base);
-            const unsigned long long big = 1ull << 62;
-            for (int q = threadIdx.x; q < S; q += blockDim.x) {
-                const int e = a.ids[base + q];
-                const bool ok = e >= 0 && e < a.n_experts;
-                if (!ok && blockIdx.x == 0) record_status(a.status, kStBadExpert);
-                s_key[q] = ok ? ((unsigned long long)e << 16) | (unsigned)q : big | (unsigned)q;
-            }
-            __syncthreads();
-            for (int q = threadIdx.x; q < S; q += blockDim.x) {
-                const unsigned long long kq = s_key[q];
-                int r = 0;
-                for (int q2 = 0; q2 < S; ++q2) r += s_key[q2] < kq;
-                s_sorted[r] = base + q;  // the slot's global index
-            }
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                int na = 0, prev = -1, r = 0;
-                for (; r < S; ++r) {
-                    const unsigned long long kr = s_key[s_sorted[r] - base];
-                    if (kr & big) break;
-                    const int e = (int)(kr >> 16);
-                    if (e != prev) {
-                        s_seg[na] = r;
-                        s_act[na] = e;
-                        ++na;
-                        prev = e;
-                    }
-                }
-                s_seg[na] = r;
-                *s_nact = na;
-            }
+            route_window(a, base, min(kMaxSlots, S_all - base),
+                         RouteSmem{s_key, s_sorted, s_seg, s_act, s_nact, s_wcnt});
             __syncthreads();
             if (*s_abort) break;  // the same in every thread after the barrier
             n_jobs = (long long)(*s_nact) * m;

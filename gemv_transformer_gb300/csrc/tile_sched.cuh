@@ -66,7 +66,7 @@ __device__ __forceinline__ bool consumers_sync_any(bool v) {
 
 // Shared-memory tables of one routing window.
 struct RouteSmem {
-    unsigned long long *key;  // [kMaxSlots]: 64-bit keys, or 32-bit keys then their ranks
+    unsigned long long *key;  // [kMaxSlots], 16-byte aligned: 64-bit keys, or 32-bit keys then their ranks
     int *sorted;              // [kMaxSlots]: the global slot index of each rank
     int *seg;                 // [kMaxSlots + 1]: segment starts, then the valid slots' end
     int *act;                 // [kMaxSlots]: the expert of each segment
