@@ -289,3 +289,51 @@ def test_moe_bit_identical_reruns(oracle_mod, wt):
     Y1 = run_moe(oracle_mod, wt, n_tok, topk, E, m, k, BIAS, ids, 5, slots=(0, 8))
     Y2 = run_moe(oracle_mod, wt, n_tok, topk, E, m, k, BIAS, ids, 5, slots=(0, 8))
     assert (Y1.view(np.int32) == Y2.view(np.int32)).all()
+
+
+@HALF
+def test_moe_window_of_bad_ids_only(oracle_mod, wt):
+    """A first window whose 256 ids are all out of range (no segment to run) and a
+    second window of valid ids: the device status says WQ_ERR_BAD_EXPERT, the bad
+    slots' rows stay unwritten and the second window's rows are correct."""
+    n_tok, topk, E, m, k = 300, 1, 5, 40, 256
+    g = synth.rng(70 + wt)
+    bank = synth.draw_weights(g, wt, E * m, k).reshape(E, m, -1)
+    X = synth.normal_f32(g, (n_tok, k))
+    ids = g.integers(0, E, size=(n_tok, topk)).astype(np.int32)
+    ids[:256] = -3
+    out = Guarded(n_tok * topk * m)
+    wq.check(wq.wq_moe_gemv(n_tok, topk, E, m, k, wt, 0, dev(X), weights_dev(bank, wt, E * m, k),
+                            dev(ids), None, None, out.view), "wq_moe_gemv")
+    torch.cuda.synchronize()
+    assert wq.wq_get_device_status() == wq.WQ_ERR_BAD_EXPERT
+    status_ok()
+    Y = out.result().reshape(n_tok * topk, m)
+    assert (Y[:256].view(np.int32) == -1).all()
+    ids_ok = ids.copy()
+    ids_ok[:256] = 0
+    Yref, S = oracle_mod.moe(n_tok, topk, E, m, k, wt, 0, X, bank, ids_ok, slots=(256, 300))
+    assert_within(Y[256:], Yref[256:], S[256:], TAU, what="moe after a bad window")
+
+
+@HALF
+def test_moe_in_place_residual(oracle_mod, wt):
+    """residual == Y: each slot's row is read and rewritten by the same thread."""
+    n_tok, topk, E, m, k = 16, 6, 64, 140, 512
+    g = synth.rng(80 + wt)
+    bank = synth.draw_weights(g, wt, E * m, k).reshape(E, m, -1)
+    X = synth.normal_f32(g, (n_tok, k))
+    ids = synth.moe_ids(g, n_tok, topk, E)
+    bias = synth.normal_f32(g, (E, m), 0.1)
+    R = synth.normal_f32(g, (n_tok * topk, m))
+    out = Guarded(n_tok * topk * m, R)
+    flags = BIAS | GELU | RES
+    wq.check(wq.wq_moe_gemv(n_tok, topk, E, m, k, wt, flags, dev(X),
+                            weights_dev(bank, wt, E * m, k), dev(ids), dev(bias), out.view,
+                            out.view), "wq_moe_gemv")
+    torch.cuda.synchronize()
+    status_ok()
+    Y = out.result().reshape(n_tok * topk, m)
+    Yref, S = oracle_mod.moe(n_tok, topk, E, m, k, wt, flags, X, bank, ids, bias=bias, residual=R)
+    assert_within(Y, Yref, S, TAU, gelu=True, R=np.abs(R) + np.abs(bias[ids.reshape(-1)]),
+                  what="moe in-place residual")
