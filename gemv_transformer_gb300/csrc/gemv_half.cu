@@ -444,9 +444,10 @@ struct BankMaps {
 // y[s] = W[ids[s]] . x[s / topk] for every slot s, through the epilogue.  The
 // arithmetic per chunk is the GEMV kernel's (build_b, tile_chunk); around it, each
 // window of kMaxSlots slots is routed in shared memory (route_window) and the CTAs
-// walk the active experts' 16-row tiles in groups of T (never across an expert),
-// once per pass of up to eight of the expert's slots.  Output row s of Y and of the
-// residual is slot s's; bias row e of [E][m] is expert e's.
+// take the active experts' 16-row tiles in groups of T (never across an expert),
+// dealt out by cost (DealWalk), once per pass of up to eight of the expert's
+// slots.  Output row s of Y and of the residual is slot s's; bias row e of [E][m]
+// is expert e's.
 //
 // A wait that runs out sets the CTA's abort flag: the consumers leave their pass
 // together (the answer of consumers_sync_any), the producer stops issuing, no window
@@ -521,7 +522,10 @@ __global__ void __launch_bounds__(BL<WT, T, KS, 1>::kThreads, 1)
         __syncthreads();
         if (*abort_flag) break;  // the same in every thread: no one writes it here
         sc.n_act = *rs.nact;
-        split_units<T>(sc, true, 7u);
+        // the groups dealt out by cost; the experts' order takes the routing keys' space
+        int *s_order = reinterpret_cast<int *>(rs.key);
+        order_by_slots(rs.seg, sc.n_act, s_order);
+        __syncthreads();
 
         if (warp == CW) {
             // ------------------------------------------------------------ producer
@@ -531,8 +535,8 @@ __global__ void __launch_bounds__(BL<WT, T, KS, 1>::kThreads, 1)
                 int sp = (int)(qp % S);
                 uint32_t wrap = (uint32_t)((qp / S) & 1);
                 bool pok = true;
-                for (Walk wk(sc); wk.more() && pok;) {
-                    const int nt = wk.group<T>();
+                for (DealWalk<T> wk(sc, s_order); wk.more() && pok;) {
+                    const int nt = wk.template group<T>();
                     const int seg0 = rs.seg[wk.ai];
                     const int ntok = rs.seg[wk.ai + 1] - seg0;
                     const int trow = wk.tl * 16, ex = rs.act[wk.ai];
@@ -592,8 +596,8 @@ __global__ void __launch_bounds__(BL<WT, T, KS, 1>::kThreads, 1)
             __syncwarp();
         } else {
             // ------------------------------------------------------------ consumers
-            for (Walk wk(sc); wk.more() && ok;) {
-                const int nt = wk.group<T>();
+            for (DealWalk<T> wk(sc, s_order); wk.more() && ok;) {
+                const int nt = wk.template group<T>();
                 const int seg0 = rs.seg[wk.ai];
                 const int ntok = rs.seg[wk.ai + 1] - seg0;
                 const int row0 = wk.tl * 16, ex = rs.act[wk.ai];

@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
             split_units<T>(s0, false, 7u);
             const uint64_t policy = l2_evict_first();
             for (Walk wk(s0); wk.more() && early < kEarly;) {
-                const int nt = wk.group<T>();
+                const int nt = wk.template group<T>();
                 for (int p0 = 0; p0 < a.n && early < kEarly; p0 += P_MAX) {
                     const int npass = min(P_MAX, a.n - p0);
                     for (int c = 0; c < KC && early < kEarly; ++c, ++early) {
@@ -429,9 +429,21 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     __syncthreads();
     if (*abort_flag) break;  // the same in every thread after the barrier
     sc.n_act = MOE ? *s_nact : 1;
-    // (a pass over a group costs about seven tiles' worth of per-chunk work besides
-    // its tiles: measured)
-    split_units<T>(sc, MOE, 7u);
+    // GEMV: contiguous ranges of tiles.  MoE: groups dealt out by cost (DealWalk);
+    // the routing keys are no longer needed, so their space holds the experts' order.
+    int *s_order = reinterpret_cast<int *>(s_key);
+    if constexpr (MOE) {
+        order_by_slots(s_seg, sc.n_act, s_order);
+        __syncthreads();
+    } else {
+        split_units<T>(sc, false, 7u);
+    }
+    auto make_walk = [&]() {
+        if constexpr (MOE)
+            return DealWalk<T>(sc, s_order);
+        else
+            return Walk(sc);
+    };
 
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
@@ -441,8 +453,8 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
             int s = (int)(q % S);               // the next one's ring slot
             uint32_t wrap = (uint32_t)((q / S) & 1);  // and the parity of its round
             bool pok = true;
-            for (Walk wk(sc); wk.more() && pok;) {
-                const int nt = wk.group<T>();
+            for (auto wk = make_walk(); wk.more() && pok;) {
+                const int nt = wk.template group<T>();
                 const int seg0 = MOE ? s_seg[wk.ai] : 0;
                 const int ntok = MOE ? s_seg[wk.ai + 1] - seg0 : a.n;
                 const int trow = wk.tl * 16, tmat = MOE ? s_act[wk.ai] : 0;
@@ -496,8 +508,8 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
     } else {
 
     // ---------------------------------------------------------------- consumers
-    for (Walk wk(sc); wk.more() && ok;) {
-        const int ntiles = wk.group<T>();
+    for (auto wk = make_walk(); wk.more() && ok;) {
+        const int ntiles = wk.template group<T>();
         const int seg0 = MOE ? s_seg[wk.ai] : 0;
         const int ntok_all = MOE ? s_seg[wk.ai + 1] - seg0 : a.n;
         const int e = MOE ? s_act[wk.ai] : 0;
@@ -982,11 +994,24 @@ cudaError_t launch_mma_moe(const StreamArgs &a, int wtype, const DeviceInfo &dev
                            cudaStream_t stream) {
     // Two CTAs of eight consumer warps per SM, with 128-row (Q4_0) or 96-row (Q8_0)
     // groups: measured on GB300 against one CTA of sixteen warps (6 % less time for
-    // both formats at 16 tokens x top-6 of 64 experts, 1408 x 2048 each).
+    // both formats at 16 tokens x top-6 of 64 experts, 1408 x 2048 each).  Groups
+    // half as tall when at most that many active experts (the slots, or the bank)
+    // give too few full groups to go round: the fewer rounds x (tiles + 7) (a pass
+    // over a group costs about seven tiles' worth of work besides its tiles).
     const long long matrices = a.n_experts;
     const int grid = dev.sm_count * Warps<8>::kCtas;
-    return wtype == kQ4_0 ? launch_inst<kQ4_0, true, kMixed, 8, 8>(a, matrices, grid, dev, stream)
-                          : launch_inst<kQ8_0, true, kMixed, 6, 8>(a, matrices, grid, dev, stream);
+    const long long slots = (long long)a.n * a.topk;
+    const long long nact = slots < a.n_experts ? slots : a.n_experts;
+    const long long tpe = (a.m + 15) / 16;
+    auto est = [&](long long t) {
+        const long long groups = nact * ((tpe + t - 1) / t);
+        return (groups + grid - 1) / grid * (t + 7);
+    };
+    if (wtype == kQ4_0)
+        return est(4) < est(8) ? launch_inst<kQ4_0, true, kMixed, 4, 8>(a, matrices, grid, dev, stream)
+                               : launch_inst<kQ4_0, true, kMixed, 8, 8>(a, matrices, grid, dev, stream);
+    return est(3) < est(6) ? launch_inst<kQ8_0, true, kMixed, 3, 8>(a, matrices, grid, dev, stream)
+                           : launch_inst<kQ8_0, true, kMixed, 6, 8>(a, matrices, grid, dev, stream);
 }
 
 }  // namespace wq

@@ -223,6 +223,21 @@ __device__ __forceinline__ void split_units(Sched &sc, bool moe, uint32_t fixed)
     }
 }
 
+// MoE: the active experts (segment indices) by ascending slot count, ties by
+// index: order[i] is the i-th.  Every thread of the block calls it; the table is
+// complete after the caller's next __syncthreads.
+__device__ __forceinline__ void order_by_slots(const int *seg, int n_act, int *order) {
+    for (int a = threadIdx.x; a < n_act; a += blockDim.x) {
+        const int na = seg[a + 1] - seg[a];
+        int r = 0;
+        for (int b = 0; b < n_act; ++b) {
+            const int nb = seg[b + 1] - seg[b];
+            r += (nb < na) || (nb == na && b < a);
+        }
+        order[r] = a;
+    }
+}
+
 // A walk over the CTA's unit range by row groups.  The position (slot ai among
 // the active experts, tile tl within it) is advanced by addition: one division
 // when the walk starts, none per group or per chunk.
@@ -250,5 +265,41 @@ struct Walk {
         }
     }
 };
+
+// MoE: a CTA's row groups dealt out by cost.  Each active expert's tiles form gpe
+// groups of T (the last one shorter when T does not divide tpe), and a group's
+// cost grows with its expert's slot count (more or wider passes).  The groups are
+// ranked by that count (`order`, from order_by_slots) and CTA b takes ranks b,
+// 2 grid - 1 - b, 2 grid + b, ...: the rounds alternate direction, so a CTA that
+// took one of the cheapest groups of a round takes one of the dearest of the next.
+// (With fewer groups than CTAs some CTAs stay idle: the launcher picks T with that
+// in view.)  Same interface as Walk: `ai` the active expert, `tl` the group's
+// first tile.
+template <int T>
+struct DealWalk {
+    const int *order;
+    int tpe, gpe, G, b, grid, r, rank, ai, tl;
+    __device__ __forceinline__ DealWalk(const Sched &sc, const int *order_)
+        : order(order_), tpe(sc.tpe), gpe((sc.tpe + T - 1) / T), G(sc.n_act * gpe),
+          b((int)blockIdx.x), grid((int)gridDim.x), r(0) {
+        locate();
+    }
+    __device__ __forceinline__ void locate() {
+        rank = r * grid + ((r & 1) ? grid - 1 - b : b);
+        if (rank < G) {
+            const int sp = rank / gpe;
+            ai = order[sp];
+            tl = (rank - sp * gpe) * T;
+        }
+    }
+    __device__ __forceinline__ bool more() const { return rank < G; }
+    template <int TT>
+    __device__ __forceinline__ int group() const { return T < tpe - tl ? T : tpe - tl; }
+    __device__ __forceinline__ void advance(int) {
+        ++r;
+        locate();
+    }
+};
+
 
 }  // namespace wq
