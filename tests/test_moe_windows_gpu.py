@@ -74,3 +74,36 @@ def test_moe_window_edge(oracle_mod):
     g = synth.rng(977)
     ids = g.integers(0, E, size=(n_tok, topk)).astype(np.int32)
     run(oracle_mod, n_tok, topk, E, m, k, Q4_0, BIAS, ids, 978)
+
+
+@pytest.mark.parametrize("wtype,k", [(Q4_0, 256),   # tensor-core MoE (quantised)
+                                     (BF16, 256),   # tensor-core MoE (bf16)
+                                     (Q4_0, 32)])   # weight-streaming MoE
+def test_moe_bank_of_2_24_experts(oracle_mod, wtype, k):
+    """A bank of 2^24 + 5 one-row experts: expert ids no longer fit the 24 bits of
+    the compact routing key, so the window is sorted with 64-bit keys.  The bank is
+    zero but for the rows the ids select (ids near both ends of the range); the
+    oracle runs on those rows alone, with the ids renumbered."""
+    E, m, n_tok, topk = (1 << 24) + 5, 1, 5, 3
+    g = synth.rng(4242 + wtype + k)
+    ids = np.array([[0, E - 1, 7], [E - 1, 3, 1 << 23], [E - 2, 0, 5],
+                    [1 << 24, 9, E - 3], [2, (1 << 24) - 1, 11]], np.int32)
+    used = np.unique(ids)
+    small = synth.draw_weights(g, wtype, len(used) * m, k).reshape(len(used), m, -1)
+    sb = np.ascontiguousarray(small).view(np.uint8).reshape(len(used), -1)  # bytes per expert
+    bank = torch.zeros(wq.wq_weight_bytes(wtype, E * m, k), dtype=torch.uint8, device="cuda")
+    rows = bank[:E * sb.shape[1]].view(E, sb.shape[1])
+    rows[torch.from_numpy(used.astype(np.int64)).cuda()] = dev(sb)
+    X = synth.normal_f32(g, (n_tok, k))
+    out = Guarded(n_tok * topk * m)
+    wq.check(wq.wq_moe_gemv(n_tok, topk, E, m, k, wtype, 0, dev(X), bank, dev(ids), None, None,
+                            out.view), "wq_moe_gemv")
+    torch.cuda.synchronize()
+    status_ok()
+    remap = {int(e): i for i, e in enumerate(used)}
+    ids_small = np.vectorize(remap.get)(ids).astype(np.int32)
+    Yref, S = oracle_mod.moe(n_tok, topk, len(used), m, k, wtype, 0, X, small, ids_small)
+    Y = out.result().reshape(Yref.shape)
+    assert_within(Y, Yref, S, TAU, what=f"moe 2^24 experts wtype={wtype} k={k}")
+    del bank, rows
+    torch.cuda.empty_cache()
