@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
             Sched s0;
             s0.tpe = (m + 15) / 16;
             s0.n_act = 1;
-            split_units<T>(s0, false, 7u);
+            split_units(s0);
             const uint64_t policy = l2_evict_first();
             for (Walk wk(s0); wk.more() && early < kEarly;) {
                 const int nt = wk.template group<T>();
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(Warps<CW>::kThreads, Warps<CW>::kCtas)
         order_by_slots(s_seg, sc.n_act, s_order);
         __syncthreads();
     } else {
-        split_units<T>(sc, false, 7u);
+        split_units(sc);
     }
     auto make_walk = [&]() {
         if constexpr (MOE)

@@ -177,10 +177,11 @@ __device__ __forceinline__ void route_window(const StreamArgs &a, int base, int 
 // ------------------------------------------------------------ job schedule --
 //
 // Work units are 16-row tiles; GEMV: tiles 0..ceil(m/16) of the one matrix; MoE:
-// tiles of the active experts in order (expert a owns units [a*tpe, (a+1)*tpe)).
-// A CTA takes a contiguous range of units and processes it in row groups of at
-// most T tiles that never straddle an expert; every group is run once per pass
-// of the tokens that fit in one.
+// tiles of the active experts (expert a owns units [a*tpe, (a+1)*tpe)).  A CTA
+// processes its units in row groups of at most T tiles that never straddle an
+// expert, each group once per pass of the tokens that fit in one: the GEMV's CTAs
+// take contiguous ranges (split_units, Walk), the MoE's the groups dealt out by
+// cost (DealWalk).
 
 struct Sched {
     int n_act;          // MoE: active experts; GEMV: 1
@@ -188,31 +189,9 @@ struct Sched {
     long long u0, u1;   // this CTA's unit range
 };
 
-// This CTA's range of the sc.n_act * sc.tpe units.  MoE (`moe`) splits by whole
-// groups of T tiles when that is cheaper: a pass over a group costs about `fixed`
-// tiles' worth of per-chunk work besides its tiles, and a split by tiles gives a CTA
-// an extra, short group wherever its range crosses an expert's end.
-template <int T>
-__device__ __forceinline__ void split_units(Sched &sc, bool moe, uint32_t fixed) {
+// This CTA's contiguous share of the sc.n_act * sc.tpe units (the GEMV's split).
+__device__ __forceinline__ void split_units(Sched &sc) {
     const long long units = (long long)sc.n_act * sc.tpe;
-    if (moe && units * gridDim.x < (1ll << 32)) {
-        const uint32_t tpe = (uint32_t)sc.tpe, grid = gridDim.x;
-        const uint32_t gpe = (tpe + T - 1) / T;                 // groups per expert
-        const uint32_t G = (uint32_t)sc.n_act * gpe;
-        const uint32_t per_g = (G + grid - 1) / grid;
-        const uint32_t per_t = ((uint32_t)units + grid - 1) / grid;
-        const uint32_t cost_g = per_g * (fixed + T);
-        const uint32_t cost_t = ((per_t + T - 1) / T + (per_t > 1 ? 1 : 0)) * fixed + per_t;
-        if (cost_g < cost_t) {
-            auto unit_of = [&](uint32_t gi) -> long long {
-                const uint32_t e = gi / gpe;
-                return (long long)e * tpe + (long long)(gi - e * gpe) * T;
-            };
-            sc.u0 = unit_of(G * blockIdx.x / grid);
-            sc.u1 = unit_of(G * (blockIdx.x + 1) / grid);
-            return;
-        }
-    }
     if (units * gridDim.x < (1ll << 32)) {  // the usual case: 32-bit divisions
         const uint32_t uu = (uint32_t)units;
         sc.u0 = uu * blockIdx.x / gridDim.x;
