@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -334,23 +335,26 @@ cudaError_t launch_bn(const GemmArgs &a, const void *xb, const DeviceInfo &dev,
 }
 
 // X f32 -> bf16, round to nearest even (the rounding the fused path applies).
-// The copy is bound by bytes in flight: each thread first requests kXU 16-byte
-// pieces with cp.async into shared memory (no registers held while they are in
-// flight, so four CTAs of 48 KB keep ~190 KB per SM outstanding), then converts
-// its own pieces and stores them.
+// The copy is bound by bytes in flight: each thread first requests `upt` <= kXU
+// 16-byte pieces with cp.async into shared memory (no registers held while they
+// are in flight, so four CTAs of up to 48 KB keep up to ~190 KB per SM
+// outstanding), then converts its own pieces and stores them.  upt is the least
+// that covers X with four CTAs per SM, so that a small X still spreads over
+// every SM.
 constexpr int kXU = 12;
 constexpr int kXThreads = 256;
 constexpr int kXSmem = kXThreads * kXU * 16;
 __global__ void __launch_bounds__(kXThreads) x_to_bf16_kernel(const float4 *__restrict__ x,
-                                                              uint2 *__restrict__ xb, size_t n4) {
+                                                              uint2 *__restrict__ xb, size_t n4,
+                                                              int upt) {
     pdl_enter();
     extern __shared__ float4 xs[];
-    const size_t per_cta = (size_t)kXThreads * kXU;
+    const size_t per_cta = (size_t)kXThreads * upt;
     for (size_t base = (size_t)blockIdx.x * per_cta; base < n4; base += (size_t)gridDim.x * per_cta) {
 #pragma unroll
         for (int u = 0; u < kXU; ++u) {
             const size_t i = base + (size_t)u * kXThreads + threadIdx.x;
-            if (i < n4)
+            if (u < upt && i < n4)
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
                                  smem_addr(&xs[u * kXThreads + threadIdx.x])),
                              "l"(x + i)
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(kXThreads) x_to_bf16_kernel(const float4 *__re
 #pragma unroll
         for (int u = 0; u < kXU; ++u) {
             const size_t i = base + (size_t)u * kXThreads + threadIdx.x;
-            if (i < n4) {
+            if (u < upt && i < n4) {
                 const float4 v = xs[u * kXThreads + threadIdx.x];
                 xb[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
             }
@@ -557,16 +561,18 @@ cudaError_t launch_gemm_tc_ws(const GemmArgs &a, int wtype, void *workspace,
     }
     if (!x_ready) {  // else the workspace already holds bf16 X (e.g. a fused LayerNorm)
         const size_t n4 = (size_t)a.n * a.k / 4;
-        const size_t per_cta = (size_t)kXThreads * kXU;
-        long long blocks = (long long)((n4 + per_cta - 1) / per_cta);
         const long long cap = (long long)dev.sm_count * 4;  // resident at once
+        const size_t round = (size_t)cap * kXThreads;          // float4s per piece per thread
+        const int upt = (int)std::min<size_t>(kXU, std::max<size_t>(1, (n4 + round - 1) / round));
+        const size_t per_cta = (size_t)kXThreads * upt;
+        long long blocks = (long long)((n4 + per_cta - 1) / per_cta);
         if (blocks > cap) blocks = cap;
         static std::atomic<unsigned long long> smem_set{0};
         cudaError_t err = ensure_smem(x_to_bf16_kernel, kXSmem, dev, smem_set);
         if (err != cudaSuccess) return err;
         err = launch_pdl(x_to_bf16_kernel, dim3((unsigned)blocks), dim3(kXThreads), kXSmem, stream,
                          reinterpret_cast<const float4 *>(a.X),
-                         reinterpret_cast<uint2 *>(workspace), n4);
+                         reinterpret_cast<uint2 *>(workspace), n4, upt);
         if (err != cudaSuccess) return err;
     }
     if (gemm_tcp_supported(g)) return launch_gemm_tcp(g, workspace, dev, stream);
